@@ -1,0 +1,390 @@
+"""Benchmark of the MoE FFN forward pass on GB300.
+
+One step = one whole layer forward (route -> permute -> grouped gate/up+SwiGLU
+-> grouped down -> shared MLP -> combine) over one batch of synthetic tokens,
+through moe_layer_forward.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   (the fp64 CPU oracle on a sample)
+
+Timing: W untimed warm-up steps, then K timed steps, each preceded by an L2
+flush (a 256 MiB device write outside the timed interval); CUDA events on the
+launching stream; barrier + synchronize around the timed region; max over
+ranks.  Multi-GPU runs are independent replicas (every token is independent;
+the layer has no exchange step without expert parallelism), so scaling is weak.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "qwen3-30b-a3b-shape-T4096"
+METRIC = "MoE layer tokens/s and grouped-GEMM TFLOP/s (% bf16 peak) on 1 GB300"
+
+# dram__bytes_read.sum + dram__bytes_write.sum of one gate/up grouped-GEMM
+# launch, from an ncu capture, keyed by workload; valid only while the kernel
+# source hashes to the recorded value.
+NCU_TRAFFIC = {}
+
+
+def _kernel_hash() -> str:
+    p = os.path.join(ROOT, "mixture_experts_ffn_04_gb300", "csrc", "gemm_tc.cu")
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=float(d["hbm_gbs"]), bf16=float(d["bf16_tflops"]),
+                    bf16_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def _dist():
+    n = int(os.environ.get("WORLD_SIZE", "1"))
+    if n > 1:
+        import torch.distributed as dist
+        if not dist.is_initialized():
+            dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        return dist, dist.get_rank(), n
+    return None, 0, 1
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            out, _ = self.p.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+            out, _ = self.p.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [c.strip() for c in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def algorithmic(wl, counts: np.ndarray):
+    """Algorithmic FLOPs and bytes of the gate/up GEMM and of the whole layer
+    (touched experts only, each weight byte once, activations once)."""
+    b = wl.esize
+    T, H, I, k, Ish = wl.T, wl.H, wl.I, wl.k, wl.I_sh
+    touched = int((counts > 0).sum())
+    rows = T * k
+    gu_flops = 4.0 * rows * H * I
+    gu_bytes = touched * 2.0 * I * H * b + rows * H * b + rows * I * b
+    dn_flops = 2.0 * rows * H * I
+    layer_flops = wl.flops()
+    layer_bytes = (touched * 3.0 * I * H * b + 3.0 * Ish * H * b + T * H * b * 2
+                   + (wl.E + (1 if wl.shared_gate else 0)) * H * b)
+    return dict(gu_flops=gu_flops, gu_bytes=gu_bytes, dn_flops=dn_flops,
+                gemm_flops=gu_flops + dn_flops + 6.0 * T * H * Ish,
+                layer_flops=layer_flops, layer_bytes=layer_bytes, touched=touched)
+
+
+def oracle_sample_rate(wl, inputs_dev, target_s: float, threads: int, max_tokens=None):
+    """tokens/s of the fp64 oracle (routing + expert FFNs + combine) on a
+    seeded token sample sized to take about target_s seconds."""
+    from oracle import oracle as O
+    hin = {k: (v.cpu() if isinstance(v, torch.Tensor) else v) for k, v in inputs_dev.items()
+           if k in ("x", "w_router", "routes_idx", "routes_w", "sh_gate", "sh_up", "sh_down")}
+    wg, wu, wd = inputs_dev["w_gate"], inputs_dev["w_up"], inputs_dev["w_down"]
+    big = wg.numel() * wg.element_size() * 3 > (8 << 30)
+    rng = np.random.Generator(np.random.PCG64(99))
+
+    def run(n):
+        tokens = np.sort(rng.choice(wl.T, size=n, replace=False))
+        t0 = time.perf_counter()
+        r = O.route(wl, hin, tokens, nthreads=threads)
+        t_route = time.perf_counter() - t0
+        idx = r["idx"]
+        # staging the weights on the host is input preparation, not oracle work
+        if big:   # keep host memory bounded: only the experts the sample uses
+            used = np.unique(idx)
+            sel = torch.as_tensor(used, device=wg.device)
+            g, u, d = (t.index_select(0, sel).cpu() for t in (wg, wu, wd))
+            remap = np.zeros(wl.E, np.int32)
+            remap[used] = np.arange(len(used), dtype=np.int32)
+            idx = remap[idx]
+        else:
+            g, u, d = wg.cpu(), wu.cpu(), wd.cpu()
+        t1 = time.perf_counter()
+        O.moe_ffn(hin["x"], idx, r["weights"], r["gate"], g, u, d, hin.get("sh_gate"),
+                  hin.get("sh_up"), hin.get("sh_down"), tokens=tokens, nthreads=threads)
+        return n, t_route + (time.perf_counter() - t1)
+
+    n0 = min(wl.T, 8)
+    n, dt = run(n0)
+    per = dt / n
+    n1 = int(max(1, min(wl.T if max_tokens is None else max_tokens, target_s / max(per, 1e-9))))
+    if n1 > n0:
+        n, dt = run(n1)
+    return n / dt, n, dt
+
+
+def run_reference(args, wl, rank, world):
+    """--impl reference: the fp64 CPU oracle as it stands, on bounded samples."""
+    if rank != 0:
+        return
+    from oracle import oracle as O
+    O.load()
+    threads = os.cpu_count() or 1
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inputs = _make_inputs(wl, dev)
+    per_step_s = max(1.0, min(8.0, 150.0 / max(1, args.steps + args.warmup)))
+    _, n, dt = oracle_sample_rate(wl, inputs, per_step_s, threads)
+    times = []
+    for i in range(args.warmup + args.steps):
+        _, n_i, dt_i = oracle_sample_rate(wl, inputs, per_step_s, threads, max_tokens=n)
+        if i >= args.warmup:
+            times.append(dt_i / n_i)
+    sec_per_token = statistics.mean(times)
+    value = 1.0 / sec_per_token
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * sec_per_token * wl.T, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": _config(wl),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": "%d seeded tokens of the workload per step (routing + "
+                                   "expert FFNs + combine, fp64)" % n},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def _config(wl):
+    return {"workload": wl.name, "tokens": wl.T, "hidden": wl.H, "experts": wl.E,
+            "top_k": wl.k, "moe_inter": wl.I, "shared_inter": wl.I_sh,
+            "shared_gate": wl.shared_gate, "norm_topk": wl.norm_topk, "routing": wl.routing,
+            "l2": "flushed before every timed step (256 MiB device write)",
+            "description": wl.description}
+
+
+def _make_inputs(wl, device):
+    from mixture_experts_ffn_04_gb300 import workloads as W
+    return W.make_inputs(wl, seed=0, device=device)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from mixture_experts_ffn_04_gb300 import workloads as W
+    wl = W.get(args.workload)
+    dist, rank, world = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+
+    if args.impl == "reference":
+        run_reference(args, wl, rank, world)
+        if dist is not None:
+            dist.barrier()
+        return
+
+    import mixture_experts_ffn_04_gb300 as m
+    m.lib()
+    peaks = _peaks()
+    inputs = _make_inputs(wl, "cuda")
+    layer = m.MoELayer(wl, inputs)
+    x = inputs["x"]
+    ridx, rw = inputs.get("routes_idx"), inputs.get("routes_w")
+    y = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    nst = len(m.STAGES)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)]
+              for _ in range(args.steps)]
+    for evs in events:
+        for e in evs:
+            e.record(stream)   # materialise the CUDA events
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        layer.forward(x, y, ridx, rw)
+    torch.cuda.synchronize()
+    st, bits = layer.device_status()
+    if st != m.MOE_OK:
+        raise RuntimeError("device status %d (bits %#x) after warm-up" % (st, bits))
+    launches_per_step = m.moe_last_launch_count()
+
+    clocks = Clocks(local)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(1)
+        m.moe_layer_forward_traced(layer.shape, layer.weights, x, ridx, rw, y, layer.ws,
+                                   events[i], stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    st, bits = layer.device_status()
+    if st != m.MOE_OK:
+        raise RuntimeError("device status %d (bits %#x) in the timed region" % (st, bits))
+
+    step_ms = [events[i][0].elapsed_time(events[i][nst]) for i in range(args.steps)]
+    stage_ms = [statistics.mean(events[i][s].elapsed_time(events[i][s + 1])
+                                for i in range(args.steps)) for s in range(nst)]
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * wl.T / (ms_per_step / 1000.0)
+
+    # ---- end to end through the public API, host buffers -------------------
+    x_host = x.cpu().pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    ridx_h = ridx.cpu().pin_memory() if ridx is not None else None
+    rw_h = rw.cpu().pin_memory() if rw is not None else None
+    xd, yd = torch.empty_like(x), torch.empty_like(x)
+    rid = torch.empty_like(ridx) if ridx is not None else None
+    rwd = torch.empty_like(rw) if rw is not None else None
+    e2e_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.fill_(1)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        xd.copy_(x_host, non_blocking=True)
+        if rid is not None:
+            rid.copy_(ridx_h, non_blocking=True)
+            rwd.copy_(rw_h, non_blocking=True)
+        layer.forward(xd, yd, rid, rwd)
+        y_host.copy_(yd, non_blocking=True)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= args.warmup:
+            e2e_ms.append(e0.elapsed_time(e1))
+    h2d = x.numel() * x.element_size() + (0 if ridx is None else
+                                            ridx.numel() * 4 + rw.numel() * 4)
+    d2h = y.numel() * y.element_size()
+    e2e_val = world * wl.T / (statistics.mean(e2e_ms) / 1000.0)
+
+    # ---- roofline of the dominant kernel (gate/up grouped GEMM) -------------
+    counts = layer.views()["counts"].cpu().numpy()
+    alg = algorithmic(wl, counts)
+    gu_ms = stage_ms[m.STAGES.index("gate_up")]
+    t_flop = alg["gu_flops"] / (peaks["bf16"] * 1e12)
+    t_byte = alg["gu_bytes"] / (peaks["hbm"] * 1e9)
+    if t_flop >= t_byte:
+        ach = alg["gu_flops"] / (gu_ms / 1000.0) / 1e12
+        roof = {"bound": "tensor", "achieved": ach, "peak": peaks["bf16"], "unit": "TFLOP/s",
+                "frac": ach / peaks["bf16"]}
+    else:
+        ach = alg["gu_bytes"] / (gu_ms / 1000.0) / 1e9
+        roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s",
+                "frac": ach / peaks["hbm"]}
+    tr = NCU_TRAFFIC.get(wl.name)
+    roof["traffic"] = tr["bytes"] if tr and tr.get("kernel_hash") == _kernel_hash() else None
+    roof["kernel"] = "tc_gemm_kernel (gate/up grouped GEMM + SwiGLU)"
+    roof["peak_source"] = peaks["source"] + (" burst" if roof["bound"] == "tensor" else " copy")
+    roof["algorithmic_per_launch"] = alg["gu_flops"] if roof["bound"] == "tensor" else alg["gu_bytes"]
+    dn_ms = stage_ms[m.STAGES.index("down")]
+    sh_ms = stage_ms[m.STAGES.index("shared")]
+    gemm_ms = gu_ms + dn_ms + sh_ms
+    gemm_tflops = alg["gemm_flops"] / (gemm_ms / 1000.0) / 1e12
+    layer_roof_ms = 1000.0 * max(alg["layer_flops"] / (peaks["bf16"] * 1e12),
+                                 alg["layer_bytes"] / (peaks["hbm"] * 1e9))
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": _config(wl),
+        "grouped_gemm_tflops": gemm_tflops,
+        "grouped_gemm_frac_bf16_peak": gemm_tflops / peaks["bf16"],
+        "layer_roofline_frac": layer_roof_ms / ms_per_step,
+        "stage_ms": dict(zip(m.STAGES, stage_ms)),
+        "roofline": roof,
+        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+        "wall_s_timed_region": t_wall,
+        "experts_touched": alg["touched"],
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import oracle as O
+        O.load()
+        threads = os.cpu_count() or 1
+        rate, n, dt = oracle_sample_rate(wl, inputs, 12.0, threads)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": threads,
+                                "kind": "oracle",
+                                "sample": "%d seeded tokens of the workload (routing + expert "
+                                          "FFNs + combine in fp64), %.1f s" % (n, dt)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,82 @@
+// combine.cu -- route-weighted gather-combine plus the shared-expert add.
+//
+//   y[t] = g_t * shared_out[t] + sum_s w[t, s] * y_perm[scatter_index[t, s]]
+//
+// "Fused MoE Kernel Notes", Scatter/gather layout (moe_gather sums the routed
+// expert outputs back to [tokens, hidden]); the Spyre adapter's decode path
+// forms the same sum as a reduction over the K axis, and warns that a
+// read-modify-write scatter-add is wrong when slots repeat an index.  So this
+// is a gather: one block per token reads its k rows (and the shared row) and
+// writes y[t] once; duplicate routes are just two reads of two rows.
+// fp32 accumulation in slot order, one rounding at the store.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+template <typename T>
+__global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y_perm,
+                                                      const int32_t* __restrict__ sidx,
+                                                      const float* __restrict__ w, int k, int H,
+                                                      const T* __restrict__ shared_out,
+                                                      const float* __restrict__ gate,
+                                                      T* __restrict__ y) {
+  extern __shared__ int32_t sm[];
+  int32_t* rows = sm;                                    // [k]
+  float* wt = reinterpret_cast<float*>(sm + k);          // [k]
+  const int64_t t = blockIdx.x;
+  for (int s = threadIdx.x; s < k; s += blockDim.x) {
+    rows[s] = sidx[t * k + s];
+    wt[s] = w[t * k + s];
+  }
+  __syncthreads();
+  const float g = gate ? gate[t] : 1.0f;
+  constexpr int V = 16 / sizeof(T);
+  const int nvec = H / V;
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    float acc[V];
+#pragma unroll
+    for (int i = 0; i < V; ++i) acc[i] = 0.f;
+    for (int s = 0; s < k; ++s) {
+      const int r = rows[s];
+      if (r < 0) continue;  // pair dropped for an out-of-range route
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(y_perm + (int64_t)r * H) + v);
+      float f[V];
+      unpack16(u, f, (const T*)nullptr);
+      const float ws = wt[s];
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] = fmaf(ws, f[i], acc[i]);
+    }
+    if (shared_out) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(shared_out + t * H) + v);
+      float f[V];
+      unpack16(u, f, (const T*)nullptr);
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] = fmaf(g, f[i], acc[i]);
+    }
+    reinterpret_cast<uint4*>(y + t * H)[v] = pack16(acc, (const T*)nullptr);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* scatter_index,
+                           const float* topk_w, const void* shared_out, const float* gate,
+                           void* y, cudaStream_t st) {
+  if (s.T == 0) return cudaSuccess;
+  const size_t smem = (size_t)s.k * 8;
+  if (s.dtype == MOE_F32) {
+    combine_kernel<float><<<(unsigned)s.T, 128, smem, st>>>(
+        reinterpret_cast<const float*>(y_perm), scatter_index, topk_w, s.k, s.H,
+        reinterpret_cast<const float*>(shared_out), gate, reinterpret_cast<float*>(y));
+  } else {
+    combine_kernel<bf16><<<(unsigned)s.T, 128, smem, st>>>(
+        reinterpret_cast<const bf16*>(y_perm), scatter_index, topk_w, s.k, s.H,
+        reinterpret_cast<const bf16*>(shared_out), gate, reinterpret_cast<bf16*>(y));
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,307 @@
+// gemm_simt.cu -- grouped GEMM on the CUDA cores (fp32 FMA), and the device
+// tile schedule shared with the tensor-core engine.
+//
+// Grouped GEMM as in "Fused MoE Kernel Notes" (group_gemm_same_nk: same N and
+// K for every expert, M varies per expert): for group g, rows r in
+// [offsets[g], offsets[g+1]) of A, out[r, n] = sum_k A[r, k] * B_g[n, k].
+// The m-tile schedule is built on the device from the real group sizes, so
+// the launch bound never truncates a group (the max_M invariant of that page:
+// a bound of `tokens` rows would miss rows of a duplicate-routed group).
+//
+// This engine serves the fp32 layer exactly (tensor cores would round fp32
+// operands to tf32) and small bf16 problems.
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+// sched[g] = sum over g' < g of ceil(count_g' / bm); sched[G] = total m-tiles,
+// forced to 0 (nothing runs) when the offsets are inconsistent or exceed the
+// caller's row bound.
+__global__ void schedule_kernel(const int32_t* __restrict__ offsets, int G, int64_t single_rows,
+                                int64_t rows_bound, int bm, int32_t* __restrict__ sched,
+                                uint32_t* flags) {
+  __shared__ int32_t warp_tot[32];
+  __shared__ int32_t carry;
+  __shared__ int bad;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
+  if (tid == 0) {
+    carry = 0;
+    bad = 0;
+    if (offsets) {
+      if (offsets[0] != 0 || (int64_t)offsets[G] > rows_bound || offsets[G] < 0) bad = 1;
+    } else if (single_rows > rows_bound || single_rows < 0) {
+      bad = 1;
+    }
+  }
+  __syncthreads();
+  for (int base = 0; base < G; base += blockDim.x) {
+    const int g = base + tid;
+    int v = 0;
+    if (g < G) {
+      int64_t cnt = offsets ? (int64_t)offsets[g + 1] - offsets[g] : single_rows;
+      if (cnt < 0) {
+        bad = 1;
+        cnt = 0;
+      }
+      v = (int)((cnt + bm - 1) / bm);
+    }
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      int w = lane < nw ? warp_tot[lane] : 0;
+      int wi = w;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        int t = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += t;
+      }
+      if (lane < nw) warp_tot[lane] = wi - w;  // exclusive prefix of warp totals
+    }
+    __syncthreads();
+    if (g < G) sched[g] = carry + warp_tot[wid] + incl - v;
+    __syncthreads();
+    if (tid == blockDim.x - 1) carry += warp_tot[wid] + incl;
+    __syncthreads();
+  }
+  if (tid == 0) {
+    if (bad) set_flag(flags, kFlagRows);
+    sched[G] = bad ? 0 : carry;
+  }
+}
+
+cudaError_t launch_schedule(const GemmArgs& a, int bm, cudaStream_t st) {
+  schedule_kernel<<<1, 256, 0, st>>>(a.offsets, a.G, a.single_rows, a.rows_bound, bm, a.sched,
+                                     a.flags);
+  count_launch();
+  return cudaGetLastError();
+}
+
+// Group g and m-tile of linear m-tile j (sched non-decreasing, j < sched[G]).
+__device__ __forceinline__ int find_group(const int32_t* sched, int G, int j) {
+  int lo = 0, hi = G;
+  while (hi - lo > 1) {
+    int mid = (lo + hi) >> 1;
+    if (sched[mid] <= j) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+namespace {
+constexpr int kBN = 64, kBK = 16, kThreads = 256;
+
+template <typename T, int MODE, int BM>
+__global__ void __launch_bounds__(kThreads) simt_gemm_kernel(GemmArgs a) {
+  constexpr int TM = BM / 16;  // rows per thread
+  __shared__ __align__(16) float As[kBK][BM + 4];
+  __shared__ __align__(16) float Bs[kBK][kBN + 4];
+  __shared__ __align__(16) float Us[MODE == kSwiGLU ? kBK : 1][kBN + 4];
+
+  const int total = a.sched[a.G];
+  const int j = blockIdx.x;
+  if (j >= total) return;
+  const int g = find_group(a.sched, a.G, j);
+  const int64_t gbeg = a.offsets ? a.offsets[g] : 0;
+  const int64_t gend = a.offsets ? a.offsets[g + 1] : a.single_rows;
+  const int64_t row0 = gbeg + (int64_t)(j - a.sched[g]) * BM;
+  const int n0 = blockIdx.y * kBN;
+  const int K = a.K, N = a.N;
+
+  const T* A = reinterpret_cast<const T*>(a.A);
+  const T* B0 = reinterpret_cast<const T*>(a.B0) + (int64_t)g * a.bstride;
+  const T* B1 = MODE == kSwiGLU ? reinterpret_cast<const T*>(a.B1) + (int64_t)g * a.bstride : nullptr;
+
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  float acc[TM][4], accu[MODE == kSwiGLU ? TM : 1][4];
+#pragma unroll
+  for (int i = 0; i < TM; ++i)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      acc[i][q] = 0.f;
+      if (MODE == kSwiGLU) accu[i][q] = 0.f;
+    }
+
+  for (int k0 = 0; k0 < K; k0 += kBK) {
+    for (int e = tid; e < BM * kBK; e += kThreads) {
+      const int r = e / kBK, kk = e % kBK;
+      const int64_t row = row0 + r;
+      float v = 0.f;
+      if (row < gend && k0 + kk < K) v = to_f(A[row * K + k0 + kk]);
+      As[kk][r] = v;
+    }
+    for (int e = tid; e < kBN * kBK; e += kThreads) {
+      const int n = e / kBK, kk = e % kBK;
+      float v = 0.f, u = 0.f;
+      if (n0 + n < N && k0 + kk < K) {
+        v = to_f(B0[(int64_t)(n0 + n) * K + k0 + kk]);
+        if (MODE == kSwiGLU) u = to_f(B1[(int64_t)(n0 + n) * K + k0 + kk]);
+      }
+      Bs[kk][n] = v;
+      if (MODE == kSwiGLU) Us[kk][n] = u;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < kBK; ++kk) {
+      float av[TM], bv[4], uv[4];
+#pragma unroll
+      for (int i = 0; i < TM; ++i) av[i] = As[kk][ty * TM + i];
+      const float4 b4 = *reinterpret_cast<const float4*>(&Bs[kk][tx * 4]);
+      bv[0] = b4.x; bv[1] = b4.y; bv[2] = b4.z; bv[3] = b4.w;
+      if (MODE == kSwiGLU) {
+        const float4 u4 = *reinterpret_cast<const float4*>(&Us[kk][tx * 4]);
+        uv[0] = u4.x; uv[1] = u4.y; uv[2] = u4.z; uv[3] = u4.w;
+      }
+#pragma unroll
+      for (int i = 0; i < TM; ++i)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[i][q] = fmaf(av[i], bv[q], acc[i][q]);
+          if (MODE == kSwiGLU) accu[i][q] = fmaf(av[i], uv[q], accu[i][q]);
+        }
+    }
+    __syncthreads();
+  }
+
+#pragma unroll
+  for (int i = 0; i < TM; ++i) {
+    const int64_t row = row0 + ty * TM + i;
+    if (row >= gend) continue;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int n = n0 + tx * 4 + q;
+      if (n >= N) continue;
+      if (MODE == kStoreF32) {
+        reinterpret_cast<float*>(a.out)[row * a.ldo + n] = acc[i][q];
+      } else if (MODE == kStoreAct) {
+        reinterpret_cast<T*>(a.out)[row * a.ldo + n] = from_f<T>(acc[i][q]);
+      } else {
+        reinterpret_cast<T*>(a.out)[row * a.ldo + n] = from_f<T>(silu_f(acc[i][q]) * accu[i][q]);
+      }
+    }
+  }
+}
+
+template <typename T, int BM>
+cudaError_t launch_t(const GemmArgs& a, cudaStream_t st) {
+  int64_t mt_bound = a.offsets ? (a.rows_bound + BM - 1) / BM + a.G
+                               : (a.single_rows + BM - 1) / BM;
+  if (mt_bound <= 0 || a.N <= 0) return cudaSuccess;
+  if (mt_bound > 0x7fffffff) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)mt_bound, (unsigned)((a.N + kBN - 1) / kBN));
+  switch (a.mode) {
+    case kSwiGLU: simt_gemm_kernel<T, kSwiGLU, BM><<<grid, kThreads, 0, st>>>(a); break;
+    case kStoreAct: simt_gemm_kernel<T, kStoreAct, BM><<<grid, kThreads, 0, st>>>(a); break;
+    default: simt_gemm_kernel<T, kStoreF32, BM><<<grid, kThreads, 0, st>>>(a); break;
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Skinny engine for decode-sized groups (a few rows per expert): the cost is
+// reading each weight row once, so one warp owns one output column n of an
+// m-tile of up to 8 rows, streams B_g[n, :] with 16-byte loads and dots it
+// with each row of A (L1-resident, shared by the block's 8 warps).
+// ---------------------------------------------------------------------------
+namespace {
+constexpr int kSkR = 8;
+
+template <typename T, int MODE>
+__global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a) {
+  const int total = a.sched[a.G];
+  const int j = blockIdx.x;
+  if (j >= total) return;
+  const int g = find_group(a.sched, a.G, j);
+  const int64_t gbeg = a.offsets ? a.offsets[g] : 0;
+  const int64_t gend = a.offsets ? a.offsets[g + 1] : a.single_rows;
+  const int64_t row0 = gbeg + (int64_t)(j - a.sched[g]) * kSkR;
+  const int nrows = (int)min((int64_t)kSkR, gend - row0);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.y * 8 + warp;
+  if (n >= a.N) return;
+  const int K = a.K;
+  constexpr int V = 16 / sizeof(T);
+  const T* A = reinterpret_cast<const T*>(a.A) + row0 * K;
+  const T* B0 = reinterpret_cast<const T*>(a.B0) + (int64_t)g * a.bstride + (int64_t)n * K;
+  const T* B1 = MODE == kSwiGLU
+                    ? reinterpret_cast<const T*>(a.B1) + (int64_t)g * a.bstride + (int64_t)n * K
+                    : nullptr;
+  float acc[kSkR], accu[kSkR];
+#pragma unroll
+  for (int r = 0; r < kSkR; ++r) acc[r] = accu[r] = 0.f;
+  for (int c = lane; c < K / V; c += 32) {
+    float w[V], u[V];
+    unpack16(__ldg(reinterpret_cast<const uint4*>(B0) + c), w, (const T*)nullptr);
+    if (MODE == kSwiGLU) unpack16(__ldg(reinterpret_cast<const uint4*>(B1) + c), u, (const T*)nullptr);
+#pragma unroll
+    for (int r = 0; r < kSkR; ++r) {
+      if (r < nrows) {
+        float xa[V];
+        unpack16(__ldg(reinterpret_cast<const uint4*>(A + (int64_t)r * K) + c), xa, (const T*)nullptr);
+#pragma unroll
+        for (int i = 0; i < V; ++i) {
+          acc[r] = fmaf(w[i], xa[i], acc[r]);
+          if (MODE == kSwiGLU) accu[r] = fmaf(u[i], xa[i], accu[r]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int r = 0; r < kSkR; ++r) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
+      if (MODE == kSwiGLU) accu[r] += __shfl_xor_sync(0xffffffffu, accu[r], o);
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int r = 0; r < kSkR; ++r) {
+      if (r >= nrows) break;
+      const int64_t o = (row0 + r) * a.ldo + n;
+      if (MODE == kStoreF32) reinterpret_cast<float*>(a.out)[o] = acc[r];
+      else if (MODE == kStoreAct) reinterpret_cast<T*>(a.out)[o] = from_f<T>(acc[r]);
+      else reinterpret_cast<T*>(a.out)[o] = from_f<T>(silu_f(acc[r]) * accu[r]);
+    }
+  }
+}
+
+template <typename T>
+cudaError_t launch_skinny_t(const GemmArgs& a, cudaStream_t st) {
+  const int64_t mt_bound = a.offsets ? (a.rows_bound + kSkR - 1) / kSkR + a.G
+                                     : (a.single_rows + kSkR - 1) / kSkR;
+  if (mt_bound <= 0 || a.N <= 0) return cudaSuccess;
+  if (mt_bound > 0x7fffffff) return cudaErrorInvalidValue;
+  dim3 grid((unsigned)mt_bound, (unsigned)((a.N + 7) / 8));
+  switch (a.mode) {
+    case kSwiGLU: skinny_kernel<T, kSwiGLU><<<grid, 256, 0, st>>>(a); break;
+    case kStoreAct: skinny_kernel<T, kStoreAct><<<grid, 256, 0, st>>>(a); break;
+    default: skinny_kernel<T, kStoreF32><<<grid, 256, 0, st>>>(a); break;
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t st) {
+  if (a.K % (a.dtype == MOE_F32 ? 4 : 8) != 0) return cudaErrorInvalidValue;
+  cudaError_t e = launch_schedule(a, kSkR, st);
+  if (e != cudaSuccess) return e;
+  return a.dtype == MOE_F32 ? launch_skinny_t<float>(a, st) : launch_skinny_t<bf16>(a, st);
+}
+
+cudaError_t launch_gemm_simt(const GemmArgs& a, int bm, cudaStream_t st) {
+  cudaError_t e = launch_schedule(a, bm, st);
+  if (e != cudaSuccess) return e;
+  if (a.dtype == MOE_F32) return bm == 16 ? launch_t<float, 16>(a, st) : launch_t<float, 64>(a, st);
+  return bm == 16 ? launch_t<bf16, 16>(a, st) : launch_t<bf16, 64>(a, st);
+}
+
+}  // namespace moe

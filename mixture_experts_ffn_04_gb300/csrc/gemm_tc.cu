@@ -1,0 +1,495 @@
+// gemm_tc.cu -- grouped bf16 GEMM on the 5th-generation tensor cores.
+//
+// Same contract as the CUDA-core engine ("Fused MoE Kernel Notes",
+// group_gemm_same_nk: per-expert groups of rows with shared N and K; the
+// m-tile schedule comes from the real group sizes, never from the token count).
+//
+// Design (one CTA per SM, persistent over a device-built tile list):
+//   warp 0     TMA producer: A tile [128 rows x 64 k] from the grouped
+//              activations (2-D tensor map), B tile [256 rows x 64 k] from the
+//              expert-major weights (3-D tensor map {k, n, expert}); both in
+//              the 128-byte swizzled K-major layout the MMA reads directly.
+//   warp 1     TMEM owner and MMA issuer: one thread issues
+//              tcgen05.mma.cta_group::1.kind::f16 (M=128, N=256, K=16, bf16 in,
+//              fp32 accumulate in TMEM), 4 per 64-wide k-block, and commits to
+//              the stage's "empty" barrier; two 256-column accumulators
+//              alternate so the epilogue of tile i overlaps the MMAs of i+1.
+//   warps 2-5  epilogue: tcgen05.ld of 32 columns at a time, one TMEM lane
+//              (= one output row) per thread, fused SwiGLU / rounding, masked
+//              stores of the rows that belong to the tile's group.
+// For SwiGLU the B tile stacks 128 gate rows over the same 128 up rows, so one
+// N=256 MMA produces both halves: columns 0-127 gate, 128-255 up.
+//
+// Every mbarrier wait is bounded (about 2 s of SM clocks); a wait that runs out
+// raises the kernel's abort flag, the other roles leave their loops, in-flight
+// TMA loads and MMAs are waited for (bounded), TMEM is released and the
+// device status word gets the timeout bit.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace tc {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+// kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
+// B bf16 (10-12 = 1), both K-major (15, 16 = 0), N >> 3 at 17-22, M >> 4 at 24-28.
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
+                           ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+constexpr long long kWaitCycles = 4000000000LL;
+
+struct TcArgs {
+  int mode, N, K, G, NT, KB;
+  const int32_t* offsets;
+  int64_t single_rows;
+  const int32_t* sched;
+  void* out;
+  int64_t ldo;
+  uint32_t* flags;
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase of `parity` to complete; false on timeout or when
+// another role has aborted.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void mbar_wait_quiet(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1,
+                                            int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor for a K-major tile stored as 128-byte rows
+// with the 128-byte swizzle (8-row core groups 1024 bytes apart).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);  // start address
+  d |= (uint64_t)1 << 16;                    // leading byte offset (unused when swizzled)
+  d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;                    // descriptor version
+  d |= (uint64_t)2 << 61;                    // 128-byte swizzle
+  return d;
+}
+
+__device__ __forceinline__ void decode_tile(const TcArgs& a, int64_t tile, int& g, int& mt,
+                                            int& nt) {
+  int lo = 0, hi = a.G;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((int64_t)a.sched[mid] * a.NT <= tile) lo = mid; else hi = mid;
+  }
+  g = lo;
+  const int mtg = a.sched[g + 1] - a.sched[g];
+  const int64_t local = tile - (int64_t)a.sched[g] * a.NT;
+  nt = (int)(local / mtg);
+  mt = (int)(local % mtg);
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                   const __grid_constant__ CUtensorMap tmB1, const TcArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars: full[0..S), empty[S..2S), tfull[2S..2S+2), tempty[2S+2..2S+4), final[2S+4]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t smem_base = smem_u32(smem);
+  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
+  auto tfull_bar = [&](int b) { return smem_u32(&bars[2 * STAGES + b]); };
+  auto tempty_bar = [&](int b) { return smem_u32(&bars[2 * STAGES + 2 + b]); };
+  const uint32_t final_bar = smem_u32(&bars[2 * STAGES + 4]);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), 128);
+    }
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int64_t total = (int64_t)a.sched[a.G] * a.NT;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer ----------------
+      int s = 0;
+      uint32_t ph = 0, issued = 0, par = 0;
+      bool ok = true;
+      for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        int g, mt, nt;
+        decode_tile(a, tile, g, mt, nt);
+        const int64_t gbase = a.offsets ? a.offsets[g] : 0;
+        const int arow = (int)(gbase + (int64_t)mt * BM);
+        for (int kb = 0; kb < a.KB; ++kb) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) { ok = false; break; }
+          const uint32_t sa = smem_base + s * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          mbar_expect_tx(full_bar(s), STAGE_BYTES);
+          tma_load_2d(sa, &tmA, kb * BK, arow, full_bar(s));
+          if (a.mode == kSwiGLU) {
+            tma_load_3d(sb, &tmB0, kb * BK, nt * (BN / 2), g, full_bar(s));
+            tma_load_3d(sb + B_BYTES / 2, &tmB1, kb * BK, nt * (BN / 2), g, full_bar(s));
+          } else {
+            tma_load_3d(sb, &tmB0, kb * BK, nt * BN, g, full_bar(s));
+          }
+          issued |= 1u << s;
+          par = (par & ~(1u << s)) | (ph << s);
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+      }
+      if (*abort_flag) {
+        // let every load still in flight land before the CTA goes away
+        for (int i = 0; i < STAGES; ++i)
+          if (issued & (1u << i)) mbar_wait_quiet(full_bar(i), (par >> i) & 1u);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer ----------------
+      int s = 0, acc = 0;
+      uint32_t ph = 0, aph = 0;
+      bool ok = true;
+      for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + (uint32_t)acc * BN;
+        for (int kb = 0; kb < a.KB; ++kb) {
+          if (!mbar_wait(full_bar(s), ph, abort_flag)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t sa = smem_base + s * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            tc_mma(d, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), IDESC,
+                   (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty_bar(s));
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit(tfull_bar(acc));
+        acc ^= 1;
+        if (acc == 0) aph ^= 1u;
+      }
+      if (*abort_flag) {
+        tc_commit(final_bar);
+        mbar_wait_quiet(final_bar, 0);
+      }
+    }
+  } else {
+    // ---------------- epilogue (warps 2..5) ----------------
+    const int q = warp & 3;  // TMEM lanes this warp may read: 32q .. 32q+31
+    const int r = q * 32 + lane;
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int g, mt, nt;
+      decode_tile(a, tile, g, mt, nt);
+      const int64_t gbeg = a.offsets ? a.offsets[g] : 0;
+      const int64_t gend = a.offsets ? a.offsets[g + 1] : a.single_rows;
+      const int64_t row = gbeg + (int64_t)mt * BM + r;
+      const bool row_ok = row < gend;
+      if (!mbar_wait(tfull_bar(acc), aph, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * BN;
+      if (a.mode == kSwiGLU) {
+        const int n0 = nt * (BN / 2);
+        bf16* out = reinterpret_cast<bf16*>(a.out) + row * a.ldo;
+#pragma unroll 1
+        for (int c = 0; c < BN / 2; c += 32) {
+          uint32_t gr[32], ur[32];
+          tmem_ld32(taddr + c, gr);
+          tmem_ld32(taddr + BN / 2 + c, ur);
+          tmem_wait_ld();
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int n = n0 + c + v * 8;
+              if (n < a.N) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  f[e] = silu_f(__uint_as_float(gr[v * 8 + e])) * __uint_as_float(ur[v * 8 + e]);
+                *reinterpret_cast<uint4*>(out + n) = pack16(f, (const bf16*)nullptr);
+              }
+            }
+          }
+        }
+      } else if (a.mode == kStoreAct) {
+        const int n0 = nt * BN;
+        bf16* out = reinterpret_cast<bf16*>(a.out) + row * a.ldo;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t vr[32];
+          tmem_ld32(taddr + c, vr);
+          tmem_wait_ld();
+          if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const int n = n0 + c + v * 8;
+              if (n < a.N) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(vr[v * 8 + e]);
+                *reinterpret_cast<uint4*>(out + n) = pack16(f, (const bf16*)nullptr);
+              }
+            }
+          }
+        }
+      } else {
+        const int n0 = nt * BN;
+        float* out = reinterpret_cast<float*>(a.out) + row * a.ldo;
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          uint32_t vr[32];
+          tmem_ld32(taddr + c, vr);
+          tmem_wait_ld();
+          if (row_ok) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e)
+              if (n0 + c + e < a.N) out[n0 + c + e] = __uint_as_float(vr[e]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tempty_bar(acc));
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+  if (threadIdx.x == 0 && *abort_flag) set_flag(a.flags, kFlagTimeout);
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D map over a row-major bf16 matrix [rows, K], box 64 x box_rows.
+bool make_map_2d(CUtensorMap* m, const void* ptr, int64_t rows, int K, int box_rows) {
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {BK, (cuuint32_t)box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map {K, N, G} over G matrices [N, K] that start `gstride` elements apart.
+bool make_map_3d(CUtensorMap* m, const void* ptr, int N, int K, int G, int64_t gstride,
+                 int box_rows) {
+  if (G == 1 && gstride == 0) gstride = (int64_t)N * K;
+  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)N, (cuuint64_t)G};
+  cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)gstride * 2};
+  cuuint32_t box[3] = {BK, (cuuint32_t)box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count() {
+  int dev = 0, n = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : 1;
+}
+
+}  // namespace tc
+
+cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
+  using namespace tc;
+  if (a.dtype != MOE_BF16 || encode_fn() == nullptr) return cudaErrorNotSupported;
+  if ((a.K % 8) != 0 || (a.N % 8) != 0 || a.K <= 0 || a.N <= 0) return cudaErrorInvalidValue;
+  cudaError_t e = launch_schedule(a, BM, st);
+  if (e != cudaSuccess) return e;
+  const int64_t rows = a.offsets ? a.rows_bound : a.single_rows;
+  if (rows <= 0) return cudaSuccess;
+  const int brows = a.mode == kSwiGLU ? BN / 2 : BN;
+  CUtensorMap mA, mB0, mB1;
+  if (!make_map_2d(&mA, a.A, rows, a.K, BM)) return cudaErrorInvalidValue;
+  if (!make_map_3d(&mB0, a.B0, a.N, a.K, a.G, a.bstride, brows)) return cudaErrorInvalidValue;
+  if (a.mode == kSwiGLU) {
+    if (!make_map_3d(&mB1, a.B1, a.N, a.K, a.G, a.bstride, brows)) return cudaErrorInvalidValue;
+  } else {
+    mB1 = mB0;
+  }
+  TcArgs t;
+  t.mode = a.mode;
+  t.N = a.N;
+  t.K = a.K;
+  t.G = a.G;
+  t.NT = (a.N + brows - 1) / brows;
+  t.KB = (a.K + BK - 1) / BK;
+  t.offsets = a.offsets;
+  t.single_rows = a.single_rows;
+  t.sched = a.sched;
+  t.out = a.out;
+  t.ldo = a.ldo;
+  t.flags = a.flags;
+  const int64_t mt_bound = a.offsets ? (a.rows_bound + BM - 1) / BM + a.G : (a.single_rows + BM - 1) / BM;
+  const int64_t tiles_bound = mt_bound * t.NT;
+  static bool attr_done = false;
+  if (!attr_done) {
+    e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  const int grid = (int)(tiles_bound < sm_count() ? tiles_bound : sm_count());
+  tc_gemm_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(mA, mB0, mB1, t);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,87 @@
+// internal.h -- host-side plumbing shared by the libmoe translation units:
+// decoded shapes, workspace layout, and the kernel launchers.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+struct Shape {
+  int64_t T;
+  int H, I, I_sh, E, k;
+  int gate;    // shared gate present
+  int norm;    // renormalised top-k
+  int dtype;   // MOE_F32 / MOE_BF16
+  int esize;   // bytes per activation / weight element
+  int ncols;   // router rows: E + gate
+  int ldl;     // leading dimension of the fp32 logits buffer
+};
+
+// Decode and validate; on failure returns the status and sets *why.
+moe_status decode_shape(const moe_shape* s, Shape* out, const char** why);
+
+// Byte offsets of every region inside the workspace (all 256-byte aligned).
+struct Layout {
+  // scratch
+  size_t flags, logits, hist, base, sched_routed, sched_shared, sched_router, scratch_end;
+  int nchunks, tokens_per_chunk;
+  // layer-forward intermediates
+  size_t topk_idx, topk_w, gate, counts, offsets, sidx, row_token, x_perm, h, y_perm, sh_h,
+      sh_out, total;
+};
+Layout layout_for(const Shape& s);
+
+// Launch accounting (per host thread).
+void count_launch(int n = 1);
+void reset_launch_count();
+
+// Which GEMM engine serves bf16: 0 auto, 1 CUDA-core tiles, 2 tensor cores,
+// 3 skinny (set through moe_testing.h by the tests).
+int gemm_path_override();
+
+// ----------------------------------------------------------------------------
+// launchers; each returns the first CUDA error it saw
+// ----------------------------------------------------------------------------
+enum GemmMode { kSwiGLU = 0, kStoreAct = 1, kStoreF32 = 2 };
+
+struct GemmArgs {
+  int mode;
+  int dtype;               // element type of A, B and (modes 0/1) the output
+  const void* A;           // [rows, K] row-major
+  const void* B0;          // group g's [N, K] at B0 + g * bstride
+  const void* B1;          // SwiGLU: the "up" matrices (same stride)
+  int64_t bstride;         // elements
+  int N, K;
+  const int32_t* offsets;  // [G + 1] device, or NULL: one group of single_rows
+  int G;
+  int64_t single_rows;
+  int64_t rows_bound;      // caller's bound on offsets[G]
+  void* out;               // [rows, ldo]
+  int64_t ldo;             // elements
+  int32_t* sched;          // [G + 1] scratch for the m-tile prefix
+  uint32_t* flags;
+};
+
+cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t st);
+cudaError_t launch_gemm_simt(const GemmArgs& a, int bm, cudaStream_t st);
+cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st);
+cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t st);
+cudaError_t launch_schedule(const GemmArgs& a, int bm, cudaStream_t st);
+
+cudaError_t launch_topk(const Shape& s, const float* logits, const void* x, const void* w_router,
+                        int32_t* topk_idx, float* topk_w, float* gate, cudaStream_t st);
+
+cudaError_t launch_permute(const Shape& s, const Layout& L, char* ws, const void* x,
+                           const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
+                           int32_t* scatter_index, int32_t* row_token, void* x_perm,
+                           cudaStream_t st);
+
+cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* scatter_index,
+                           const float* topk_w, const void* shared_out, const float* gate,
+                           void* y, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,534 @@
+// moe_api.cu -- the C ABI of libmoe: argument validation, workspace layout,
+// engine dispatch and the whole-layer sequence.  Declarations and contracts
+// are in include/moe.h.
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "../../include/moe.h"
+#include "../../include/moe_testing.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+static thread_local int tl_launches = 0;
+static thread_local const char* tl_error = "";
+static std::atomic<int> g_engine{0};
+
+void count_launch(int n) { tl_launches += n; }
+void reset_launch_count() { tl_launches = 0; }
+int gemm_path_override() { return g_engine.load(); }
+
+static moe_status fail(moe_status st, const char* why) {
+  tl_error = why;
+  return st;
+}
+
+static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+moe_status decode_shape(const moe_shape* s, Shape* o, const char** why) {
+  if (!s) { *why = "shape is NULL"; return MOE_ERR_INVALID_ARG; }
+  if (s->topk_shape == 0) {
+    *why = "topk_shape is 0: the routing shape word (num_experts << 8) | top_k was never set";
+    return MOE_ERR_INVALID_ARG;
+  }
+  int32_t E, k;
+  if (moe_topk_unpack(s->topk_shape, &E, &k) != MOE_OK) {
+    *why = "topk_shape is not a valid (num_experts << 8) | top_k word";
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (s->dtype != MOE_F32 && s->dtype != MOE_BF16) {
+    *why = "dtype must be MOE_F32 or MOE_BF16";
+    return MOE_ERR_UNSUPPORTED;
+  }
+  if (s->tokens < 0 || s->tokens > (int64_t)0x7fffffff / (k > 0 ? k : 1)) {
+    *why = "tokens must be in [0, 2^31 / top_k)";
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (s->hidden <= 0 || s->hidden % 8 || s->moe_inter <= 0 || s->moe_inter % 8) {
+    *why = "hidden and moe_inter must be positive multiples of 8";
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (s->shared_inter < 0 || s->shared_inter % 8) {
+    *why = "shared_inter must be 0 or a positive multiple of 8";
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (s->shared_gate != 0 && s->shared_gate != 1) {
+    *why = "shared_gate must be 0 or 1";
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (s->shared_gate && s->shared_inter == 0) {
+    *why = "shared_gate is set but shared_inter is 0 (half-specified shared expert)";
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (s->norm_topk != 0 && s->norm_topk != 1) {
+    *why = "norm_topk must be 0 or 1";
+    return MOE_ERR_INVALID_ARG;
+  }
+  o->T = s->tokens;
+  o->H = s->hidden;
+  o->I = s->moe_inter;
+  o->I_sh = s->shared_inter;
+  o->E = E;
+  o->k = k;
+  o->gate = s->shared_gate;
+  o->norm = s->norm_topk;
+  o->dtype = s->dtype;
+  o->esize = s->dtype == MOE_F32 ? 4 : 2;
+  o->ncols = E + s->shared_gate;
+  o->ldl = (o->ncols + 3) & ~3;
+  return MOE_OK;
+}
+
+Layout layout_for(const Shape& s) {
+  Layout L;
+  size_t off = 0;
+  const size_t T = (size_t)s.T, k = (size_t)s.k, E = (size_t)s.E;
+  L.flags = off; off += 256;
+  L.logits = off; off += align256(T * (size_t)s.ldl * 4);
+  int64_t nchunks = (s.T + 15) / 16;
+  int64_t cap = 262144 / s.E;
+  if (cap < 1) cap = 1;
+  if (nchunks > cap) nchunks = cap;
+  if (nchunks < 1) nchunks = 1;
+  L.nchunks = (int)nchunks;
+  L.tokens_per_chunk = (int)((s.T + nchunks - 1) / nchunks);
+  if (L.tokens_per_chunk < 1) L.tokens_per_chunk = 1;
+  L.hist = off; off += align256((size_t)nchunks * E * 4);
+  L.base = off; off += align256((size_t)nchunks * E * 4);
+  L.sched_routed = off; off += align256((E + 1) * 4);
+  L.sched_shared = off; off += 256;
+  L.sched_router = off; off += 256;
+  L.scratch_end = off;
+  L.topk_idx = off; off += align256(T * k * 4);
+  L.topk_w = off; off += align256(T * k * 4);
+  L.gate = off; off += align256(T * 4);
+  L.counts = off; off += align256(E * 4);
+  L.offsets = off; off += align256((E + 1) * 4);
+  L.sidx = off; off += align256(T * k * 4);
+  L.row_token = off; off += align256(T * k * 4);
+  L.x_perm = off; off += align256(T * k * (size_t)s.H * s.esize);
+  L.h = off; off += align256(T * k * (size_t)s.I * s.esize);
+  L.y_perm = off; off += align256(T * k * (size_t)s.H * s.esize);
+  L.sh_h = off; off += align256(T * (size_t)s.I_sh * s.esize);
+  L.sh_out = off; off += align256(s.I_sh ? T * (size_t)s.H * s.esize : 0);
+  L.total = off;
+  return L;
+}
+
+cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t st) {
+  const int ov = gemm_path_override();
+  const int64_t rows = a.offsets ? a.rows_bound : a.single_rows;
+  if (a.dtype == MOE_F32) return ov == 3 ? launch_gemm_skinny(a, st) : launch_gemm_simt(a, 64, st);
+  switch (ov) {
+    case 1: return launch_gemm_simt(a, 64, st);
+    case 2: return launch_gemm_tc(a, st);
+    case 3: return launch_gemm_skinny(a, st);
+    default: break;
+  }
+  if (rows <= 16) return launch_gemm_skinny(a, st);
+  return launch_gemm_tc(a, st);
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+#define CHECK_CUDA(expr)                                        \
+  do {                                                          \
+    cudaError_t e_ = (expr);                                    \
+    if (e_ != cudaSuccess) {                                    \
+      tl_error = cudaGetErrorString(e_);                        \
+      return MOE_ERR_CUDA;                                      \
+    }                                                           \
+  } while (0)
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static moe_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (!ws) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+  if ((uintptr_t)ws & 255u) return fail(MOE_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+  if (ws_bytes < need) return fail(MOE_ERR_WORKSPACE, "workspace smaller than required");
+  return MOE_OK;
+}
+
+#define DECODE(shape, s)                                       \
+  Shape s;                                                     \
+  do {                                                         \
+    const char* why_ = "";                                     \
+    moe_status st_ = decode_shape(shape, &s, &why_);           \
+    if (st_ != MOE_OK) return fail(st_, why_);                 \
+  } while (0)
+
+extern "C" {
+
+uint32_t moe_topk_pack(int32_t num_experts, int32_t top_k) {
+  if (num_experts < 1 || num_experts > 16383 || top_k < 1 || top_k > 255) return 0;
+  return ((uint32_t)num_experts << 8) | (uint32_t)top_k;
+}
+
+moe_status moe_topk_unpack(uint32_t word, int32_t* num_experts, int32_t* top_k) {
+  if (word == 0 || word > 0x3FFFFFu) return MOE_ERR_INVALID_ARG;
+  const int32_t e = (int32_t)(word >> 8), k = (int32_t)(word & 0xFFu);
+  if (e < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (num_experts) *num_experts = e;
+  if (top_k) *top_k = k;
+  return MOE_OK;
+}
+
+size_t moe_scratch_bytes(const moe_shape* shape) {
+  Shape s;
+  const char* why;
+  if (decode_shape(shape, &s, &why) != MOE_OK) return 0;
+  return layout_for(s).scratch_end;
+}
+
+size_t moe_workspace_bytes(const moe_shape* shape) {
+  Shape s;
+  const char* why;
+  if (decode_shape(shape, &s, &why) != MOE_OK) return 0;
+  return layout_for(s).total;
+}
+
+moe_status moe_workspace_views(const moe_shape* shape, void* ws, moe_route_info* v) {
+  DECODE(shape, s);
+  if (!ws || !v) return fail(MOE_ERR_INVALID_ARG, "ws and views must be non-NULL");
+  const Layout L = layout_for(s);
+  char* w = static_cast<char*>(ws);
+  v->topk_idx = reinterpret_cast<int32_t*>(w + L.topk_idx);
+  v->topk_w = reinterpret_cast<float*>(w + L.topk_w);
+  v->gate = s.gate ? reinterpret_cast<float*>(w + L.gate) : nullptr;
+  v->counts = reinterpret_cast<int32_t*>(w + L.counts);
+  v->offsets = reinterpret_cast<int32_t*>(w + L.offsets);
+  v->scatter_index = reinterpret_cast<int32_t*>(w + L.sidx);
+  v->row_token = reinterpret_cast<int32_t*>(w + L.row_token);
+  v->x_perm = w + L.x_perm;
+  v->h = w + L.h;
+  v->y_perm = w + L.y_perm;
+  v->shared_out = s.I_sh ? w + L.sh_out : nullptr;
+  return MOE_OK;
+}
+
+moe_status moe_workspace_init(void* ws, void* stream) {
+  if (!ws) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+  CHECK_CUDA(cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+// Router GEMM into the scratch logits, then top-k.
+static moe_status do_route(const Shape& s, const Layout& L, char* w, const void* x,
+                           const void* router, int32_t* idx, float* tw, float* gate,
+                           cudaStream_t st) {
+  if (s.T == 0) return MOE_OK;
+  float* logits = reinterpret_cast<float*>(w + L.logits);
+  GemmArgs ra;
+  ra.mode = kStoreF32;
+  ra.dtype = s.dtype;
+  ra.A = x;
+  ra.B0 = router;
+  ra.B1 = nullptr;
+  ra.bstride = 0;
+  ra.N = s.ncols;
+  ra.K = s.H;
+  ra.offsets = nullptr;
+  ra.G = 1;
+  ra.single_rows = s.T;
+  ra.rows_bound = s.T;
+  ra.out = logits;
+  ra.ldo = s.ldl;
+  ra.sched = reinterpret_cast<int32_t*>(w + L.sched_router);
+  ra.flags = reinterpret_cast<uint32_t*>(w + L.flags);
+  CHECK_CUDA(launch_grouped_gemm(ra, st));
+  CHECK_CUDA(launch_topk(s, logits, x, router, idx, tw, gate, st));
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_shape* shape, const void* x, const void* w_router,
+                     int32_t* topk_idx, float* topk_w, float* gate, void* ws, size_t ws_bytes,
+                     void* stream) {
+  reset_launch_count();
+  DECODE(shape, s);
+  if (s.k > s.E) return fail(MOE_ERR_INVALID_ARG, "top_k exceeds num_experts");
+  if (s.T > 0 && (!x || !w_router || !topk_idx || !topk_w))
+    return fail(MOE_ERR_INVALID_ARG, "x, w_router, topk_idx and topk_w must be non-NULL");
+  if (s.T > 0 && s.gate && !gate) return fail(MOE_ERR_INVALID_ARG, "shared_gate needs a gate output");
+  if (!aligned16(x) || !aligned16(w_router))
+    return fail(MOE_ERR_INVALID_ARG, "x and w_router must be 16-byte aligned");
+  const Layout L = layout_for(s);
+  moe_status c = check_ws(ws, ws_bytes, L.scratch_end);
+  if (c != MOE_OK) return c;
+  return do_route(s, L, static_cast<char*>(ws), x, w_router, topk_idx, topk_w, gate,
+                  (cudaStream_t)stream);
+}
+
+moe_status moe_permute(const moe_shape* shape, const void* x, const int32_t* topk_idx,
+                       int32_t* counts, int32_t* offsets, int32_t* scatter_index,
+                       int32_t* row_token, void* x_perm, void* ws, size_t ws_bytes,
+                       void* stream) {
+  reset_launch_count();
+  DECODE(shape, s);
+  if (!counts || !offsets) return fail(MOE_ERR_INVALID_ARG, "counts and offsets must be non-NULL");
+  if (s.T > 0 && (!x || !topk_idx || !scatter_index || !row_token || !x_perm))
+    return fail(MOE_ERR_INVALID_ARG, "x, topk_idx, scatter_index, row_token, x_perm must be non-NULL");
+  if (!aligned16(x) || !aligned16(x_perm))
+    return fail(MOE_ERR_INVALID_ARG, "x and x_perm must be 16-byte aligned");
+  const Layout L = layout_for(s);
+  moe_status c = check_ws(ws, ws_bytes, L.scratch_end);
+  if (c != MOE_OK) return c;
+  CHECK_CUDA(launch_permute(s, L, static_cast<char*>(ws), x, topk_idx, counts, offsets,
+                            scatter_index, row_token, x_perm, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+static moe_status grouped(int mode, const moe_shape* shape, const void* A, const void* B0,
+                          const void* B1, int64_t stride, const int32_t* offsets, int32_t G,
+                          int64_t rows_bound, int32_t inter, void* out, void* ws,
+                          size_t ws_bytes, void* stream) {
+  reset_launch_count();
+  DECODE(shape, s);
+  if (G < 1 || (G > s.E && G != 1)) return fail(MOE_ERR_INVALID_ARG, "num_groups must be in [1, E]");
+  if (!offsets) return fail(MOE_ERR_INVALID_ARG, "offsets must be non-NULL");
+  if (inter <= 0 || inter % 8) return fail(MOE_ERR_INVALID_ARG, "inter must be a positive multiple of 8");
+  if (rows_bound < 0 || rows_bound > 0x7fffffff) return fail(MOE_ERR_INVALID_ARG, "rows_bound out of range");
+  if (stride < 0) return fail(MOE_ERR_INVALID_ARG, "expert_stride must be >= 0");
+  if (G > 1 && stride == 0) return fail(MOE_ERR_INVALID_ARG, "expert_stride is 0 with several groups");
+  if (rows_bound > 0 && (!A || !B0 || !out || (mode == kSwiGLU && !B1)))
+    return fail(MOE_ERR_INVALID_ARG, "operand pointers must be non-NULL");
+  if (!aligned16(A) || !aligned16(B0) || !aligned16(B1) || !aligned16(out) || (stride * s.esize) % 16)
+    return fail(MOE_ERR_INVALID_ARG, "operands and expert_stride must be 16-byte aligned");
+  const Layout L = layout_for(s);
+  moe_status c = check_ws(ws, ws_bytes, L.scratch_end);
+  if (c != MOE_OK) return c;
+  char* w = static_cast<char*>(ws);
+  GemmArgs a;
+  a.mode = mode;
+  a.dtype = s.dtype;
+  a.A = A;
+  a.B0 = B0;
+  a.B1 = B1;
+  a.bstride = stride;
+  a.N = mode == kSwiGLU ? inter : s.H;
+  a.K = mode == kSwiGLU ? s.H : inter;
+  a.offsets = offsets;
+  a.G = G;
+  a.single_rows = 0;
+  a.rows_bound = rows_bound;
+  a.out = out;
+  a.ldo = a.N;
+  a.sched = reinterpret_cast<int32_t*>(w + (G > 1 ? L.sched_routed : L.sched_shared));
+  a.flags = reinterpret_cast<uint32_t*>(w + L.flags);
+  CHECK_CUDA(launch_grouped_gemm(a, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status moe_grouped_swiglu(const moe_shape* shape, const void* x_perm, const void* w_gate,
+                              const void* w_up, int64_t expert_stride, const int32_t* offsets,
+                              int32_t num_groups, int64_t rows_bound, int32_t inter, void* h,
+                              void* ws, size_t ws_bytes, void* stream) {
+  return grouped(kSwiGLU, shape, x_perm, w_gate, w_up, expert_stride, offsets, num_groups,
+                 rows_bound, inter, h, ws, ws_bytes, stream);
+}
+
+moe_status moe_grouped_down(const moe_shape* shape, const void* h, const void* w_down,
+                            int64_t expert_stride, const int32_t* offsets, int32_t num_groups,
+                            int64_t rows_bound, int32_t inter, void* y_perm, void* ws,
+                            size_t ws_bytes, void* stream) {
+  return grouped(kStoreAct, shape, h, w_down, nullptr, expert_stride, offsets, num_groups,
+                 rows_bound, inter, y_perm, ws, ws_bytes, stream);
+}
+
+moe_status moe_combine(const moe_shape* shape, const void* y_perm, const int32_t* scatter_index,
+                       const float* topk_w, const void* shared_out, const float* gate, void* y,
+                       void* stream) {
+  reset_launch_count();
+  DECODE(shape, s);
+  if (s.T > 0 && (!y_perm || !scatter_index || !topk_w || !y))
+    return fail(MOE_ERR_INVALID_ARG, "y_perm, scatter_index, topk_w and y must be non-NULL");
+  if (!aligned16(y_perm) || !aligned16(shared_out) || !aligned16(y))
+    return fail(MOE_ERR_INVALID_ARG, "y_perm, shared_out and y must be 16-byte aligned");
+  CHECK_CUDA(launch_combine(s, y_perm, scatter_index, topk_w, shared_out, gate, y,
+                            (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status moe_layer_forward(const moe_shape* shape, const moe_weights* W, const void* x,
+                             const int32_t* routes_idx, const float* routes_w, void* y, void* ws,
+                             size_t ws_bytes, void* stream) {
+  return moe_layer_forward_traced(shape, W, x, routes_idx, routes_w, y, ws, ws_bytes, stream,
+                                  nullptr);
+}
+
+moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W, const void* x,
+                                    const int32_t* routes_idx, const float* routes_w, void* y,
+                                    void* ws, size_t ws_bytes, void* stream,
+                                    void* const* ev) {
+  reset_launch_count();
+  DECODE(shape, s);
+  if (!W) return fail(MOE_ERR_INVALID_ARG, "weights is NULL");
+  const bool direct = routes_idx != nullptr;
+  if ((routes_idx == nullptr) != (routes_w == nullptr))
+    return fail(MOE_ERR_INVALID_ARG, "routes_idx and routes_w go together");
+  if (!direct && !W->router) return fail(MOE_ERR_INVALID_ARG, "no router and no direct routes");
+  if (direct && s.gate) return fail(MOE_ERR_INVALID_ARG, "shared_gate needs the router");
+  if (!direct && s.k > s.E) return fail(MOE_ERR_INVALID_ARG, "top_k exceeds num_experts");
+  if (s.T > 0 && (!x || !y || !W->gate || !W->up || !W->down))
+    return fail(MOE_ERR_INVALID_ARG, "x, y and the expert weights must be non-NULL");
+  if (s.I_sh && (!W->shared_gate_proj || !W->shared_up || !W->shared_down))
+    return fail(MOE_ERR_INVALID_ARG, "shared_inter > 0 needs the three shared weights");
+  if (!s.I_sh && (W->shared_gate_proj || W->shared_up || W->shared_down))
+    return fail(MOE_ERR_INVALID_ARG, "shared weights given but shared_inter is 0");
+  if (W->gate_up_stride < (int64_t)s.I * s.H || W->down_stride < (int64_t)s.H * s.I)
+    return fail(MOE_ERR_INVALID_ARG, "expert strides smaller than one expert matrix");
+  if (!aligned16(x) || !aligned16(y) || !aligned16(W->router) || !aligned16(W->gate) ||
+      !aligned16(W->up) || !aligned16(W->down) || !aligned16(W->shared_gate_proj) ||
+      !aligned16(W->shared_up) || !aligned16(W->shared_down) ||
+      (W->gate_up_stride * s.esize) % 16 || (W->down_stride * s.esize) % 16)
+    return fail(MOE_ERR_INVALID_ARG, "tensors and strides must be 16-byte aligned");
+  const Layout L = layout_for(s);
+  moe_status c = check_ws(ws, ws_bytes, L.total);
+  if (c != MOE_OK) return c;
+  if (s.T == 0) return MOE_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  char* w = static_cast<char*>(ws);
+  uint32_t* flags = reinterpret_cast<uint32_t*>(w + L.flags);
+  int32_t* idx = reinterpret_cast<int32_t*>(w + L.topk_idx);
+  float* tw = reinterpret_cast<float*>(w + L.topk_w);
+  float* gate = s.gate ? reinterpret_cast<float*>(w + L.gate) : nullptr;
+  const int32_t* use_idx = idx;
+  const float* use_w = tw;
+#define STAGE_EVENT(i) \
+  if (ev) CHECK_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st))
+  STAGE_EVENT(MOE_STAGE_ROUTE);
+  if (direct) {
+    use_idx = routes_idx;
+    use_w = routes_w;
+  } else {
+    moe_status r = do_route(s, L, w, x, W->router, idx, tw, gate, st);
+    if (r != MOE_OK) return r;
+  }
+  int32_t* counts = reinterpret_cast<int32_t*>(w + L.counts);
+  int32_t* offsets = reinterpret_cast<int32_t*>(w + L.offsets);
+  int32_t* sidx = reinterpret_cast<int32_t*>(w + L.sidx);
+  int32_t* row_token = reinterpret_cast<int32_t*>(w + L.row_token);
+  void* x_perm = w + L.x_perm;
+  void* h = w + L.h;
+  void* y_perm = w + L.y_perm;
+  STAGE_EVENT(MOE_STAGE_PERMUTE);
+  CHECK_CUDA(launch_permute(s, L, w, x, use_idx, counts, offsets, sidx, row_token, x_perm, st));
+  STAGE_EVENT(MOE_STAGE_GATE_UP);
+
+  GemmArgs a;
+  a.dtype = s.dtype;
+  a.offsets = offsets;
+  a.G = s.E;
+  a.single_rows = 0;
+  a.rows_bound = s.T * s.k;
+  a.sched = reinterpret_cast<int32_t*>(w + L.sched_routed);
+  a.flags = flags;
+  a.mode = kSwiGLU;
+  a.A = x_perm;
+  a.B0 = W->gate;
+  a.B1 = W->up;
+  a.bstride = W->gate_up_stride;
+  a.N = s.I;
+  a.K = s.H;
+  a.out = h;
+  a.ldo = s.I;
+  CHECK_CUDA(launch_grouped_gemm(a, st));
+  STAGE_EVENT(MOE_STAGE_DOWN);
+  a.mode = kStoreAct;
+  a.A = h;
+  a.B0 = W->down;
+  a.B1 = nullptr;
+  a.bstride = W->down_stride;
+  a.N = s.H;
+  a.K = s.I;
+  a.out = y_perm;
+  a.ldo = s.H;
+  CHECK_CUDA(launch_grouped_gemm(a, st));
+
+  STAGE_EVENT(MOE_STAGE_SHARED);
+  void* sh_out = nullptr;
+  if (s.I_sh) {
+    sh_out = w + L.sh_out;
+    GemmArgs b;
+    b.dtype = s.dtype;
+    b.offsets = nullptr;
+    b.G = 1;
+    b.single_rows = s.T;
+    b.rows_bound = s.T;
+    b.sched = reinterpret_cast<int32_t*>(w + L.sched_shared);
+    b.flags = flags;
+    b.mode = kSwiGLU;
+    b.A = x;
+    b.B0 = W->shared_gate_proj;
+    b.B1 = W->shared_up;
+    b.bstride = 0;
+    b.N = s.I_sh;
+    b.K = s.H;
+    b.out = w + L.sh_h;
+    b.ldo = s.I_sh;
+    CHECK_CUDA(launch_grouped_gemm(b, st));
+    b.mode = kStoreAct;
+    b.A = w + L.sh_h;
+    b.B0 = W->shared_down;
+    b.B1 = nullptr;
+    b.N = s.H;
+    b.K = s.I_sh;
+    b.out = sh_out;
+    b.ldo = s.H;
+    CHECK_CUDA(launch_grouped_gemm(b, st));
+  }
+  STAGE_EVENT(MOE_STAGE_COMBINE);
+  CHECK_CUDA(launch_combine(s, y_perm, sidx, use_w, sh_out, gate, y, st));
+  STAGE_EVENT(MOE_NUM_STAGES);
+#undef STAGE_EVENT
+  return MOE_OK;
+}
+
+moe_status moe_get_device_status(void* ws, void* stream, uint32_t* bits) {
+  if (!ws) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+  CHECK_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+  uint32_t v = 0;
+  CHECK_CUDA(cudaMemcpy(&v, ws, sizeof(v), cudaMemcpyDeviceToHost));
+  CHECK_CUDA(cudaMemset(ws, 0, sizeof(v)));
+  if (bits) *bits = v;
+  if (v & kFlagRoute) return MOE_ERR_DEVICE_ROUTE;
+  if (v & kFlagRows) return MOE_ERR_ROWS;
+  if (v & kFlagTimeout) return MOE_ERR_TIMEOUT;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status st) {
+  switch (st) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_ROUTE: return "MOE_ERR_DEVICE_ROUTE";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_ROWS: return "MOE_ERR_ROWS";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+const char* moe_last_error(void) { return tl_error; }
+
+const char* moe_stage_name(int32_t stage) {
+  static const char* names[MOE_NUM_STAGES] = {"route",  "permute", "gate_up",
+                                              "down",   "shared",  "combine"};
+  if (stage < 0 || stage >= MOE_NUM_STAGES) return "";
+  return names[stage];
+}
+
+int32_t moe_last_launch_count(void) { return tl_launches; }
+
+int32_t moe_testing_set_gemm_engine(int32_t engine) {
+  if (engine < 0 || engine > 3) engine = 0;
+  return g_engine.exchange(engine);
+}
+
+}  // extern "C"

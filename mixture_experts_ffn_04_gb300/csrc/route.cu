@@ -1,0 +1,284 @@
+// route.cu -- top-k softmax over router logits, one warp per token.
+//
+// "MoE: timing-replay harnesses, shared experts, parameterized V_TOPK routing"
+// (C_SET_TOPK_REG section): topk_softmax is generic in (num_experts, top_k),
+// so this kernel takes any E <= 16383 and k <= 255 from the packed shape word.
+//
+//   selection  k rounds of a warp arg-max (shuffle reduction), equal values
+//              resolved to the lower expert index; slot s = (s+1)-th largest;
+//   weights    norm_topk: exp(l_s - l_max) / sum over the k selected;
+//              otherwise: exp(l_s - l_max) / sum over all E;
+//   gate       Qwen2-MoE shared gate sigmoid(z), z = logit column E
+//              ("MoE: shared experts, arbitrary V_TOPK expert shapes, ...",
+//              Group C).
+//
+// Near ties.  The logits arrive in fp32 (tensor-core or FMA sums), within a
+// small error of the exact dot products.  When two neighbours of the sorted
+// top-(k+1) list are closer than a bound tau well above that error, the
+// experts within tau of the boundary are re-evaluated with an error-free
+// compensated dot product (Ogita, Rump and Oishi, "Accurate Sum and Dot
+// Product", SIAM J. Sci. Comput. 26(6), 2005: algorithm Dot2) and the
+// selection among them is redone on those values.  The decision then matches
+// exact arithmetic except for true near-ties far below the fp32 error.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kMaxRounds = 256;  // k <= 255 plus one round for the boundary
+constexpr int kMaxCand = 64;     // experts re-evaluated in a near tie
+
+struct TopkArgs {
+  const float* logits;
+  int ldl;
+  const void* x;
+  const void* w;  // router [ncols, H]
+  int H, E, k, norm, gated;
+  int64_t T;
+  float tau_scale;
+  int32_t* idx;
+  float* wout;
+  float* gate;
+};
+
+struct WarpSmem {
+  float* buf;        // [E] logits of this token
+  uint32_t* taken;   // [ceil(E/32)]
+  int* sel_i;        // [kMaxRounds]
+  float* sel_v;      // [kMaxRounds]
+  int* cand_i;       // [kMaxCand]
+  double* cand_v;    // [kMaxCand]
+};
+
+__host__ __device__ inline size_t warp_smem_bytes(int E) {
+  size_t b = 0;
+  b += (size_t)kMaxCand * 8;            // cand_v (first: 8-byte aligned)
+  b += (size_t)E * 4;                   // buf
+  b += (size_t)((E + 31) / 32) * 4;     // taken
+  b += (size_t)kMaxRounds * 8;          // sel_i + sel_v
+  b += (size_t)kMaxCand * 4;            // cand_i
+  return (b + 15) & ~(size_t)15;
+}
+
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+// Warp arg-max of (v, i); every lane receives the winner.
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (better(ov, oi, v, i)) { v = ov; i = oi; }
+  }
+}
+
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
+  s = __fadd_rn(a, b);
+  float z = __fsub_rn(s, a);
+  e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, z)), __fsub_rn(b, z));
+}
+
+__device__ __forceinline__ void two_prod(float a, float b, float& p, float& e) {
+  p = __fmul_rn(a, b);
+  e = __fmaf_rn(a, b, -p);
+}
+
+// Dot2 of row x and router row w over H, cooperatively by the warp.
+template <typename T>
+__device__ double dot2(const T* x, const T* w, int H, int lane) {
+  float p = 0.f, s = 0.f;
+  for (int h = lane; h < H; h += 32) {
+    float hp, r, q;
+    two_prod(to_f(x[h]), to_f(w[h]), hp, r);
+    two_sum(p, hp, p, q);
+    s = __fadd_rn(s, __fadd_rn(q, r));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    float op = __shfl_xor_sync(0xffffffffu, p, o);
+    float os = __shfl_xor_sync(0xffffffffu, s, o);
+    float q;
+    two_sum(p, op, p, q);
+    s = __fadd_rn(__fadd_rn(s, os), q);
+  }
+  return (double)p + (double)s;
+}
+
+template <typename T>
+__global__ void topk_kernel(TopkArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int E = a.E, k = a.k;
+  unsigned char* base = smem_raw + warp_smem_bytes(E) * wid;
+  WarpSmem sm;
+  sm.cand_v = reinterpret_cast<double*>(base);
+  sm.buf = reinterpret_cast<float*>(base + kMaxCand * 8);
+  sm.taken = reinterpret_cast<uint32_t*>(sm.buf + E);
+  sm.sel_i = reinterpret_cast<int*>(sm.taken + (E + 31) / 32);
+  sm.sel_v = reinterpret_cast<float*>(sm.sel_i + kMaxRounds);
+  sm.cand_i = reinterpret_cast<int*>(sm.sel_v + kMaxRounds);
+
+  const int R = k < E ? k + 1 : k;
+  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + wid;
+  if (t >= a.T) return;
+
+  const float* row = a.logits + t * a.ldl;
+  float m = -INFINITY;
+  for (int e = lane; e < E; e += 32) {
+    float v = row[e];
+    sm.buf[e] = v;
+    m = fmaxf(m, v);
+  }
+  for (int w = lane; w < (E + 31) / 32; w += 32) sm.taken[w] = 0u;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __syncwarp();
+
+  for (int r = 0; r < R; ++r) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int e = lane; e < E; e += 32) {
+      if (sm.taken[e >> 5] & (1u << (e & 31))) continue;
+      float v = sm.buf[e];
+      if (bi == 0x7fffffff || better(v, e, bv, bi)) { bv = v; bi = e; }
+    }
+    warp_argmax(bv, bi);
+    if (lane == 0) {
+      sm.sel_i[r] = bi;
+      sm.sel_v[r] = bv;
+      sm.taken[bi >> 5] |= 1u << (bi & 31);
+    }
+    __syncwarp();
+  }
+
+  // ---- near-tie re-decision -------------------------------------------
+  const float vb = sm.sel_v[R - 1];
+  const float tau = a.tau_scale * (fabsf(sm.sel_v[0]) + fabsf(vb) + 1.0f);
+  bool near = false;
+  for (int r = lane; r + 1 < R; r += 32) near |= (sm.sel_v[r] - sm.sel_v[r + 1]) < tau;
+  near = __any_sync(0xffffffffu, near);
+  if (near && a.x != nullptr) {
+    // candidates: every expert within tau below the boundary value, plus above
+    int nc = 0;
+    bool overflow = false;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+      int e = e0 + lane;
+      bool c = e < E && sm.buf[e] >= vb - tau;
+      unsigned msk = __ballot_sync(0xffffffffu, c);
+      int pos = nc + __popc(msk & ((1u << lane) - 1u));
+      if (c && pos < kMaxCand) sm.cand_i[pos] = e;
+      nc += __popc(msk);
+    }
+    if (nc > kMaxCand) overflow = true;
+    __syncwarp();
+    if (!overflow) {
+      const T* xr = reinterpret_cast<const T*>(a.x) + t * a.H;
+      for (int c = 0; c < nc; ++c) {
+        const T* wr = reinterpret_cast<const T*>(a.w) + (int64_t)sm.cand_i[c] * a.H;
+        double v = dot2<T>(xr, wr, a.H, lane);
+        if (lane == 0) sm.cand_v[c] = v;
+      }
+      __syncwarp();
+      // Every non-candidate lies more than tau below the boundary, so the top
+      // R experts are all candidates: redo the rounds among them exactly.
+      uint64_t used = 0ull;  // candidate c taken (nc <= 64)
+      for (int r = 0; r < R && r < nc; ++r) {
+        double bv2 = -INFINITY;
+        int bi2 = 0x7fffffff, bc = -1;
+        for (int c = lane; c < nc; c += 32) {
+          if (used & (1ull << c)) continue;
+          double v = sm.cand_v[c];
+          int e = sm.cand_i[c];
+          if (bc < 0 || v > bv2 || (v == bv2 && e < bi2)) { bv2 = v; bi2 = e; bc = c; }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+          double ov = __shfl_xor_sync(0xffffffffu, bv2, o);
+          int oi = __shfl_xor_sync(0xffffffffu, bi2, o);
+          int oc = __shfl_xor_sync(0xffffffffu, bc, o);
+          bool take = (bc < 0 && oc >= 0) ||
+                      (oc >= 0 && (ov > bv2 || (ov == bv2 && oi < bi2)));
+          if (take) { bv2 = ov; bi2 = oi; bc = oc; }
+        }
+        used |= 1ull << bc;
+        if (lane == 0) {
+          sm.sel_i[r] = bi2;
+          sm.sel_v[r] = sm.buf[bi2];
+        }
+        __syncwarp();
+      }
+    }
+    __syncwarp();
+  }
+
+  // ---- weights ------------------------------------------------------------
+  float denom = 0.f;
+  if (a.norm) {
+    const float top = sm.sel_v[0];
+    for (int s = lane; s < k; s += 32) denom += expf(sm.sel_v[s] - top);
+  } else {
+    for (int e = lane; e < E; e += 32) denom += expf(sm.buf[e] - m);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, o);
+  const float ref = a.norm ? sm.sel_v[0] : m;
+  for (int s = lane; s < k; s += 32) {
+    a.idx[t * k + s] = sm.sel_i[s];
+    a.wout[t * k + s] = expf(sm.sel_v[s] - ref) / denom;
+  }
+  if (a.gated && lane == 0) {
+    const float z = row[E];
+    a.gate[t] = 1.0f / (1.0f + expf(-z));
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const Shape& s, const float* logits, const void* x, const void* w_router,
+                        int32_t* topk_idx, float* topk_w, float* gate, cudaStream_t st) {
+  if (s.T == 0) return cudaSuccess;
+  TopkArgs a;
+  a.logits = logits;
+  a.ldl = s.ldl;
+  a.x = x;
+  a.w = w_router;
+  a.H = s.H;
+  a.E = s.E;
+  a.k = s.k;
+  a.norm = s.norm;
+  a.gated = s.gate;
+  a.T = s.T;
+  // tau = 2^-20 * sqrt(H) * (|l_top| + |l_boundary| + 1): about 100x the
+  // typical fp32 rounding error of an H-term dot product of these magnitudes.
+  a.tau_scale = (float)(ldexp(1.0, -20) * sqrt((double)s.H));
+  a.idx = topk_idx;
+  a.wout = topk_w;
+  a.gate = gate;
+  const size_t per_warp = warp_smem_bytes(s.E);
+  int warps = (int)((96 * 1024) / per_warp);
+  if (warps > 8) warps = 8;
+  if (warps < 1) warps = 1;
+  const size_t smem = per_warp * warps;
+  const int64_t blocks = (s.T + warps - 1) / warps;
+  cudaError_t e;
+  if (s.dtype == MOE_F32) {
+    e = cudaFuncSetAttribute(topk_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    topk_kernel<float><<<(unsigned)blocks, warps * 32, smem, st>>>(a);
+  } else {
+    e = cudaFuncSetAttribute(topk_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    topk_kernel<bf16><<<(unsigned)blocks, warps * 32, smem, st>>>(a);
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,131 @@
+"""The C ABI without a GPU: the library loads, exports every symbol the
+headers declare, and rejects bad arguments on the host before any CUDA call
+(status codes and messages follow include/moe.h)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def m():
+    import mixture_experts_ffn_04_gb300 as m
+    from mixture_experts_ffn_04_gb300 import build
+    build.build()
+    m.lib()
+    return m
+
+
+def _declared_functions():
+    names = []
+    for h in ("moe.h", "moe_testing.h"):
+        src = open(os.path.join(ROOT, "include", h)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w \*]*?\b(moe_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(m):
+    names = _declared_functions()
+    assert len(names) >= 18
+    lib = ctypes.CDLL(m.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_pack_unpack_matches_pages_rule(m):
+    assert m.moe_topk_pack(256, 8) == (256 << 8) | 8
+    assert m.moe_topk_pack(16383, 255) == (1 << 22) - 1
+    assert m.moe_topk_pack(16384, 1) == 0 and m.moe_topk_pack(8, 256) == 0
+    assert m.moe_topk_unpack(15364) == (60, 4)
+    with pytest.raises(m.MoEError) as e:
+        m.moe_topk_unpack(0)
+    assert e.value.status == m.MOE_ERR_INVALID_ARG
+
+
+def test_stage_names(m):
+    """The stage vocabulary of the header and the binding agree both ways."""
+    names = [m.moe_stage_name(i) for i in range(6)]
+    assert tuple(names) == m.STAGES
+    assert m.moe_stage_name(6) == "" and m.moe_stage_name(-1) == ""
+
+
+def _shape(m, **kw):
+    s = m.MoEShape()
+    s.tokens, s.hidden, s.moe_inter, s.shared_inter = 64, 256, 128, 0
+    s.topk_shape = m.moe_topk_pack(8, 2)
+    s.shared_gate, s.norm_topk, s.dtype = 0, 1, m.MOE_BF16
+    for k, v in kw.items():
+        setattr(s, k, v)
+    return s
+
+
+def test_validation_rejects_bad_shapes(m):
+    lib = m.lib()
+    P = ctypes.c_void_p
+    w = m.MoEWeights()
+    cases = [
+        (dict(topk_shape=0), m.MOE_ERR_INVALID_ARG, "never set"),
+        (dict(shared_gate=1, shared_inter=0), m.MOE_ERR_INVALID_ARG, "half-specified"),
+        (dict(dtype=7), m.MOE_ERR_UNSUPPORTED, "dtype"),
+        (dict(hidden=100), m.MOE_ERR_INVALID_ARG, "multiples of 8"),
+        (dict(tokens=-1), m.MOE_ERR_INVALID_ARG, "tokens"),
+    ]
+    for kw, status, frag in cases:
+        s = _shape(m, **kw)
+        assert m.moe_workspace_bytes(s) == 0
+        st = lib.moe_layer_forward(ctypes.byref(s), ctypes.byref(w), P(16), None, None, P(16),
+                                   P(256), 1 << 30, None)
+        assert st == status, (kw, st)
+        assert frag in m.moe_last_error(), m.moe_last_error()
+
+
+def test_validation_rejects_bad_calls(m):
+    lib = m.lib()
+    P = ctypes.c_void_p
+    s = _shape(m)
+    need = m.moe_workspace_bytes(s)
+    assert need > m.moe_scratch_bytes(s) > 0
+    w = m.MoEWeights()
+    w.router = w.gate = w.up = w.down = 4096
+    w.gate_up_stride = 128 * 256
+    w.down_stride = 256 * 128
+    # workspace too small / misaligned / missing
+    for ws, n in ((P(4096), need - 1), (P(4096 + 16), need), (None, need)):
+        st = lib.moe_layer_forward(ctypes.byref(s), ctypes.byref(w), P(4096), None, None,
+                                   P(4096), ws, n, None)
+        assert st == m.MOE_ERR_WORKSPACE
+    # routes_idx without routes_w
+    st = lib.moe_layer_forward(ctypes.byref(s), ctypes.byref(w), P(4096), P(4096), None,
+                               P(4096), P(4096), need, None)
+    assert st == m.MOE_ERR_INVALID_ARG
+    # router with k > E
+    s2 = _shape(m, topk_shape=m.moe_topk_pack(4, 8))
+    st = lib.moe_route(ctypes.byref(s2), P(4096), P(4096), P(4096), P(4096), None, P(4096),
+                       1 << 30, None)
+    assert st == m.MOE_ERR_INVALID_ARG and "top_k" in m.moe_last_error()
+    # shared weights without shared_inter
+    w.shared_up = 4096
+    st = lib.moe_layer_forward(ctypes.byref(s), ctypes.byref(w), P(4096), None, None, P(4096),
+                               P(4096), need, None)
+    assert st == m.MOE_ERR_INVALID_ARG
+    # grouped GEMM: zero stride with several groups, misaligned operand
+    st = lib.moe_grouped_swiglu(ctypes.byref(s), P(4096), P(4096), P(4096), 0, P(4096), 8, 128,
+                                128, P(4096), P(4096), 1 << 30, None)
+    assert st == m.MOE_ERR_INVALID_ARG
+    st = lib.moe_grouped_down(ctypes.byref(s), P(4098), P(4096), 32768, P(4096), 8, 128, 128,
+                              P(4096), P(4096), 1 << 30, None)
+    assert st == m.MOE_ERR_INVALID_ARG
+
+
+def test_workspace_layout_scales(m):
+    """Intermediates grow with T*k rows; scratch stays small."""
+    from mixture_experts_ffn_04_gb300 import workloads as W
+    s = m.shape_for(W.DEEPSEEK_V3)
+    T, k, H, I = 8192, 8, 7168, 2048
+    inter = 2 * T * k * H * 2 + T * k * I * 2
+    assert inter <= m.moe_workspace_bytes(s) <= inter * 1.2
+    assert m.moe_scratch_bytes(s) < 64 << 20

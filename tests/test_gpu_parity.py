@@ -1,0 +1,154 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Reduced shapes keep each workload's routing structure (E, k, gate, top-k
+convention, direct routes) at sizes the oracle checks in full; they span
+several 128-row tiles, ragged group tails and partial N and K tiles.  Full
+sizes run in the launch configuration the benchmark times and are checked
+on routing (every token, bit-exact), grouping (bit-exact) and a seeded token
+sample of the output.  Intermediates are poisoned with NaN before each run, so
+a row the kernels failed to write shows up as a non-finite output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_ffn_04_gb300 as m
+from mixture_experts_ffn_04_gb300 import workloads as W
+
+from gpu_util import TOL, check_layer, rel_l2, run_gpu, to_dev
+
+pytestmark = pytest.mark.gpu
+
+REDUCED = [
+    W.small(W.TINY_F32, T=300),
+    W.small(W.QWEN3_30B_A3B, T=300, H=512, I=256),
+    W.small(W.QWEN3_30B_A3B, T=77, H=392, I=200, E=16, k=3),      # ragged N and K
+    W.small(W.DEEPSEEK_V3, T=260, H=512, I=256, I_sh=256),
+    W.small(W.QWEN2_MOE, T=300, H=512, I=256, I_sh=512),
+    W.small(W.QWEN2_MOE, T=5, H=512, I=256, I_sh=512),            # decode-sized
+    W.small(W.ADV_E0, T=300, H=512, I=256, I_sh=256),
+    W.small(W.ADV_ZIPF, T=300, H=512, I=256, I_sh=256),
+]
+ENGINES = {0: "auto", 1: "cuda-core", 2: "tensor-core", 3: "skinny"}
+
+
+def _cases():
+    for wl in REDUCED:
+        engines = [0, 3] if wl.dtype == "f32" else [0, 1, 2, 3]
+        for e in engines:
+            yield pytest.param(wl, e, id="%s-%s" % (wl.name, ENGINES[e]))
+
+
+@pytest.mark.parametrize("wl,engine", list(_cases()))
+def test_reduced_parity(wl, engine):
+    inp = W.make_inputs(wl, seed=0, device="cpu")
+    dev = to_dev(inp)
+    res = run_gpu(wl, dev, engine=engine)
+    out = check_layer(wl, dev, res)
+    assert out["launches"] > 0
+    if wl.routing == "all_to_e0":
+        assert out["max_group"] == wl.T * wl.k
+
+
+FULL = [
+    (W.TINY_F32, None),
+    (W.QWEN3_30B_A3B, 48),
+    (W.DEEPSEEK_V3, 8),
+    (W.get("qwen2-moe-shape-T2048"), 12),
+    (W.get("qwen2-moe-shape-T64"), 12),
+    (W.get("qwen2-moe-shape-T8"), None),
+    (W.get("qwen2-moe-shape-T1"), None),
+    (W.get("adversarial-all-e0-T128"), 24),
+    (W.get("adversarial-all-e0-T16384"), 8),
+    (W.get("adversarial-zipf-T128"), 24),
+    (W.get("adversarial-zipf-T16384"), 8),
+]
+
+
+@pytest.mark.parametrize("wl,nsample", FULL, ids=[f[0].name for f in FULL])
+def test_full_size_parity(wl, nsample):
+    dev = W.make_inputs(wl, seed=0, device="cuda")
+    res = run_gpu(wl, dev, poison=False)
+    sample = None
+    if nsample is not None:
+        rng = np.random.Generator(np.random.PCG64(1234))
+        sample = np.sort(rng.choice(wl.T, size=min(nsample, wl.T), replace=False))
+    out = check_layer(wl, dev, res, sample=sample)
+    print("%s: rel_l2=%.3e near_ties=%d max_group=%d launches=%d" % (
+        wl.name, out["rel_l2"], out["ties"], out["max_group"], out["launches"]))
+    del dev, res
+    torch.cuda.empty_cache()
+
+
+def test_step_api_matches_layer_and_merged_fc1():
+    """route -> permute -> grouped gate/up -> grouped down -> shared -> combine
+    through the individual entry points gives the layer's output bit for bit,
+    and merged fc1 ([E, 2I, H] with stride 2*I*H) gives the split result."""
+    wl = W.small(W.QWEN2_MOE, T=300, H=512, I=256, I_sh=512)
+    dev = to_dev(W.make_inputs(wl, seed=3, device="cpu"))
+    layer = m.MoELayer(wl, dev)
+    y_ref = layer.forward(dev["x"])
+    s = layer.shape
+    T, H, I, E, k, Ish = wl.T, wl.H, wl.I, wl.E, wl.k, wl.I_sh
+    ws = m.alloc_workspace(s, full=False)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    idx, tw = torch.empty(T, k, **i32), torch.empty(T, k, dtype=torch.float32, device="cuda")
+    gate = torch.empty(T, dtype=torch.float32, device="cuda")
+    m.moe_route(s, dev["x"], dev["w_router"], idx, tw, gate, ws)
+    counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
+    sidx, row_token = torch.empty(T, k, **i32), torch.empty(T * k, **i32)
+    x_perm = torch.empty(T * k, H, dtype=torch.bfloat16, device="cuda")
+    m.moe_permute(s, dev["x"], idx, counts, offsets, sidx, row_token, x_perm, ws)
+    h = torch.empty(T * k, I, dtype=torch.bfloat16, device="cuda")
+    merged = torch.cat([dev["w_gate"], dev["w_up"]], dim=1).contiguous()
+    m.moe_grouped_swiglu(s, x_perm, merged, None, 2 * I * H, offsets, E, T * k, I, h, ws,
+                         w_up_ptr=merged.data_ptr() + I * H * 2)
+    y_perm = torch.empty(T * k, H, dtype=torch.bfloat16, device="cuda")
+    m.moe_grouped_down(s, h, dev["w_down"], H * I, offsets, E, T * k, I, y_perm, ws)
+    one = torch.tensor([0, T], **i32)
+    hs = torch.empty(T, Ish, dtype=torch.bfloat16, device="cuda")
+    m.moe_grouped_swiglu(s, dev["x"], dev["sh_gate"], dev["sh_up"], 0, one, 1, T, Ish, hs, ws)
+    sh = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
+    m.moe_grouped_down(s, hs, dev["sh_down"], 0, one, 1, T, Ish, sh, ws)
+    y = torch.empty_like(dev["x"])
+    m.moe_combine(s, y_perm, sidx, tw, sh, gate, y)
+    torch.cuda.synchronize()
+    assert m.moe_get_device_status(ws)[0] == m.MOE_OK
+    assert torch.equal(y, y_ref)
+
+
+def test_bad_direct_route_sets_device_flag():
+    wl = W.small(W.ADV_ZIPF, T=64, H=256, I=128, I_sh=256)
+    dev = to_dev(W.make_inputs(wl, seed=0, device="cpu"))
+    dev["routes_idx"][5, 2] = wl.E + 3
+    layer = m.MoELayer(wl, dev)
+    y = layer.forward(dev["x"], routes_idx=dev["routes_idx"], routes_w=dev["routes_w"])
+    st, bits = layer.device_status()
+    assert st == m.MOE_ERR_DEVICE_ROUTE and bits & 1
+    assert int(layer.views()["counts"].sum()) == wl.T * wl.k - 1
+    assert bool(torch.isfinite(y).all())
+    assert layer.device_status()[0] == m.MOE_OK  # read-and-clear
+
+
+def test_rows_beyond_bound_set_device_flag():
+    wl = W.small(W.QWEN3_30B_A3B, T=64, H=256, I=128, E=4, k=2)
+    s = m.shape_for(wl)
+    ws = m.alloc_workspace(s, full=False)
+    offsets = torch.tensor([0, 40, 80, 100, 128], dtype=torch.int32, device="cuda")
+    xp = torch.randn(128, 256, device="cuda").bfloat16()
+    wg = torch.randn(4, 128, 256, device="cuda").bfloat16()
+    h = torch.full((128, 128), 7.0, device="cuda").bfloat16()
+    m.moe_grouped_swiglu(s, xp, wg, wg, 128 * 256, offsets, 4, 100, 128, h, ws)
+    assert m.moe_get_device_status(ws)[0] == m.MOE_ERR_ROWS
+    assert bool((h.float() == 7.0).all())  # nothing was computed
+
+
+def test_zero_tokens_is_a_no_op():
+    wl = W.small(W.QWEN3_30B_A3B, T=1, H=256, I=128, E=8, k=2)
+    dev = to_dev(W.make_inputs(wl, seed=0, device="cpu"))
+    s = m.shape_for(wl, T=0)
+    ws = m.alloc_workspace(s)
+    x = dev["x"][:0]
+    y = torch.empty_like(x)
+    m.moe_layer_forward(s, m.weights_from(dev), x, None, None, y, ws)
+    assert m.moe_last_launch_count() == 0
