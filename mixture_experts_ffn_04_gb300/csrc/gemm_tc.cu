@@ -451,7 +451,9 @@ int sm_count() {
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   using namespace tc;
   if (a.dtype != MOE_BF16 || encode_fn() == nullptr) return cudaErrorNotSupported;
-  if ((a.K % 8) != 0 || (a.N % 8) != 0 || a.K <= 0 || a.N <= 0) return cudaErrorInvalidValue;
+  // bf16 outputs are stored as 8-element vectors; fp32 outputs column by column
+  if ((a.K % 8) != 0 || (a.mode != kStoreF32 && (a.N % 8) != 0) || a.K <= 0 || a.N <= 0)
+    return cudaErrorInvalidValue;
   cudaError_t e = launch_schedule(a, BM, st);
   if (e != cudaSuccess) return e;
   const int64_t rows = a.offsets ? a.rows_bound : a.single_rows;
