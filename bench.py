@@ -204,8 +204,8 @@ def run_reference(args, wl, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def _config(wl):
-    return {"workload": wl.name, "tokens": wl.T, "hidden": wl.H, "experts": wl.E,
+def _config(wl, graph=None):
+    return {"workload": wl.name, "cuda_graph": graph, "tokens": wl.T, "hidden": wl.H, "experts": wl.E,
             "top_k": wl.k, "moe_inter": wl.I, "shared_inter": wl.I_sh,
             "shared_gate": wl.shared_gate, "norm_topk": wl.norm_topk, "routing": wl.routing,
             "l2": "flushed before every timed step (256 MiB device write)",
@@ -225,6 +225,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch every step from the host instead of replaying a CUDA graph")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -252,11 +254,9 @@ def main():
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     nst = len(m.STAGES)
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)]
-              for _ in range(args.steps)]
-    for evs in events:
-        for e in evs:
-            e.record(stream)   # materialise the CUDA events
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)]
+    for e in evs:
+        e.record(stream)   # materialise the CUDA events
     torch.cuda.synchronize()
 
     for _ in range(args.warmup):
@@ -268,6 +268,31 @@ def main():
         raise RuntimeError("device status %d (bits %#x) after warm-up" % (st, bits))
     launches_per_step = m.moe_last_launch_count()
 
+    # One step = [L2 flush, traced layer forward].  With --graph (default) the
+    # step is captured once as a CUDA graph and replayed, so the device never
+    # waits on host-side launch work; the kernels are the same.
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            flush.fill_(1)
+            m.moe_layer_forward_traced(layer.shape, layer.weights, x, ridx, rw, y, layer.ws,
+                                       evs)
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
+
+    def one_step():
+        if graph is not None:
+            graph.replay()
+        else:
+            flush.fill_(1)
+            m.moe_layer_forward_traced(layer.shape, layer.weights, x, ridx, rw, y, layer.ws,
+                                       evs, stream)
+        evs[nst].synchronize()
+        return ([evs[s].elapsed_time(evs[s + 1]) for s in range(nst)],
+                evs[0].elapsed_time(evs[nst]))
+
     clocks = Clocks(local)
     if dist is not None:
         dist.barrier()
@@ -275,10 +300,11 @@ def main():
     clocks.start()
     time.sleep(0.3)
     t_wall = time.perf_counter()
+    per_stage, step_ms = [], []
     for i in range(args.steps):
-        flush.fill_(1)
-        m.moe_layer_forward_traced(layer.shape, layer.weights, x, ridx, rw, y, layer.ws,
-                                   events[i], stream)
+        ps, tot = one_step()
+        per_stage.append(ps)
+        step_ms.append(tot)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     if dist is not None:
@@ -288,9 +314,7 @@ def main():
     if st != m.MOE_OK:
         raise RuntimeError("device status %d (bits %#x) in the timed region" % (st, bits))
 
-    step_ms = [events[i][0].elapsed_time(events[i][nst]) for i in range(args.steps)]
-    stage_ms = [statistics.mean(events[i][s].elapsed_time(events[i][s + 1])
-                                for i in range(args.steps)) for s in range(nst)]
+    stage_ms = [statistics.mean(p[s] for p in per_stage) for s in range(nst)]
     total_ms = sum(step_ms)
     if dist is not None:
         t = torch.tensor([total_ms], device="cuda")
@@ -358,7 +382,7 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if wl.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": _config(wl),
+        "config": _config(wl, graph is not None),
         "grouped_gemm_tflops": gemm_tflops,
         "grouped_gemm_frac_bf16_peak": gemm_tflops / peaks["bf16"],
         "layer_roofline_frac": layer_roof_ms / ms_per_step,

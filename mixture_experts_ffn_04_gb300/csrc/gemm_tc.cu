@@ -318,7 +318,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int64_t gend = a.offsets ? a.offsets[g + 1] : a.single_rows;
       const int64_t row = gbeg + (int64_t)mt * BM + r;
       const bool row_ok = row < gend;
-      if (!mbar_wait(tfull_bar(acc), aph, abort_flag)) break;
+      // all 32 lanes must agree before the warp-collective tcgen05.ld
+      if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, abort_flag))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * BN;
       if (a.mode == kSwiGLU) {
