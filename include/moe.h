@@ -167,6 +167,25 @@ moe_status moe_permute(const moe_shape *shape, const void *x, const int32_t *top
                        int32_t *row_token, void *x_perm, void *ws, size_t ws_bytes,
                        void *stream);
 
+/* moe_permute without a workspace, for callers that may not allocate device
+ * memory while they run (a plugin handed only its tensors, a real-time loop
+ * that forbids allocation after start-up since it can synchronise the device,
+ * memory already carved up by another owner).  No passage of the pages has a
+ * counterpart: this is a deployment variant of moe_permute, with the same
+ * arguments minus the workspace and the same outputs.
+ *  - Scratch: a 2 MiB static device array inside the library (held by every
+ *    GPU that loads it until exit); every valid shape fits, a shape that
+ *    would not is rejected with MOE_ERR_UNSUPPORTED and a message.
+ *  - Allocates nothing (no cudaMalloc/cudaFree, no allocating library call).
+ *  - The first call on a device looks up the array's device address with
+ *    that device current; make that first call before any stream capture.
+ *  - All calls share the array: calls that overlap on the GPU race.
+ *  - No device status word: a route outside [0, E) is dropped
+ *    (scatter_index -1, not counted), visible as offsets[E] < T*k. */
+moe_status moe_permute_static(const moe_shape *shape, const void *x, const int32_t *topk_idx,
+                              int32_t *counts, int32_t *offsets, int32_t *scatter_index,
+                              int32_t *row_token, void *x_perm, void *stream);
+
 /* Grouped GEMM gate/up with fused SwiGLU: for each group g < num_groups,
  * rows r in [offsets[g], offsets[g+1]) of x_perm [rows, H]:
  *   h[r, j] = silu(x_perm[r] . w_gate_g[j]) * (x_perm[r] . w_up_g[j]),  j < inter

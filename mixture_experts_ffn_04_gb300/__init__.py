@@ -78,6 +78,7 @@ def lib():
         "moe_workspace_init": (i32, [P, P]),
         "moe_route": (i32, [S, P, P, P, P, P, P, sz, P]),
         "moe_permute": (i32, [S, P, P, P, P, P, P, P, P, sz, P]),
+        "moe_permute_static": (i32, [S, P, P, P, P, P, P, P, P]),
         "moe_grouped_swiglu": (i32, [S, P, P, P, i64, P, i32, i64, i32, P, P, sz, P]),
         "moe_grouped_down": (i32, [S, P, P, i64, P, i32, i64, i32, P, P, sz, P]),
         "moe_combine": (i32, [S, P, P, P, P, P, P, P]),
@@ -196,6 +197,14 @@ def moe_permute(shape, x, topk_idx, counts, offsets, scatter_index, row_token, x
     _check(lib().moe_permute(ctypes.byref(shape), _p(x), _p(topk_idx), _p(counts), _p(offsets),
                              _p(scatter_index), _p(row_token), _p(x_perm), _p(ws),
                              ws.numel() * ws.element_size(), _stream(stream)), "moe_permute")
+
+
+def moe_permute_static(shape, x, topk_idx, counts, offsets, scatter_index, row_token, x_perm,
+                       stream=None):
+    """moe_permute with the library's static scratch instead of a workspace."""
+    _check(lib().moe_permute_static(ctypes.byref(shape), _p(x), _p(topk_idx), _p(counts),
+                                    _p(offsets), _p(scatter_index), _p(row_token), _p(x_perm),
+                                    _stream(stream)), "moe_permute_static")
 
 
 def moe_grouped_swiglu(shape, x_perm, w_gate, w_up, expert_stride, offsets, num_groups,

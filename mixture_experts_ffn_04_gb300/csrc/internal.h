@@ -80,6 +80,15 @@ cudaError_t launch_permute(const Shape& s, const Layout& L, char* ws, const void
                            int32_t* scatter_index, int32_t* row_token, void* x_perm,
                            cudaStream_t st);
 
+cudaError_t launch_permute_scratch(const Shape& s, int nchunks, int tpc, int32_t* hist,
+                                   int32_t* base, uint32_t* flags, const void* x,
+                                   const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
+                                   int32_t* scatter_index, int32_t* row_token, void* x_perm,
+                                   cudaStream_t st);
+
+// Record why the current host call failed (read back by moe_last_error).
+void set_error_message(const char* why);
+
 cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* scatter_index,
                            const float* topk_w, const void* shared_out, const float* gate,
                            void* y, cudaStream_t st);

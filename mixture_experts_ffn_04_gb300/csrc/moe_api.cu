@@ -21,6 +21,8 @@ void count_launch(int n) { tl_launches += n; }
 void reset_launch_count() { tl_launches = 0; }
 int gemm_path_override() { return g_engine.load(); }
 
+void set_error_message(const char* why) { tl_error = why; }
+
 static moe_status fail(moe_status st, const char* why) {
   tl_error = why;
   return st;

@@ -229,4 +229,59 @@ cudaError_t launch_permute(const Shape& s, const Layout& L, char* ws, const void
   return cudaGetLastError();
 }
 
+// Same three launches with caller-chosen scratch tables (hist and base, each
+// nchunks * E int32) and an optional status word; used by the allocation-free
+// entry point, whose scratch is a static device array.
+cudaError_t launch_permute_scratch(const Shape& s, int nchunks, int tpc, int32_t* hist,
+                                   int32_t* base, uint32_t* flags, const void* x,
+                                   const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
+                                   int32_t* scatter_index, int32_t* row_token, void* x_perm,
+                                   cudaStream_t st) {
+  if (s.T == 0) nchunks = 0;
+  cudaError_t e;
+  if (nchunks > 0) {
+    const size_t hsm = (size_t)s.E * 4;
+    if (hsm > 48 * 1024) {
+      e = cudaFuncSetAttribute(hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsm);
+      if (e != cudaSuccess) return e;
+    }
+    hist_kernel<<<nchunks, 256, hsm, st>>>(topk_idx, s.T, s.k, s.E, tpc, hist, flags);
+    count_launch();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  int S = 1;
+  if (s.E <= 1024 && nchunks > 0) S = 1024 / s.E < nchunks ? 1024 / s.E : nchunks;
+  const size_t ssm = (size_t)S * s.E * 4;
+  if (ssm > 48 * 1024) {
+    e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
+    if (e != cudaSuccess) return e;
+  }
+  scan_kernel<<<1, 1024, ssm, st>>>(hist, nchunks, s.E, S, base, counts, offsets);
+  count_launch();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (nchunks == 0) return cudaSuccess;
+  const size_t csm = ((size_t)s.E + (size_t)tpc * s.k) * 4;
+  if (s.dtype == MOE_F32) {
+    if (csm > 48 * 1024) {
+      e = cudaFuncSetAttribute(scatter_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)csm);
+      if (e != cudaSuccess) return e;
+    }
+    scatter_kernel<float><<<nchunks, 256, csm, st>>>(
+        reinterpret_cast<const float*>(x), topk_idx, s.T, s.k, s.E, s.H, tpc, base, scatter_index,
+        row_token, reinterpret_cast<float*>(x_perm));
+  } else {
+    if (csm > 48 * 1024) {
+      e = cudaFuncSetAttribute(scatter_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)csm);
+      if (e != cudaSuccess) return e;
+    }
+    scatter_kernel<bf16><<<nchunks, 256, csm, st>>>(
+        reinterpret_cast<const bf16*>(x), topk_idx, s.T, s.k, s.E, s.H, tpc, base, scatter_index,
+        row_token, reinterpret_cast<bf16*>(x_perm));
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
 }  // namespace moe
