@@ -355,6 +355,17 @@ moe_status moe_combine(const moe_shape* shape, const void* y_perm, const int32_t
   return MOE_OK;
 }
 
+// During stream capture an event record must become an external event node
+// of the graph (otherwise it only orders the capture and cannot be timed).
+static cudaError_t record_stage_event(void* ev, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(st, &cs);
+  if (e != cudaSuccess) return e;
+  return cudaEventRecordWithFlags(static_cast<cudaEvent_t>(ev), st,
+                                  cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal
+                                                                      : cudaEventRecordDefault);
+}
+
 moe_status moe_layer_forward(const moe_shape* shape, const moe_weights* W, const void* x,
                              const int32_t* routes_idx, const float* routes_w, void* y, void* ws,
                              size_t ws_bytes, void* stream) {
@@ -401,7 +412,7 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
   const int32_t* use_idx = idx;
   const float* use_w = tw;
 #define STAGE_EVENT(i) \
-  if (ev) CHECK_CUDA(cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st))
+  if (ev) CHECK_CUDA(record_stage_event(ev[i], st))
   STAGE_EVENT(MOE_STAGE_ROUTE);
   if (direct) {
     use_idx = routes_idx;
