@@ -65,6 +65,21 @@ def _dist():
     return None, 0, 1
 
 
+def max_over_ranks(v: float, dist) -> float:
+    """The slowest rank's value (the job is done when the last replica is)."""
+    if dist is None:
+        return v
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every rank runs its own batch of tokens (weak scaling)."""
+    return world * tokens_per_rank / (ms_per_step / 1000.0)
+
+
 class Clocks:
     """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
     Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -315,13 +330,9 @@ def main():
         raise RuntimeError("device status %d (bits %#x) in the timed region" % (st, bits))
 
     stage_ms = [statistics.mean(p[s] for p in per_stage) for s in range(nst)]
-    total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dist)
     ms_per_step = total_ms / args.steps
-    value = world * wl.T / (ms_per_step / 1000.0)
+    value = replica_throughput(world, wl.T, ms_per_step)
 
     # ---- end to end through the public API, host buffers -------------------
     x_host = x.cpu().pin_memory()

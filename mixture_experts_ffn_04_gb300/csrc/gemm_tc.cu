@@ -42,7 +42,9 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES;
+constexpr int MAX_SMEM_G = 1024;   // larger group counts use a schedule kernel
+constexpr int SCHED_BYTES = (MAX_SMEM_G + 1) * 4;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + SCHED_BYTES;
 // kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
 // B bf16 (10-12 = 1), both K-major (15, 16 = 0), N >> 3 at 17-22, M >> 4 at 24-28.
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
@@ -53,10 +55,13 @@ struct TcArgs {
   int mode, N, K, G, NT, KB;
   const int32_t* offsets;
   int64_t single_rows;
-  const int32_t* sched;
+  int64_t rows_bound;
+  const int32_t* sched;   // global m-tile prefix, or NULL: built in shared memory
   void* out;
   int64_t ldo;
   uint32_t* flags;
+  int ksplit;             // >1 only for fp32 outputs: partial sums per K range
+  int64_t split_stride;   // floats between partial outputs
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -180,18 +185,59 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return d;
 }
 
-__device__ __forceinline__ void decode_tile(const TcArgs& a, int64_t tile, int& g, int& mt,
-                                            int& nt) {
+// Tile -> (K split, group, m-tile, n-tile).  Within a split, tiles of one
+// group are ordered n-tile major, m-tile minor, so the CTAs sharing a weight
+// tile run side by side.
+__device__ __forceinline__ void decode_tile(const TcArgs& a, const int32_t* sched, int64_t tile,
+                                            int& ks, int& g, int& mt, int& nt) {
+  const int64_t per_split = (int64_t)sched[a.G] * a.NT;
+  ks = (int)(tile / per_split);
+  tile -= (int64_t)ks * per_split;
   int lo = 0, hi = a.G;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if ((int64_t)a.sched[mid] * a.NT <= tile) lo = mid; else hi = mid;
+    if ((int64_t)sched[mid] * a.NT <= tile) lo = mid; else hi = mid;
   }
   g = lo;
-  const int mtg = a.sched[g + 1] - a.sched[g];
-  const int64_t local = tile - (int64_t)a.sched[g] * a.NT;
+  const int mtg = sched[g + 1] - sched[g];
+  const int64_t local = tile - (int64_t)sched[g] * a.NT;
   nt = (int)(local / mtg);
   mt = (int)(local % mtg);
+}
+
+// m-tile prefix of the groups, built by one warp into shared memory:
+// sched[g] = sum over g' < g of ceil(rows_g' / BM); sched[G] = total, or 0 when
+// the offsets are inconsistent or exceed the row bound (then nothing runs and
+// CTA 0 raises the device flag).
+__device__ void build_schedule(const TcArgs& a, int32_t* sched, int lane) {
+  int carry = 0;
+  bool bad = false;
+  for (int base = 0; base < a.G; base += 32) {
+    const int g = base + lane;
+    int v = 0;
+    if (g < a.G) {
+      int64_t cnt = a.offsets ? (int64_t)a.offsets[g + 1] - a.offsets[g] : a.single_rows;
+      if (cnt < 0) { bad = true; cnt = 0; }
+      v = (int)((cnt + BM - 1) / BM);
+    }
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (g < a.G) sched[g] = carry + incl - v;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) {
+    if (a.offsets) bad |= a.offsets[0] != 0 || (int64_t)a.offsets[a.G] > a.rows_bound;
+    else bad |= a.single_rows > a.rows_bound || a.single_rows < 0;
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  if (lane == 0) {
+    sched[a.G] = bad ? 0 : carry;
+    if (bad && blockIdx.x == 0) set_flag(a.flags, kFlagRows);
+  }
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -204,6 +250,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   // bars: full[0..S), empty[S..2S), tfull[2S..2S+2), tempty[2S+2..2S+4), final[2S+4]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* s_sched = reinterpret_cast<int32_t*>(smem + STAGES * STAGE_BYTES + BAR_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
@@ -231,12 +278,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish();
   }
+  if (warp == 2 && a.sched == nullptr) build_schedule(a, s_sched, lane);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const int32_t* sched = a.sched ? a.sched : s_sched;
 
-  const int64_t total = (int64_t)a.sched[a.G] * a.NT;
+  const int64_t total = (int64_t)sched[a.G] * a.NT * a.ksplit;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -245,11 +294,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t ph = 0, issued = 0, par = 0;
       bool ok = true;
       for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        int g, mt, nt;
-        decode_tile(a, tile, g, mt, nt);
+        int ks, g, mt, nt;
+        decode_tile(a, sched, tile, ks, g, mt, nt);
         const int64_t gbase = a.offsets ? a.offsets[g] : 0;
         const int arow = (int)(gbase + (int64_t)mt * BM);
-        for (int kb = 0; kb < a.KB; ++kb) {
+        const int kb0 = ks * a.KB / a.ksplit, kb1 = (ks + 1) * a.KB / a.ksplit;
+        for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) { ok = false; break; }
           const uint32_t sa = smem_base + s * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
@@ -279,10 +329,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t ph = 0, aph = 0;
       bool ok = true;
       for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const int ks = (int)(tile / ((int64_t)sched[a.G] * a.NT));
+        const int nkb = (ks + 1) * a.KB / a.ksplit - ks * a.KB / a.ksplit;
         if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)acc * BN;
-        for (int kb = 0; kb < a.KB; ++kb) {
+        for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(full_bar(s), ph, abort_flag)) { ok = false; break; }
           tc_fence_after();
           const uint32_t sa = smem_base + s * STAGE_BYTES;
@@ -312,8 +364,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     int acc = 0;
     uint32_t aph = 0;
     for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      int g, mt, nt;
-      decode_tile(a, tile, g, mt, nt);
+      int ks, g, mt, nt;
+      decode_tile(a, sched, tile, ks, g, mt, nt);
       const int64_t gbeg = a.offsets ? a.offsets[g] : 0;
       const int64_t gend = a.offsets ? a.offsets[g + 1] : a.single_rows;
       const int64_t row = gbeg + (int64_t)mt * BM + r;
@@ -368,7 +420,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       } else {
         const int n0 = nt * BN;
-        float* out = reinterpret_cast<float*>(a.out) + row * a.ldo;
+        float* out = reinterpret_cast<float*>(a.out) + ks * a.split_stride + row * a.ldo;
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
           uint32_t vr[32];
@@ -449,14 +501,28 @@ int sm_count() {
 
 }  // namespace tc
 
+int router_split(int64_t rows, int ncols, int K) {
+  const int64_t base = ((rows + tc::BM - 1) / tc::BM) * ((ncols + tc::BN - 1) / tc::BN);
+  const int kb = (K + tc::BK - 1) / tc::BK;
+  int64_t s = base > 0 ? tc::sm_count() / base : 1;
+  if (s > kMaxSplit) s = kMaxSplit;
+  if (s > kb / 4) s = kb / 4;
+  return s < 1 ? 1 : (int)s;
+}
+
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   using namespace tc;
   if (a.dtype != MOE_BF16 || encode_fn() == nullptr) return cudaErrorNotSupported;
   // bf16 outputs are stored as 8-element vectors; fp32 outputs column by column
   if ((a.K % 8) != 0 || (a.mode != kStoreF32 && (a.N % 8) != 0) || a.K <= 0 || a.N <= 0)
     return cudaErrorInvalidValue;
-  cudaError_t e = launch_schedule(a, BM, st);
-  if (e != cudaSuccess) return e;
+  if (a.ksplit < 1 || (a.ksplit > 1 && a.mode != kStoreF32)) return cudaErrorInvalidValue;
+  cudaError_t e;
+  const bool smem_sched = a.G <= MAX_SMEM_G;
+  if (!smem_sched) {
+    e = launch_schedule(a, BM, st);
+    if (e != cudaSuccess) return e;
+  }
   const int64_t rows = a.offsets ? a.rows_bound : a.single_rows;
   if (rows <= 0) return cudaSuccess;
   const int brows = a.mode == kSwiGLU ? BN / 2 : BN;
@@ -477,12 +543,15 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   t.KB = (a.K + BK - 1) / BK;
   t.offsets = a.offsets;
   t.single_rows = a.single_rows;
-  t.sched = a.sched;
+  t.rows_bound = a.rows_bound;
+  t.sched = smem_sched ? nullptr : a.sched;
+  t.ksplit = a.ksplit;
+  t.split_stride = a.split_stride;
   t.out = a.out;
   t.ldo = a.ldo;
   t.flags = a.flags;
   const int64_t mt_bound = a.offsets ? (a.rows_bound + BM - 1) / BM + a.G : (a.single_rows + BM - 1) / BM;
-  const int64_t tiles_bound = mt_bound * t.NT;
+  const int64_t tiles_bound = mt_bound * t.NT * t.ksplit;
   static bool attr_done = false;
   if (!attr_done) {
     e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);

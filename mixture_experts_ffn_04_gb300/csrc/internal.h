@@ -64,6 +64,8 @@ struct GemmArgs {
   int64_t ldo;             // elements
   int32_t* sched;          // [G + 1] scratch for the m-tile prefix
   uint32_t* flags;
+  int ksplit = 1;          // kStoreF32 only: partial sums over K ranges,
+  int64_t split_stride = 0;  // written split_stride floats apart
 };
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t st);
@@ -72,8 +74,15 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_schedule(const GemmArgs& a, int bm, cudaStream_t st);
 
-cudaError_t launch_topk(const Shape& s, const float* logits, const void* x, const void* w_router,
-                        int32_t* topk_idx, float* topk_w, float* gate, cudaStream_t st);
+// logits: nsplit partial sums of [T, ldl] floats, T * ldl apart.
+cudaError_t launch_topk(const Shape& s, const float* logits, int nsplit, const void* x,
+                        const void* w_router, int32_t* topk_idx, float* topk_w, float* gate,
+                        cudaStream_t st);
+
+// Split-K factor for a tensor-core fp32-output GEMM of one group (router):
+// enough CTAs to cover the SMs, at most kMaxSplit, at least 4 k-blocks each.
+constexpr int kMaxSplit = 8;
+int router_split(int64_t rows, int ncols, int K);
 
 cudaError_t launch_permute(const Shape& s, const Layout& L, char* ws, const void* x,
                            const int32_t* topk_idx, int32_t* counts, int32_t* offsets,

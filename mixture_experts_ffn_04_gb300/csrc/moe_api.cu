@@ -89,7 +89,7 @@ Layout layout_for(const Shape& s) {
   size_t off = 0;
   const size_t T = (size_t)s.T, k = (size_t)s.k, E = (size_t)s.E;
   L.flags = off; off += 256;
-  L.logits = off; off += align256(T * (size_t)s.ldl * 4);
+  L.logits = off; off += align256((size_t)kMaxSplit * T * (size_t)s.ldl * 4);
   int64_t nchunks = (s.T + 15) / 16;
   int64_t cap = 262144 / s.E;
   if (cap < 1) cap = 1;
@@ -120,18 +120,21 @@ Layout layout_for(const Shape& s) {
   return L;
 }
 
-cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t st) {
+// Engine for a grouped GEMM: 1 CUDA-core tiles, 2 tensor cores, 3 skinny.
+static int engine_for(const GemmArgs& a) {
   const int ov = gemm_path_override();
   const int64_t rows = a.offsets ? a.rows_bound : a.single_rows;
-  if (a.dtype == MOE_F32) return ov == 3 ? launch_gemm_skinny(a, st) : launch_gemm_simt(a, 64, st);
-  switch (ov) {
+  if (a.dtype == MOE_F32) return ov == 3 ? 3 : 1;
+  if (ov >= 1 && ov <= 3) return ov;
+  return rows <= 16 ? 3 : 2;
+}
+
+cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t st) {
+  switch (engine_for(a)) {
     case 1: return launch_gemm_simt(a, 64, st);
     case 2: return launch_gemm_tc(a, st);
-    case 3: return launch_gemm_skinny(a, st);
-    default: break;
+    default: return launch_gemm_skinny(a, st);
   }
-  if (rows <= 16) return launch_gemm_skinny(a, st);
-  return launch_gemm_tc(a, st);
 }
 
 }  // namespace moe
@@ -242,8 +245,12 @@ static moe_status do_route(const Shape& s, const Layout& L, char* w, const void*
   ra.ldo = s.ldl;
   ra.sched = reinterpret_cast<int32_t*>(w + L.sched_router);
   ra.flags = reinterpret_cast<uint32_t*>(w + L.flags);
+  // On the tensor cores the router is split over K so that its few m-tiles
+  // still cover the SMs; the top-k kernel adds the partial sums in order.
+  ra.ksplit = engine_for(ra) == 2 ? router_split(s.T, s.ncols, s.H) : 1;
+  ra.split_stride = s.T * (int64_t)s.ldl;
   CHECK_CUDA(launch_grouped_gemm(ra, st));
-  CHECK_CUDA(launch_topk(s, logits, x, router, idx, tw, gate, st));
+  CHECK_CUDA(launch_topk(s, logits, ra.ksplit, x, router, idx, tw, gate, st));
   return MOE_OK;
 }
 

@@ -57,6 +57,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
     const int e = it % E, seg = it / E;
     const int c0 = (int)((int64_t)nchunks * seg / S), c1 = (int)((int64_t)nchunks * (seg + 1) / S);
     int32_t s = 0;
+#pragma unroll 16
     for (int c = c0; c < c1; ++c) s += hist[(int64_t)c * E + e];
     segsum[seg * E + e] = s;
   }
@@ -108,6 +109,7 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
     const int e = it % E, seg = it / E;
     const int c0 = (int)((int64_t)nchunks * seg / S), c1 = (int)((int64_t)nchunks * (seg + 1) / S);
     int32_t run = offsets[e] + segsum[seg * E + e];
+#pragma unroll 16
     for (int c = c0; c < c1; ++c) {
       const int64_t at = (int64_t)c * E + e;
       const int32_t v = hist[at];

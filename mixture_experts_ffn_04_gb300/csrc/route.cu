@@ -32,8 +32,10 @@ constexpr int kMaxRounds = 256;  // k <= 255 plus one round for the boundary
 constexpr int kMaxCand = 64;     // experts re-evaluated in a near tie
 
 struct TopkArgs {
-  const float* logits;
+  const float* logits;  // nsplit partial sums, split_stride floats apart
   int ldl;
+  int nsplit;
+  int64_t split_stride;
   const void* x;
   const void* w;  // router [ncols, H]
   int H, E, k, norm, gated;
@@ -88,25 +90,48 @@ __device__ __forceinline__ void two_prod(float a, float b, float& p, float& e) {
   e = __fmaf_rn(a, b, -p);
 }
 
-// Dot2 of row x and router row w over H, cooperatively by the warp.
+// Dot2 of row x and router row w over H, cooperatively by the warp: each lane
+// streams 16-byte chunks and keeps one (sum, compensation) pair per vector
+// position, so the dependent chains are short and loads stay in flight; the
+// pairs are merged with TwoSum across positions and then across lanes.
 template <typename T>
 __device__ double dot2(const T* x, const T* w, int H, int lane) {
-  float p = 0.f, s = 0.f;
-  for (int h = lane; h < H; h += 32) {
-    float hp, r, q;
-    two_prod(to_f(x[h]), to_f(w[h]), hp, r);
-    two_sum(p, hp, p, q);
-    s = __fadd_rn(s, __fadd_rn(q, r));
+  constexpr int V = 16 / sizeof(T);
+  float p[V], s[V];
+#pragma unroll
+  for (int i = 0; i < V; ++i) p[i] = s[i] = 0.f;
+  const int nv = H / V;
+  const uint4* xv = reinterpret_cast<const uint4*>(x);
+  const uint4* wv = reinterpret_cast<const uint4*>(w);
+#pragma unroll 4
+  for (int c = lane; c < nv; c += 32) {
+    float xf[V], wf[V];
+    unpack16(__ldg(xv + c), xf, (const T*)nullptr);
+    unpack16(__ldg(wv + c), wf, (const T*)nullptr);
+#pragma unroll
+    for (int i = 0; i < V; ++i) {
+      float hp, r, q;
+      two_prod(xf[i], wf[i], hp, r);
+      two_sum(p[i], hp, p[i], q);
+      s[i] = __fadd_rn(s[i], __fadd_rn(q, r));
+    }
+  }
+  float P = p[0], S = s[0];
+#pragma unroll
+  for (int i = 1; i < V; ++i) {
+    float q;
+    two_sum(P, p[i], P, q);
+    S = __fadd_rn(S, __fadd_rn(s[i], q));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
-    float op = __shfl_xor_sync(0xffffffffu, p, o);
-    float os = __shfl_xor_sync(0xffffffffu, s, o);
+    float op = __shfl_xor_sync(0xffffffffu, P, o);
+    float os = __shfl_xor_sync(0xffffffffu, S, o);
     float q;
-    two_sum(p, op, p, q);
-    s = __fadd_rn(__fadd_rn(s, os), q);
+    two_sum(P, op, P, q);
+    S = __fadd_rn(__fadd_rn(S, os), q);
   }
-  return (double)p + (double)s;
+  return (double)P + (double)S;
 }
 
 template <typename T>
@@ -127,10 +152,12 @@ __global__ void topk_kernel(TopkArgs a) {
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + wid;
   if (t >= a.T) return;
 
+  // logits = sum of the split-K partials, always in split order
   const float* row = a.logits + t * a.ldl;
   float m = -INFINITY;
   for (int e = lane; e < E; e += 32) {
     float v = row[e];
+    for (int sp = 1; sp < a.nsplit; ++sp) v += row[sp * a.split_stride + e];
     sm.buf[e] = v;
     m = fmaxf(m, v);
   }
@@ -163,9 +190,12 @@ __global__ void topk_kernel(TopkArgs a) {
   for (int r = lane; r + 1 < R; r += 32) near |= (sm.sel_v[r] - sm.sel_v[r + 1]) < tau;
   near = __any_sync(0xffffffffu, near);
   if (near && a.x != nullptr) {
-    // candidates: every expert within tau below the boundary value, plus above
+    // L = every expert within tau below the boundary value (so all of the
+    // top R, plus the ones just under it).  Only members of L closer than tau
+    // to another member can swap places; they are re-evaluated exactly, the
+    // rest keep their fp32 value (every comparison they take part in is
+    // decided by a margin of at least tau).
     int nc = 0;
-    bool overflow = false;
     for (int e0 = 0; e0 < E; e0 += 32) {
       int e = e0 + lane;
       bool c = e < E && sm.buf[e] >= vb - tau;
@@ -174,37 +204,49 @@ __global__ void topk_kernel(TopkArgs a) {
       if (c && pos < kMaxCand) sm.cand_i[pos] = e;
       nc += __popc(msk);
     }
-    if (nc > kMaxCand) overflow = true;
     __syncwarp();
-    if (!overflow) {
+    if (nc <= kMaxCand) {
+      unsigned long long marked = 0ull;
+      for (int c = lane; c < nc; c += 32) {
+        const float vc = sm.buf[sm.cand_i[c]];
+        bool mk = false;
+        for (int o = 0; o < nc; ++o)
+          mk |= (o != c) && fabsf(vc - sm.buf[sm.cand_i[o]]) < tau;
+        sm.cand_v[c] = (double)vc;
+        if (mk) marked |= 1ull << c;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) marked |= __shfl_xor_sync(0xffffffffu, marked, o);
+      __syncwarp();
       const T* xr = reinterpret_cast<const T*>(a.x) + t * a.H;
-      for (int c = 0; c < nc; ++c) {
+      for (unsigned long long mm = marked; mm; mm &= mm - 1) {
+        const int c = __ffsll((long long)mm) - 1;
         const T* wr = reinterpret_cast<const T*>(a.w) + (int64_t)sm.cand_i[c] * a.H;
-        double v = dot2<T>(xr, wr, a.H, lane);
+        const double v = dot2<T>(xr, wr, a.H, lane);
         if (lane == 0) sm.cand_v[c] = v;
       }
       __syncwarp();
-      // Every non-candidate lies more than tau below the boundary, so the top
-      // R experts are all candidates: redo the rounds among them exactly.
-      uint64_t used = 0ull;  // candidate c taken (nc <= 64)
+      // Redo the R rounds among L on these keys (every expert outside L lies
+      // more than tau below the boundary, so the top R are all in L).
+      unsigned long long used = 0ull;
       for (int r = 0; r < R && r < nc; ++r) {
         double bv2 = -INFINITY;
         int bi2 = 0x7fffffff, bc = -1;
         for (int c = lane; c < nc; c += 32) {
           if (used & (1ull << c)) continue;
-          double v = sm.cand_v[c];
-          int e = sm.cand_i[c];
+          const double v = sm.cand_v[c];
+          const int e = sm.cand_i[c];
           if (bc < 0 || v > bv2 || (v == bv2 && e < bi2)) { bv2 = v; bi2 = e; bc = c; }
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
-          double ov = __shfl_xor_sync(0xffffffffu, bv2, o);
-          int oi = __shfl_xor_sync(0xffffffffu, bi2, o);
-          int oc = __shfl_xor_sync(0xffffffffu, bc, o);
-          bool take = (bc < 0 && oc >= 0) ||
-                      (oc >= 0 && (ov > bv2 || (ov == bv2 && oi < bi2)));
+          const double ov = __shfl_xor_sync(0xffffffffu, bv2, o);
+          const int oi = __shfl_xor_sync(0xffffffffu, bi2, o);
+          const int oc = __shfl_xor_sync(0xffffffffu, bc, o);
+          const bool take = oc >= 0 && (bc < 0 || ov > bv2 || (ov == bv2 && oi < bi2));
           if (take) { bv2 = ov; bi2 = oi; bc = oc; }
         }
+        if (bc < 0) break;
         used |= 1ull << bc;
         if (lane == 0) {
           sm.sel_i[r] = bi2;
@@ -232,19 +274,23 @@ __global__ void topk_kernel(TopkArgs a) {
     a.wout[t * k + s] = expf(sm.sel_v[s] - ref) / denom;
   }
   if (a.gated && lane == 0) {
-    const float z = row[E];
+    float z = row[E];
+    for (int sp = 1; sp < a.nsplit; ++sp) z += row[sp * a.split_stride + E];
     a.gate[t] = 1.0f / (1.0f + expf(-z));
   }
 }
 
 }  // namespace
 
-cudaError_t launch_topk(const Shape& s, const float* logits, const void* x, const void* w_router,
-                        int32_t* topk_idx, float* topk_w, float* gate, cudaStream_t st) {
+cudaError_t launch_topk(const Shape& s, const float* logits, int nsplit, const void* x,
+                        const void* w_router, int32_t* topk_idx, float* topk_w, float* gate,
+                        cudaStream_t st) {
   if (s.T == 0) return cudaSuccess;
   TopkArgs a;
   a.logits = logits;
   a.ldl = s.ldl;
+  a.nsplit = nsplit;
+  a.split_stride = s.T * (int64_t)s.ldl;
   a.x = x;
   a.w = w_router;
   a.H = s.H;

@@ -128,4 +128,4 @@ def test_workspace_layout_scales(m):
     T, k, H, I = 8192, 8, 7168, 2048
     inter = 2 * T * k * H * 2 + T * k * I * 2
     assert inter <= m.moe_workspace_bytes(s) <= inter * 1.2
-    assert m.moe_scratch_bytes(s) < 64 << 20
+    assert m.moe_scratch_bytes(s) < 128 << 20   # split-K router partials dominate
