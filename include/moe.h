@@ -252,6 +252,11 @@ moe_status moe_workspace_init(void *ws, void *stream);
  * MOE_ERR_TIMEOUT that is set (*bits, if non-NULL, receives every bit). */
 moe_status moe_get_device_status(void *ws, void *stream, uint32_t *bits);
 
+/* Synchronise `stream`, then read and clear the workspace's count of tokens
+ * whose top-k order was re-decided with the exact compensated dot product
+ * (neighbouring fp32 logits closer than the error bound; see moe_route). */
+moe_status moe_get_route_stats(void *ws, void *stream, uint32_t *redecided);
+
 /* Static strings; never NULL. */
 const char *moe_status_string(moe_status status);
 /* Why the last call from this thread that failed host-side validation was

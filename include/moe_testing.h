@@ -10,7 +10,10 @@
 #ifndef MOE_TESTING_H_
 #define MOE_TESTING_H_
 
+#include <stddef.h>
 #include <stdint.h>
+
+#include "moe.h"
 
 #ifdef __cplusplus
 extern "C" {
@@ -21,6 +24,13 @@ extern "C" {
  * fp32 layers always use the CUDA-core engine (values other than 0 and 3 are
  * ignored for them). */
 int32_t moe_testing_set_gemm_engine(int32_t engine);
+
+/* The router logits moe_route decides on: the router GEMM exactly as
+ * moe_route runs it (same engine and K split), with the partial sums added in
+ * the same order, written to logits [T, E + shared_gate] (fp32, device).
+ * Lets tests measure the fp32 logit error against exact dot products. */
+moe_status moe_testing_router_logits(const moe_shape *shape, const void *x, const void *w_router,
+                                     float *logits, void *ws, size_t ws_bytes, void *stream);
 
 #ifdef __cplusplus
 }

@@ -91,6 +91,8 @@ def lib():
         "moe_stage_name": (ctypes.c_char_p, [i32]),
         "moe_last_launch_count": (i32, []),
         "moe_testing_set_gemm_engine": (i32, [i32]),
+        "moe_get_route_stats": (i32, [P, P, ctypes.POINTER(u32)]),
+        "moe_testing_router_logits": (i32, [S, P, P, P, P, sz, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -251,6 +253,20 @@ def moe_get_device_status(ws, stream=None):
     bits = ctypes.c_uint32(0)
     st = lib().moe_get_device_status(_p(ws), _stream(stream), ctypes.byref(bits))
     return int(st), int(bits.value)
+
+
+def moe_get_route_stats(ws, stream=None) -> int:
+    """Read and clear the count of tokens whose top-k was re-decided exactly."""
+    n = ctypes.c_uint32(0)
+    _check(lib().moe_get_route_stats(_p(ws), _stream(stream), ctypes.byref(n)),
+           "moe_get_route_stats")
+    return int(n.value)
+
+
+def moe_testing_router_logits(shape, x, w_router, logits, ws, stream=None):
+    _check(lib().moe_testing_router_logits(ctypes.byref(shape), _p(x), _p(w_router), _p(logits),
+                                           _p(ws), ws.numel() * ws.element_size(),
+                                           _stream(stream)), "moe_testing_router_logits")
 
 
 def moe_status_string(status: int) -> str:

@@ -50,7 +50,6 @@ constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + SCHED_BYTES
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
                            ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 constexpr long long kWaitCycles = 4000000000LL;
-constexpr int PREFETCH_AHEAD = 8;   // k-blocks the L2 prefetch runs ahead of the loads
 
 struct TcArgs {
   int mode, N, K, G, NT, KB;
@@ -124,21 +123,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
-}
-
-// L2 prefetch of the box a tensor-map load would fetch (no shared memory, no
-// barrier): the producer runs these ahead of its loads to hide DRAM latency.
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1)
-               : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() {
@@ -256,44 +240,6 @@ __device__ void build_schedule(const TcArgs& a, int32_t* sched, int lane) {
   }
 }
 
-// Position of the producer in this CTA's sequence of (tile, k-block) loads.
-struct Cursor {
-  int64_t tile;
-  int kb, kb1, g, nt, arow;
-  bool valid;
-};
-
-__device__ __forceinline__ void cursor_tile(const TcArgs& a, const int32_t* sched, int64_t total,
-                                            Cursor& c) {
-  c.valid = c.tile < total;
-  if (!c.valid) return;
-  int ks, mt;
-  decode_tile(a, sched, c.tile, ks, c.g, mt, c.nt);
-  const int64_t gbase = a.offsets ? a.offsets[c.g] : 0;
-  c.arow = (int)(gbase + (int64_t)mt * BM);
-  c.kb = ks * a.KB / a.ksplit;
-  c.kb1 = (ks + 1) * a.KB / a.ksplit;
-}
-
-__device__ __forceinline__ void cursor_next(const TcArgs& a, const int32_t* sched, int64_t total,
-                                            Cursor& c) {
-  if (++c.kb < c.kb1) return;
-  c.tile += gridDim.x;
-  cursor_tile(a, sched, total, c);
-}
-
-__device__ __forceinline__ void prefetch_at(const TcArgs& a, const Cursor& c,
-                                            const CUtensorMap* mA, const CUtensorMap* mB0,
-                                            const CUtensorMap* mB1) {
-  tma_prefetch_2d(mA, c.kb * BK, c.arow);
-  if (a.mode == kSwiGLU) {
-    tma_prefetch_3d(mB0, c.kb * BK, c.nt * (BN / 2), c.g);
-    tma_prefetch_3d(mB1, c.kb * BK, c.nt * (BN / 2), c.g);
-  } else {
-    tma_prefetch_3d(mB0, c.kb * BK, c.nt * BN, c.g);
-  }
-}
-
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, const TcArgs a) {
@@ -346,34 +292,30 @@ __global__ void __launch_bounds__(THREADS, 1)
       // ---------------- TMA producer ----------------
       int s = 0;
       uint32_t ph = 0, issued = 0, par = 0;
-      Cursor ld, pf;
-      ld.tile = pf.tile = blockIdx.x;
-      cursor_tile(a, sched, total, ld);
-      cursor_tile(a, sched, total, pf);
-      for (int i = 0; i < PREFETCH_AHEAD && pf.valid; ++i) {
-        prefetch_at(a, pf, &tmA, &tmB0, &tmB1);
-        cursor_next(a, sched, total, pf);
-      }
-      while (ld.valid) {
-        if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) break;
-        const uint32_t sa = smem_base + s * STAGE_BYTES;
-        const uint32_t sb = sa + A_BYTES;
-        mbar_expect_tx(full_bar(s), STAGE_BYTES);
-        tma_load_2d(sa, &tmA, ld.kb * BK, ld.arow, full_bar(s));
-        if (a.mode == kSwiGLU) {
-          tma_load_3d(sb, &tmB0, ld.kb * BK, ld.nt * (BN / 2), ld.g, full_bar(s));
-          tma_load_3d(sb + B_BYTES / 2, &tmB1, ld.kb * BK, ld.nt * (BN / 2), ld.g, full_bar(s));
-        } else {
-          tma_load_3d(sb, &tmB0, ld.kb * BK, ld.nt * BN, ld.g, full_bar(s));
+      for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        int ks, g, mt, nt;
+        decode_tile(a, sched, tile, ks, g, mt, nt);
+        const int64_t gbase = a.offsets ? a.offsets[g] : 0;
+        const int arow = (int)(gbase + (int64_t)mt * BM);
+        const int kb0 = ks * a.KB / a.ksplit, kb1 = (ks + 1) * a.KB / a.ksplit;
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) { ok = false; break; }
+          const uint32_t sa = smem_base + s * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          mbar_expect_tx(full_bar(s), STAGE_BYTES);
+          tma_load_2d(sa, &tmA, kb * BK, arow, full_bar(s));
+          if (a.mode == kSwiGLU) {
+            tma_load_3d(sb, &tmB0, kb * BK, nt * (BN / 2), g, full_bar(s));
+            tma_load_3d(sb + B_BYTES / 2, &tmB1, kb * BK, nt * (BN / 2), g, full_bar(s));
+          } else {
+            tma_load_3d(sb, &tmB0, kb * BK, nt * BN, g, full_bar(s));
+          }
+          issued |= 1u << s;
+          par = (par & ~(1u << s)) | (ph << s);
+          if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
-        issued |= 1u << s;
-        par = (par & ~(1u << s)) | (ph << s);
-        if (++s == STAGES) { s = 0; ph ^= 1u; }
-        cursor_next(a, sched, total, ld);
-        if (pf.valid) {
-          prefetch_at(a, pf, &tmA, &tmB0, &tmB1);
-          cursor_next(a, sched, total, pf);
-        }
+        if (!ok) break;
       }
       if (*abort_flag) {
         // let every load still in flight land before the CTA goes away
@@ -437,7 +379,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int n0 = nt * (BN / 2);
         bf16* out = reinterpret_cast<bf16*>(a.out) + row * a.ldo;
 #pragma unroll 1
-        for (int c = 0; c < BN / 2; c += 32) {
+        for (int c = 0; c < BN / 2 && n0 + c < a.N; c += 32) {
           uint32_t gr[32], ur[32];
           tmem_ld32(taddr + c, gr);
           tmem_ld32(taddr + BN / 2 + c, ur);
@@ -460,7 +402,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int n0 = nt * BN;
         bf16* out = reinterpret_cast<bf16*>(a.out) + row * a.ldo;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = 0; c < BN && n0 + c < a.N; c += 32) {
           uint32_t vr[32];
           tmem_ld32(taddr + c, vr);
           tmem_wait_ld();
@@ -478,17 +420,28 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
         }
       } else {
+        // fp32 rows (router logits): ldo and split_stride are multiples of 4
         const int n0 = nt * BN;
         float* out = reinterpret_cast<float*>(a.out) + ks * a.split_stride + row * a.ldo;
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = 0; c < BN && n0 + c < a.N; c += 32) {
           uint32_t vr[32];
           tmem_ld32(taddr + c, vr);
           tmem_wait_ld();
           if (row_ok) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e)
-              if (n0 + c + e < a.N) out[n0 + c + e] = __uint_as_float(vr[e]);
+            for (int e = 0; e < 32; e += 4) {
+              const int n = n0 + c + e;
+              if (n + 3 < a.N) {
+                *reinterpret_cast<float4*>(out + n) =
+                    make_float4(__uint_as_float(vr[e]), __uint_as_float(vr[e + 1]),
+                                __uint_as_float(vr[e + 2]), __uint_as_float(vr[e + 3]));
+              } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  if (n + q < a.N) out[n + q] = __uint_as_float(vr[e + q]);
+              }
+            }
           }
         }
       }

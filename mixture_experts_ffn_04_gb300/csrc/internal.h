@@ -77,7 +77,9 @@ cudaError_t launch_schedule(const GemmArgs& a, int bm, cudaStream_t st);
 // logits: nsplit partial sums of [T, ldl] floats, T * ldl apart.
 cudaError_t launch_topk(const Shape& s, const float* logits, int nsplit, const void* x,
                         const void* w_router, int32_t* topk_idx, float* topk_w, float* gate,
-                        cudaStream_t st);
+                        uint32_t* redecided, cudaStream_t st);
+cudaError_t launch_sum_partials(const Shape& s, const float* logits, int nsplit, float* out,
+                                cudaStream_t st);
 
 // Split-K factor for a tensor-core fp32-output GEMM of one group (router):
 // enough CTAs to cover the SMs, at most kMaxSplit, at least 4 k-blocks each.

@@ -90,7 +90,7 @@ Layout layout_for(const Shape& s) {
   const size_t T = (size_t)s.T, k = (size_t)s.k, E = (size_t)s.E;
   L.flags = off; off += 256;
   L.logits = off; off += align256((size_t)kMaxSplit * T * (size_t)s.ldl * 4);
-  int64_t nchunks = (s.T + 15) / 16;
+  int64_t nchunks = (s.T + 31) / 32;
   int64_t cap = 262144 / s.E;
   if (cap < 1) cap = 1;
   if (nchunks > cap) nchunks = cap;
@@ -222,11 +222,10 @@ moe_status moe_workspace_init(void* ws, void* stream) {
   return MOE_OK;
 }
 
-// Router GEMM into the scratch logits, then top-k.
-static moe_status do_route(const Shape& s, const Layout& L, char* w, const void* x,
-                           const void* router, int32_t* idx, float* tw, float* gate,
-                           cudaStream_t st) {
-  if (s.T == 0) return MOE_OK;
+// Router GEMM into the scratch logits (split-K partial sums on the tensor
+// cores); returns the number of partials.
+static moe_status router_gemm(const Shape& s, const Layout& L, char* w, const void* x,
+                              const void* router, int* nsplit, cudaStream_t st) {
   float* logits = reinterpret_cast<float*>(w + L.logits);
   GemmArgs ra;
   ra.mode = kStoreF32;
@@ -250,7 +249,21 @@ static moe_status do_route(const Shape& s, const Layout& L, char* w, const void*
   ra.ksplit = engine_for(ra) == 2 ? router_split(s.T, s.ncols, s.H) : 1;
   ra.split_stride = s.T * (int64_t)s.ldl;
   CHECK_CUDA(launch_grouped_gemm(ra, st));
-  CHECK_CUDA(launch_topk(s, logits, ra.ksplit, x, router, idx, tw, gate, st));
+  *nsplit = ra.ksplit;
+  return MOE_OK;
+}
+
+// Router GEMM, then top-k.
+static moe_status do_route(const Shape& s, const Layout& L, char* w, const void* x,
+                           const void* router, int32_t* idx, float* tw, float* gate,
+                           cudaStream_t st) {
+  if (s.T == 0) return MOE_OK;
+  int nsplit = 1;
+  moe_status r = router_gemm(s, L, w, x, router, &nsplit, st);
+  if (r != MOE_OK) return r;
+  float* logits = reinterpret_cast<float*>(w + L.logits);
+  uint32_t* stats = reinterpret_cast<uint32_t*>(w + L.flags) + 1;
+  CHECK_CUDA(launch_topk(s, logits, nsplit, x, router, idx, tw, gate, stats, st));
   return MOE_OK;
 }
 
@@ -505,6 +518,34 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
   CHECK_CUDA(launch_combine(s, y_perm, sidx, use_w, sh_out, gate, y, st));
   STAGE_EVENT(MOE_NUM_STAGES);
 #undef STAGE_EVENT
+  return MOE_OK;
+}
+
+moe_status moe_get_route_stats(void* ws, void* stream, uint32_t* redecided) {
+  if (!ws) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+  if (!redecided) return fail(MOE_ERR_INVALID_ARG, "redecided is NULL");
+  CHECK_CUDA(cudaStreamSynchronize((cudaStream_t)stream));
+  CHECK_CUDA(cudaMemcpy(redecided, static_cast<char*>(ws) + 4, 4, cudaMemcpyDeviceToHost));
+  CHECK_CUDA(cudaMemset(static_cast<char*>(ws) + 4, 0, 4));
+  return MOE_OK;
+}
+
+moe_status moe_testing_router_logits(const moe_shape* shape, const void* x, const void* w_router,
+                                     float* logits, void* ws, size_t ws_bytes, void* stream) {
+  reset_launch_count();
+  DECODE(shape, s);
+  if (s.T > 0 && (!x || !w_router || !logits))
+    return fail(MOE_ERR_INVALID_ARG, "x, w_router and logits must be non-NULL");
+  const Layout L = layout_for(s);
+  moe_status c = check_ws(ws, ws_bytes, L.scratch_end);
+  if (c != MOE_OK) return c;
+  if (s.T == 0) return MOE_OK;
+  char* w = static_cast<char*>(ws);
+  int nsplit = 1;
+  moe_status r = router_gemm(s, L, w, x, w_router, &nsplit, (cudaStream_t)stream);
+  if (r != MOE_OK) return r;
+  CHECK_CUDA(launch_sum_partials(s, reinterpret_cast<float*>(w + L.logits), nsplit, logits,
+                                 (cudaStream_t)stream));
   return MOE_OK;
 }
 

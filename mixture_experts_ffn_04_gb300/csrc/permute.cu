@@ -7,42 +7,57 @@
 // keep row-major (token, slot) order, so the result is deterministic and a
 // duplicate route (two slots of one token on one expert) simply adds a row.
 //
-// Three launches, no global atomics:
-//   1. hist     per chunk of tokens, count pairs per expert (shared memory);
-//   2. scan     one block: per-expert prefix over chunks, then the exclusive
-//               prefix over experts -> counts, offsets, per-(chunk, expert) base;
-//   3. scatter  per chunk: one warp ranks the chunk's pairs in row-major order
-//               (__match_any_sync groups equal experts within 32 pairs), then
-//               all warps copy each token row once from x and write it to its
-//               k destinations with 16-byte vectors.
+// Three launches, no global atomics (rank, scan, scatter + copy; see each
+// kernel below).
 #include "common.cuh"
 #include "internal.h"
 
 namespace moe {
 namespace {
 
-__global__ void hist_kernel(const int32_t* __restrict__ idx, int64_t T, int k, int E, int tpc,
-                            int32_t* __restrict__ hist, uint32_t* flags) {
-  extern __shared__ int32_t cnt[];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
-  __syncthreads();
-  const int64_t t0 = (int64_t)blockIdx.x * tpc;
-  const int64_t t1 = min(T, t0 + tpc);
-  for (int64_t p = t0 * k + threadIdx.x; p < t1 * k; p += blockDim.x) {
-    const int e = idx[p];
-    if (e < 0 || e >= E) {
-      set_flag(flags, kFlagRoute);
-      continue;
-    }
-    atomicAdd(&cnt[e], 1);
+// 1. rank: one warp per chunk of `tpc` tokens walks the chunk's (token, slot)
+//    pairs in row-major order, 32 at a time; __match_any_sync groups the
+//    lanes that route to the same expert, so each pair gets its rank among the
+//    chunk's earlier pairs of that expert.  The rank is parked in
+//    scatter_index (overwritten by step 3) and the chunk's per-expert count
+//    goes to hist[chunk][e].
+__global__ void __launch_bounds__(256) rank_kernel(const int32_t* __restrict__ idx, int64_t T,
+                                                   int k, int E, int tpc, int nchunks,
+                                                   int32_t* __restrict__ hist,
+                                                   int32_t* __restrict__ local_rank,
+                                                   uint32_t* flags) {
+  extern __shared__ int32_t sm[];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int c = blockIdx.x * (blockDim.x >> 5) + wid;
+  if (c >= nchunks) return;
+  int32_t* cnt = sm + (size_t)wid * E;
+  for (int e = lane; e < E; e += 32) cnt[e] = 0;
+  __syncwarp();
+  const int64_t p0 = (int64_t)c * tpc * k;
+  const int64_t p1 = min(T, (int64_t)(c + 1) * tpc) * k;
+  for (int64_t pb = p0; pb < p1; pb += 32) {
+    const int64_t p = pb + lane;
+    const bool valid = p < p1;
+    const int e = valid ? idx[p] : -1;
+    const bool ok = valid && e >= 0 && e < E;
+    if (valid && !ok) set_flag(flags, kFlagRoute);
+    const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : -1 - lane);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    int r = -1;
+    if (ok) r = cnt[e] + rank;
+    __syncwarp();
+    if (ok && rank == 0) cnt[e] += __popc(peers);
+    __syncwarp();
+    if (valid) local_rank[p] = r;
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)blockIdx.x * E + e] = cnt[e];
+  __syncwarp();
+  for (int e = lane; e < E; e += 32) hist[(int64_t)c * E + e] = cnt[e];
 }
 
-// One block of 1024 threads.  Work items (e, seg): expert e, segment seg of
-// the chunks (S segments when E <= 1024, else one).  smem: segsum[S*E] and
-// block-scan scratch.
+// 2. scan: one block of 1024 threads.  Work items (e, seg): expert e and
+//    segment seg of the chunks (S segments when E <= 1024, else one).
+//    Produces counts, offsets and base[chunk][e] = offsets[e] + rows of e in
+//    earlier chunks.
 __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ hist, int nchunks,
                                                     int E, int S, int32_t* __restrict__ base,
                                                     int32_t* __restrict__ counts,
@@ -62,7 +77,6 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
     segsum[seg * E + e] = s;
   }
   __syncthreads();
-  // per-expert exclusive prefix over segments (in place) and the count
   for (int e = tid; e < E; e += blockDim.x) {
     int32_t run = 0;
     for (int seg = 0; seg < S; ++seg) {
@@ -74,7 +88,6 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
   }
   if (tid == 0) carry = 0;
   __syncthreads();
-  // exclusive prefix of counts over experts -> offsets (chunks of 1024)
   for (int b = 0; b < E; b += blockDim.x) {
     const int e = b + tid;
     const int32_t v = e < E ? counts[e] : 0;
@@ -104,7 +117,6 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
   }
   if (tid == 0) offsets[E] = carry;
   __syncthreads();
-  // per-(chunk, expert) base row
   for (int it = tid; it < items; it += blockDim.x) {
     const int e = it % E, seg = it / E;
     const int c0 = (int)((int64_t)nchunks * seg / S), c1 = (int)((int64_t)nchunks * (seg + 1) / S);
@@ -119,121 +131,77 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
   }
 }
 
+// 3. scatter + copy: one warp per token (grid-stride).  The warp turns the k
+//    local ranks into grouped rows (scatter_index, row_token), then copies the
+//    token's row once from x to each of its rows with 16-byte vectors, four
+//    loads in flight per lane.
 template <typename T>
-__global__ void __launch_bounds__(256) scatter_kernel(const T* __restrict__ x,
-                                                      const int32_t* __restrict__ idx, int64_t T_,
-                                                      int k, int E, int H, int tpc,
-                                                      const int32_t* __restrict__ base,
-                                                      int32_t* __restrict__ scatter_index,
-                                                      int32_t* __restrict__ row_token,
-                                                      T* __restrict__ x_perm) {
+__global__ void __launch_bounds__(256) scatter_copy_kernel(
+    const T* __restrict__ x, const int32_t* __restrict__ idx, int64_t T_, int k, int E, int H,
+    int tpc, const int32_t* __restrict__ base, int32_t* __restrict__ scatter_index,
+    int32_t* __restrict__ row_token, T* __restrict__ x_perm) {
   extern __shared__ int32_t sm[];
-  int32_t* running = sm;      // [E]
-  int32_t* dst = sm + E;      // [tpc * k]
-  const int64_t t0 = (int64_t)blockIdx.x * tpc;
-  const int64_t t1 = min(T_, t0 + tpc);
-  const int npairs = (int)((t1 - t0) * k);
-  for (int e = threadIdx.x; e < E; e += blockDim.x) running[e] = base[(int64_t)blockIdx.x * E + e];
-  __syncthreads();
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    for (int p0 = 0; p0 < npairs; p0 += 32) {
-      const int pl = p0 + lane;
-      const bool valid = pl < npairs;
-      const int64_t p = t0 * k + pl;
-      int e = valid ? idx[p] : -1;
-      const bool ok = valid && e >= 0 && e < E;
-      const int key = ok ? e : -1 - lane;  // invalid lanes never group
-      const unsigned peers = __match_any_sync(0xffffffffu, key);
-      const int rank = __popc(peers & ((1u << lane) - 1u));
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int32_t* dst = sm + (size_t)wid * k;
+  constexpr int V = 16 / sizeof(T);
+  const int nvec = H / V;
+  for (int64_t t = (int64_t)blockIdx.x * nw + wid; t < T_; t += (int64_t)gridDim.x * nw) {
+    const int64_t c = t / tpc;
+    for (int s = lane; s < k; s += 32) {
+      const int64_t p = t * k + s;
+      const int e = idx[p];
+      const int r = scatter_index[p];
       int d = -1;
-      if (ok) d = running[e] + rank;
-      __syncwarp();
-      if (ok && rank == 0) running[e] += __popc(peers);
-      __syncwarp();
-      if (valid) {
-        scatter_index[p] = d;
-        dst[pl] = d;
-        if (ok) row_token[d] = (int32_t)(p / k);
+      if (r >= 0) {
+        d = base[c * E + e] + r;
+        row_token[d] = (int32_t)t;
+      }
+      scatter_index[p] = d;
+      dst[s] = d;
+    }
+    __syncwarp();
+    const uint4* src = reinterpret_cast<const uint4*>(x + t * H);
+    int v = lane;
+    for (; v + 96 < nvec; v += 128) {
+      uint4 val[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) val[u] = __ldg(src + v + 32 * u);
+      for (int s = 0; s < k; ++s) {
+        const int d = dst[s];
+        if (d < 0) continue;
+        uint4* o = reinterpret_cast<uint4*>(x_perm + (int64_t)d * H) + v;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) o[32 * u] = val[u];
       }
     }
-  }
-  __syncthreads();
-  // copy: each token row read once, written to its k destinations
-  const int V = 16 / (int)sizeof(T);
-  const int nvec = H / V;
-  const int warps = blockDim.x >> 5, wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int64_t tl = wid; tl < t1 - t0; tl += warps) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + (t0 + tl) * H);
-    for (int v = lane; v < nvec; v += 32) {
+    for (; v < nvec; v += 32) {
       const uint4 val = __ldg(src + v);
       for (int s = 0; s < k; ++s) {
-        const int d = dst[tl * k + s];
+        const int d = dst[s];
         if (d >= 0) reinterpret_cast<uint4*>(x_perm + (int64_t)d * H)[v] = val;
       }
     }
+    __syncwarp();
   }
+}
+
+int sm_count_cached() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
 }
 
 }  // namespace
 
-cudaError_t launch_permute(const Shape& s, const Layout& L, char* ws, const void* x,
-                           const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
-                           int32_t* scatter_index, int32_t* row_token, void* x_perm,
-                           cudaStream_t st) {
-  int32_t* hist = reinterpret_cast<int32_t*>(ws + L.hist);
-  int32_t* base = reinterpret_cast<int32_t*>(ws + L.base);
-  uint32_t* flags = reinterpret_cast<uint32_t*>(ws + L.flags);
-  const int nchunks = s.T > 0 ? L.nchunks : 0;
-  const int tpc = L.tokens_per_chunk;
-  cudaError_t e;
-  if (nchunks > 0) {
-    const size_t hsm = (size_t)s.E * 4;
-    if (hsm > 48 * 1024) {
-      e = cudaFuncSetAttribute(hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsm);
-      if (e != cudaSuccess) return e;
-    }
-    hist_kernel<<<nchunks, 256, hsm, st>>>(topk_idx, s.T, s.k, s.E, tpc, hist, flags);
-    count_launch();
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  const int S = s.E <= 1024 ? (nchunks > 0 ? (1024 / s.E < nchunks ? 1024 / s.E : nchunks) : 1) : 1;
-  const size_t ssm = (size_t)(S > 0 ? S : 1) * s.E * 4;
-  if (ssm > 48 * 1024) {
-    e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
-    if (e != cudaSuccess) return e;
-  }
-  scan_kernel<<<1, 1024, ssm, st>>>(hist, nchunks, s.E, S > 0 ? S : 1, base, counts, offsets);
-  count_launch();
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (nchunks == 0) return cudaSuccess;
-  const size_t csm = ((size_t)s.E + (size_t)tpc * s.k) * 4;
-  if (s.dtype == MOE_F32) {
-    if (csm > 48 * 1024) {
-      e = cudaFuncSetAttribute(scatter_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)csm);
-      if (e != cudaSuccess) return e;
-    }
-    scatter_kernel<float><<<nchunks, 256, csm, st>>>(
-        reinterpret_cast<const float*>(x), topk_idx, s.T, s.k, s.E, s.H, tpc, base, scatter_index,
-        row_token, reinterpret_cast<float*>(x_perm));
-  } else {
-    if (csm > 48 * 1024) {
-      e = cudaFuncSetAttribute(scatter_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)csm);
-      if (e != cudaSuccess) return e;
-    }
-    scatter_kernel<bf16><<<nchunks, 256, csm, st>>>(
-        reinterpret_cast<const bf16*>(x), topk_idx, s.T, s.k, s.E, s.H, tpc, base, scatter_index,
-        row_token, reinterpret_cast<bf16*>(x_perm));
-  }
-  count_launch();
-  return cudaGetLastError();
-}
-
-// Same three launches with caller-chosen scratch tables (hist and base, each
-// nchunks * E int32) and an optional status word; used by the allocation-free
-// entry point, whose scratch is a static device array.
+// The three launches with caller-chosen scratch tables (hist and base, each
+// nchunks * E int32) and an optional status word.  Used with workspace
+// tables by moe_permute / moe_layer_forward and with the library's static
+// array by moe_permute_static.
 cudaError_t launch_permute_scratch(const Shape& s, int nchunks, int tpc, int32_t* hist,
                                    int32_t* base, uint32_t* flags, const void* x,
                                    const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
@@ -242,12 +210,16 @@ cudaError_t launch_permute_scratch(const Shape& s, int nchunks, int tpc, int32_t
   if (s.T == 0) nchunks = 0;
   cudaError_t e;
   if (nchunks > 0) {
-    const size_t hsm = (size_t)s.E * 4;
-    if (hsm > 48 * 1024) {
-      e = cudaFuncSetAttribute(hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)hsm);
+    int wpb = (int)((48 * 1024) / ((size_t)s.E * 4));
+    if (wpb > 8) wpb = 8;
+    if (wpb < 1) wpb = 1;
+    const size_t rsm = (size_t)wpb * s.E * 4;
+    if (rsm > 48 * 1024) {
+      e = cudaFuncSetAttribute(rank_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)rsm);
       if (e != cudaSuccess) return e;
     }
-    hist_kernel<<<nchunks, 256, hsm, st>>>(topk_idx, s.T, s.k, s.E, tpc, hist, flags);
+    rank_kernel<<<(nchunks + wpb - 1) / wpb, wpb * 32, rsm, st>>>(
+        topk_idx, s.T, s.k, s.E, tpc, nchunks, hist, scatter_index, flags);
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -262,28 +234,32 @@ cudaError_t launch_permute_scratch(const Shape& s, int nchunks, int tpc, int32_t
   count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (nchunks == 0) return cudaSuccess;
-  const size_t csm = ((size_t)s.E + (size_t)tpc * s.k) * 4;
+  const size_t csm = (size_t)8 * s.k * 4;
+  int64_t blocks = (s.T + 7) / 8;
+  const int64_t cap = (int64_t)sm_count_cached() * 8;
+  if (blocks > cap) blocks = cap;
   if (s.dtype == MOE_F32) {
-    if (csm > 48 * 1024) {
-      e = cudaFuncSetAttribute(scatter_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)csm);
-      if (e != cudaSuccess) return e;
-    }
-    scatter_kernel<float><<<nchunks, 256, csm, st>>>(
+    scatter_copy_kernel<float><<<(unsigned)blocks, 256, csm, st>>>(
         reinterpret_cast<const float*>(x), topk_idx, s.T, s.k, s.E, s.H, tpc, base, scatter_index,
         row_token, reinterpret_cast<float*>(x_perm));
   } else {
-    if (csm > 48 * 1024) {
-      e = cudaFuncSetAttribute(scatter_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)csm);
-      if (e != cudaSuccess) return e;
-    }
-    scatter_kernel<bf16><<<nchunks, 256, csm, st>>>(
+    scatter_copy_kernel<bf16><<<(unsigned)blocks, 256, csm, st>>>(
         reinterpret_cast<const bf16*>(x), topk_idx, s.T, s.k, s.E, s.H, tpc, base, scatter_index,
         row_token, reinterpret_cast<bf16*>(x_perm));
   }
   count_launch();
   return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const Shape& s, const Layout& L, char* ws, const void* x,
+                           const int32_t* topk_idx, int32_t* counts, int32_t* offsets,
+                           int32_t* scatter_index, int32_t* row_token, void* x_perm,
+                           cudaStream_t st) {
+  return launch_permute_scratch(s, L.nchunks, L.tokens_per_chunk,
+                                reinterpret_cast<int32_t*>(ws + L.hist),
+                                reinterpret_cast<int32_t*>(ws + L.base),
+                                reinterpret_cast<uint32_t*>(ws + L.flags), x, topk_idx, counts,
+                                offsets, scatter_index, row_token, x_perm, st);
 }
 
 }  // namespace moe

@@ -44,6 +44,7 @@ struct TopkArgs {
   int32_t* idx;
   float* wout;
   float* gate;
+  uint32_t* redecided;  // count of tokens whose order was re-decided exactly
 };
 
 struct WarpSmem {
@@ -190,6 +191,7 @@ __global__ void topk_kernel(TopkArgs a) {
   for (int r = lane; r + 1 < R; r += 32) near |= (sm.sel_v[r] - sm.sel_v[r + 1]) < tau;
   near = __any_sync(0xffffffffu, near);
   if (near && a.x != nullptr) {
+    if (lane == 0 && a.redecided) atomicAdd(a.redecided, 1u);
     // L = every expert within tau below the boundary value (so all of the
     // top R, plus the ones just under it).  Only members of L closer than tau
     // to another member can swap places; they are re-evaluated exactly, the
@@ -284,7 +286,7 @@ __global__ void topk_kernel(TopkArgs a) {
 
 cudaError_t launch_topk(const Shape& s, const float* logits, int nsplit, const void* x,
                         const void* w_router, int32_t* topk_idx, float* topk_w, float* gate,
-                        cudaStream_t st) {
+                        uint32_t* redecided, cudaStream_t st) {
   if (s.T == 0) return cudaSuccess;
   TopkArgs a;
   a.logits = logits;
@@ -305,6 +307,7 @@ cudaError_t launch_topk(const Shape& s, const float* logits, int nsplit, const v
   a.idx = topk_idx;
   a.wout = topk_w;
   a.gate = gate;
+  a.redecided = redecided;
   const size_t per_warp = warp_smem_bytes(s.E);
   int warps = (int)((96 * 1024) / per_warp);
   if (warps > 8) warps = 8;
@@ -323,6 +326,34 @@ cudaError_t launch_topk(const Shape& s, const float* logits, int nsplit, const v
     if (e != cudaSuccess) return e;
     topk_kernel<bf16><<<(unsigned)blocks, warps * 32, smem, st>>>(a);
   }
+  count_launch();
+  return cudaGetLastError();
+}
+
+namespace {
+// Sum of the split-K partial logits, in split order (the same sum the top-k
+// kernel forms), into a caller buffer [T, ncols].
+__global__ void sum_partials_kernel(const float* __restrict__ part, int nsplit,
+                                    int64_t split_stride, int64_t T, int ncols, int ldl,
+                                    float* __restrict__ out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < T * ncols;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / ncols;
+    const int c = (int)(i % ncols);
+    float v = part[t * ldl + c];
+    for (int sp = 1; sp < nsplit; ++sp) v += part[sp * split_stride + t * ldl + c];
+    out[i] = v;
+  }
+}
+}  // namespace
+
+cudaError_t launch_sum_partials(const Shape& s, const float* logits, int nsplit, float* out,
+                                cudaStream_t st) {
+  if (s.T == 0) return cudaSuccess;
+  const int64_t n = s.T * s.ncols;
+  const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  sum_partials_kernel<<<blocks, 256, 0, st>>>(logits, nsplit, s.T * (int64_t)s.ldl, s.T, s.ncols,
+                                              s.ldl, out);
   count_launch();
   return cudaGetLastError();
 }

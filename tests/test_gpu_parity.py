@@ -188,3 +188,32 @@ def test_near_ties_match_the_oracle():
     assert close > 20, close   # the construction really produced near-ties
     print("near-tie tokens (gap < 1e-3): %d, exact ties: %d, mismatches: %d" % (
         close, int((gap == 0).sum()), int(mism.sum())))
+
+
+@pytest.mark.parametrize("wl", [W.QWEN3_30B_A3B, W.DEEPSEEK_V3, W.get("qwen2-moe-shape-T2048"),
+                                W.TINY_F32], ids=lambda w: w.name)
+def test_router_logit_error_within_tie_bound(wl):
+    """The fp32 router logits (tensor-core or FMA sums, split-K partials added
+    in order) stay well inside the kernel's near-tie bound
+    tau >= 2^-20 * sqrt(H): that bound is what makes the exact re-decision
+    complete.  Also reports how many tokens were re-decided."""
+    from oracle import oracle as O
+    T = min(wl.T, 2048)
+    inp = W.make_inputs(wl, seed=0, device="cuda", with_experts=False)
+    x = inp["x"][:T].contiguous()
+    s = m.shape_for(wl, T=T)
+    ws = m.alloc_workspace(s, full=False)
+    ncols = inp["w_router"].shape[0]
+    lg = torch.empty(T, ncols, dtype=torch.float32, device="cuda")
+    m.moe_testing_router_logits(s, x, inp["w_router"], lg, ws)
+    idx = torch.empty(T, wl.k, dtype=torch.int32, device="cuda")
+    tw = torch.empty(T, wl.k, dtype=torch.float32, device="cuda")
+    gate = torch.empty(T, dtype=torch.float32, device="cuda") if wl.shared_gate else None
+    m.moe_route(s, x, inp["w_router"], idx, tw, gate, ws)
+    redecided = m.moe_get_route_stats(ws)
+    ref = O.router_logits(x.cpu(), inp["w_router"].cpu())
+    err = np.abs(lg.double().cpu().numpy() - ref).max()
+    bound = 2.0 ** -20 * np.sqrt(wl.H)
+    print("%s: max |fp32 logit - exact| = %.3e (%.3f of the smallest tie bound), "
+          "re-decided %d of %d tokens" % (wl.name, err, err / bound, redecided, T))
+    assert err < 0.5 * bound
