@@ -127,25 +127,44 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(GemmArgs a) {
       if (MODE == kSwiGLU) accu[i][q] = 0.f;
     }
 
-  for (int k0 = 0; k0 < K; k0 += kBK) {
-    for (int e = tid; e < BM * kBK; e += kThreads) {
-      const int r = e / kBK, kk = e % kBK;
+  // Register double buffer: the next k-slice is fetched from global memory
+  // while the current one is multiplied out of shared memory.
+  constexpr int EA = BM * kBK / kThreads, EB = kBN * kBK / kThreads;
+  float ra[EA], rb[EB], ru[MODE == kSwiGLU ? EB : 1];
+  auto fetch = [&](int k0) {
+#pragma unroll
+    for (int q = 0; q < EA; ++q) {
+      const int e = tid + q * kThreads, r = e / kBK, kk = e % kBK;
       const int64_t row = row0 + r;
-      float v = 0.f;
-      if (row < gend && k0 + kk < K) v = to_f(A[row * K + k0 + kk]);
-      As[kk][r] = v;
+      ra[q] = (row < gend && k0 + kk < K) ? to_f(A[row * K + k0 + kk]) : 0.f;
     }
-    for (int e = tid; e < kBN * kBK; e += kThreads) {
-      const int n = e / kBK, kk = e % kBK;
-      float v = 0.f, u = 0.f;
-      if (n0 + n < N && k0 + kk < K) {
-        v = to_f(B0[(int64_t)(n0 + n) * K + k0 + kk]);
-        if (MODE == kSwiGLU) u = to_f(B1[(int64_t)(n0 + n) * K + k0 + kk]);
-      }
-      Bs[kk][n] = v;
-      if (MODE == kSwiGLU) Us[kk][n] = u;
+#pragma unroll
+    for (int q = 0; q < EB; ++q) {
+      const int e = tid + q * kThreads, n = e / kBK, kk = e % kBK;
+      const bool in = n0 + n < N && k0 + kk < K;
+      rb[q] = in ? to_f(B0[(int64_t)(n0 + n) * K + k0 + kk]) : 0.f;
+      if (MODE == kSwiGLU) ru[q] = in ? to_f(B1[(int64_t)(n0 + n) * K + k0 + kk]) : 0.f;
     }
-    __syncthreads();
+  };
+  auto stash = [&]() {
+#pragma unroll
+    for (int q = 0; q < EA; ++q) {
+      const int e = tid + q * kThreads;
+      As[e % kBK][e / kBK] = ra[q];
+    }
+#pragma unroll
+    for (int q = 0; q < EB; ++q) {
+      const int e = tid + q * kThreads;
+      Bs[e % kBK][e / kBK] = rb[q];
+      if (MODE == kSwiGLU) Us[e % kBK][e / kBK] = ru[q];
+    }
+  };
+  fetch(0);
+  stash();
+  __syncthreads();
+  for (int k0 = 0; k0 < K; k0 += kBK) {
+    const bool more = k0 + kBK < K;
+    if (more) fetch(k0 + kBK);
 #pragma unroll
     for (int kk = 0; kk < kBK; ++kk) {
       float av[TM], bv[4], uv[4];
@@ -166,6 +185,10 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(GemmArgs a) {
         }
     }
     __syncthreads();
+    if (more) {
+      stash();
+      __syncthreads();
+    }
   }
 
 #pragma unroll
@@ -187,10 +210,11 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(GemmArgs a) {
   }
 }
 
+int64_t mtile_bound(const GemmArgs& a, int bm);
+
 template <typename T, int BM>
 cudaError_t launch_t(const GemmArgs& a, cudaStream_t st) {
-  int64_t mt_bound = a.offsets ? (a.rows_bound + BM - 1) / BM + a.G
-                               : (a.single_rows + BM - 1) / BM;
+  const int64_t mt_bound = mtile_bound(a, BM);
   if (mt_bound <= 0 || a.N <= 0) return cudaSuccess;
   if (mt_bound > 0x7fffffff) return cudaErrorInvalidValue;
   dim3 grid((unsigned)mt_bound, (unsigned)((a.N + kBN - 1) / kBN));
@@ -211,8 +235,13 @@ cudaError_t launch_t(const GemmArgs& a, cudaStream_t st) {
 // with each row of A (L1-resident, shared by the block's 8 warps).
 // ---------------------------------------------------------------------------
 namespace {
-constexpr int kSkR = 8;
+constexpr int kSkR = 8;   // rows per m-tile
+constexpr int kSkC = 4;   // output columns per warp
 
+// One warp: kSkC consecutive output columns of one m-tile.  Each lane walks
+// its 16-byte chunks of K; a chunk of each A row is loaded once and used for
+// all kSkC columns, and the kSkC (x2 for SwiGLU) weight chunks of an
+// iteration are independent loads, so several are in flight per lane.
 template <typename T, int MODE>
 __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a) {
   const int total = a.sched[a.G];
@@ -224,62 +253,94 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a) {
   const int64_t row0 = gbeg + (int64_t)(j - a.sched[g]) * kSkR;
   const int nrows = (int)min((int64_t)kSkR, gend - row0);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n = blockIdx.y * 8 + warp;
-  if (n >= a.N) return;
+  const int n0 = (blockIdx.y * 8 + warp) * kSkC;
+  if (n0 >= a.N) return;
   const int K = a.K;
   constexpr int V = 16 / sizeof(T);
-  const T* A = reinterpret_cast<const T*>(a.A) + row0 * K;
-  const T* B0 = reinterpret_cast<const T*>(a.B0) + (int64_t)g * a.bstride + (int64_t)n * K;
-  const T* B1 = MODE == kSwiGLU
-                    ? reinterpret_cast<const T*>(a.B1) + (int64_t)g * a.bstride + (int64_t)n * K
-                    : nullptr;
-  float acc[kSkR], accu[kSkR];
+  const uint4* A = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.A) + row0 * K);
+  const T* B0 = reinterpret_cast<const T*>(a.B0) + (int64_t)g * a.bstride;
+  const T* B1 = MODE == kSwiGLU ? reinterpret_cast<const T*>(a.B1) + (int64_t)g * a.bstride
+                                : nullptr;
+  const int nv = K / V;
+  float acc[kSkR][kSkC], accu[MODE == kSwiGLU ? kSkR : 1][kSkC];
 #pragma unroll
-  for (int r = 0; r < kSkR; ++r) acc[r] = accu[r] = 0.f;
-  for (int c = lane; c < K / V; c += 32) {
-    float w[V], u[V];
-    unpack16(__ldg(reinterpret_cast<const uint4*>(B0) + c), w, (const T*)nullptr);
-    if (MODE == kSwiGLU) unpack16(__ldg(reinterpret_cast<const uint4*>(B1) + c), u, (const T*)nullptr);
+  for (int r = 0; r < kSkR; ++r)
+#pragma unroll
+    for (int q = 0; q < kSkC; ++q) {
+      acc[r][q] = 0.f;
+      if (MODE == kSwiGLU) accu[r][q] = 0.f;
+    }
+  const uint4* Bc[kSkC];
+  const uint4* Uc[kSkC];
+#pragma unroll
+  for (int q = 0; q < kSkC; ++q) {
+    const int n = min(n0 + q, a.N - 1);   // clamped columns are computed, not stored
+    Bc[q] = reinterpret_cast<const uint4*>(B0 + (int64_t)n * K);
+    Uc[q] = MODE == kSwiGLU ? reinterpret_cast<const uint4*>(B1 + (int64_t)n * K) : nullptr;
+  }
+#pragma unroll 2
+  for (int c = lane; c < nv; c += 32) {
+    float w[kSkC][V], u[MODE == kSwiGLU ? kSkC : 1][V];
+#pragma unroll
+    for (int q = 0; q < kSkC; ++q) {
+      unpack16(__ldg(Bc[q] + c), w[q], (const T*)nullptr);
+      if (MODE == kSwiGLU) unpack16(__ldg(Uc[q] + c), u[q], (const T*)nullptr);
+    }
 #pragma unroll
     for (int r = 0; r < kSkR; ++r) {
       if (r < nrows) {
         float xa[V];
-        unpack16(__ldg(reinterpret_cast<const uint4*>(A + (int64_t)r * K) + c), xa, (const T*)nullptr);
+        unpack16(__ldg(A + (int64_t)r * nv + c), xa, (const T*)nullptr);
 #pragma unroll
-        for (int i = 0; i < V; ++i) {
-          acc[r] = fmaf(w[i], xa[i], acc[r]);
-          if (MODE == kSwiGLU) accu[r] = fmaf(u[i], xa[i], accu[r]);
-        }
+        for (int q = 0; q < kSkC; ++q)
+#pragma unroll
+          for (int i = 0; i < V; ++i) {
+            acc[r][q] = fmaf(w[q][i], xa[i], acc[r][q]);
+            if (MODE == kSwiGLU) accu[r][q] = fmaf(u[q][i], xa[i], accu[r][q]);
+          }
       }
     }
   }
 #pragma unroll
-  for (int r = 0; r < kSkR; ++r) {
+  for (int r = 0; r < kSkR; ++r)
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      acc[r] += __shfl_xor_sync(0xffffffffu, acc[r], o);
-      if (MODE == kSwiGLU) accu[r] += __shfl_xor_sync(0xffffffffu, accu[r], o);
-    }
-  }
+    for (int q = 0; q < kSkC; ++q)
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        acc[r][q] += __shfl_xor_sync(0xffffffffu, acc[r][q], o);
+        if (MODE == kSwiGLU) accu[r][q] += __shfl_xor_sync(0xffffffffu, accu[r][q], o);
+      }
   if (lane == 0) {
 #pragma unroll
     for (int r = 0; r < kSkR; ++r) {
       if (r >= nrows) break;
-      const int64_t o = (row0 + r) * a.ldo + n;
-      if (MODE == kStoreF32) reinterpret_cast<float*>(a.out)[o] = acc[r];
-      else if (MODE == kStoreAct) reinterpret_cast<T*>(a.out)[o] = from_f<T>(acc[r]);
-      else reinterpret_cast<T*>(a.out)[o] = from_f<T>(silu_f(acc[r]) * accu[r]);
+#pragma unroll
+      for (int q = 0; q < kSkC; ++q) {
+        const int n = n0 + q;
+        if (n >= a.N) continue;
+        const int64_t o = (row0 + r) * a.ldo + n;
+        if (MODE == kStoreF32) reinterpret_cast<float*>(a.out)[o] = acc[r][q];
+        else if (MODE == kStoreAct) reinterpret_cast<T*>(a.out)[o] = from_f<T>(acc[r][q]);
+        else reinterpret_cast<T*>(a.out)[o] = from_f<T>(silu_f(acc[r][q]) * accu[r][q]);
+      }
     }
   }
 }
 
+// Upper bound on the m-tiles of a call: each group needs ceil(rows/bm), and a
+// non-empty tile holds at least one row.
+int64_t mtile_bound(const GemmArgs& a, int bm) {
+  if (!a.offsets) return (a.single_rows + bm - 1) / bm;
+  int64_t b = (a.rows_bound + bm - 1) / bm + a.G;
+  return b < a.rows_bound ? b : a.rows_bound;
+}
+
 template <typename T>
 cudaError_t launch_skinny_t(const GemmArgs& a, cudaStream_t st) {
-  const int64_t mt_bound = a.offsets ? (a.rows_bound + kSkR - 1) / kSkR + a.G
-                                     : (a.single_rows + kSkR - 1) / kSkR;
+  const int64_t mt_bound = mtile_bound(a, kSkR);
   if (mt_bound <= 0 || a.N <= 0) return cudaSuccess;
   if (mt_bound > 0x7fffffff) return cudaErrorInvalidValue;
-  dim3 grid((unsigned)mt_bound, (unsigned)((a.N + 7) / 8));
+  dim3 grid((unsigned)mt_bound, (unsigned)((a.N + 8 * kSkC - 1) / (8 * kSkC)));
   switch (a.mode) {
     case kSwiGLU: skinny_kernel<T, kSwiGLU><<<grid, 256, 0, st>>>(a); break;
     case kStoreAct: skinny_kernel<T, kStoreAct><<<grid, 256, 0, st>>>(a); break;

@@ -562,7 +562,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   t.out = a.out;
   t.ldo = a.ldo;
   t.flags = a.flags;
-  const int64_t mt_bound = a.offsets ? (a.rows_bound + BM - 1) / BM + a.G : (a.single_rows + BM - 1) / BM;
+  int64_t mt_bound = a.offsets ? (a.rows_bound + BM - 1) / BM + a.G : (a.single_rows + BM - 1) / BM;
+  if (a.offsets && mt_bound > a.rows_bound) mt_bound = a.rows_bound;  // >= 1 row per tile
   const int64_t tiles_bound = mt_bound * t.NT * t.ksplit;
   static bool attr_done = false;
   if (!attr_done) {

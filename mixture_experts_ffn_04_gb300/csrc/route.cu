@@ -135,8 +135,12 @@ __device__ double dot2(const T* x, const T* w, int H, int lane) {
   return (double)P + (double)S;
 }
 
-template <typename T>
-__global__ void topk_kernel(TopkArgs a) {
+// VPL > 0: register path for E <= 32 * VPL and k + 1 <= 32 -- lane l holds
+// logits l, l+32, ... in registers and a taken mask, so a selection round is a
+// few register compares plus one shuffle arg-max, with no shared-memory scan.
+// VPL == 0: general path (any E <= 16383, k <= 255) over shared memory.
+template <typename T, int VPL>
+__global__ void __launch_bounds__(256) topk_kernel(TopkArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int E = a.E, k = a.k;
@@ -156,32 +160,68 @@ __global__ void topk_kernel(TopkArgs a) {
   // logits = sum of the split-K partials, always in split order
   const float* row = a.logits + t * a.ldl;
   float m = -INFINITY;
-  for (int e = lane; e < E; e += 32) {
-    float v = row[e];
-    for (int sp = 1; sp < a.nsplit; ++sp) v += row[sp * a.split_stride + e];
-    sm.buf[e] = v;
-    m = fmaxf(m, v);
-  }
-  for (int w = lane; w < (E + 31) / 32; w += 32) sm.taken[w] = 0u;
+  if constexpr (VPL > 0) {
+    float v[VPL];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  __syncwarp();
-
-  for (int r = 0; r < R; ++r) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int e = lane; e < E; e += 32) {
-      if (sm.taken[e >> 5] & (1u << (e & 31))) continue;
-      float v = sm.buf[e];
-      if (bi == 0x7fffffff || better(v, e, bv, bi)) { bv = v; bi = e; }
+    for (int j = 0; j < VPL; ++j) {
+      const int e = lane + 32 * j;
+      v[j] = -INFINITY;
+      if (e < E) {
+        float x = row[e];
+        for (int sp = 1; sp < a.nsplit; ++sp) x += row[sp * a.split_stride + e];
+        v[j] = x;
+        sm.buf[e] = x;
+        m = fmaxf(m, x);
+      }
     }
-    warp_argmax(bv, bi);
-    if (lane == 0) {
-      sm.sel_i[r] = bi;
-      sm.sel_v[r] = bv;
-      sm.taken[bi >> 5] |= 1u << (bi & 31);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    uint32_t taken = 0u;
+    for (int r = 0; r < R; ++r) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) {
+        const int e = lane + 32 * j;
+        const bool free = e < E && !(taken & (1u << j));
+        if (free && (bi == 0x7fffffff || better(v[j], e, bv, bi))) { bv = v[j]; bi = e; }
+      }
+      warp_argmax(bv, bi);
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == r) {
+        sm.sel_i[r] = bi;
+        sm.sel_v[r] = bv;
+      }
     }
     __syncwarp();
+  } else {
+    for (int e = lane; e < E; e += 32) {
+      float v = row[e];
+      for (int sp = 1; sp < a.nsplit; ++sp) v += row[sp * a.split_stride + e];
+      sm.buf[e] = v;
+      m = fmaxf(m, v);
+    }
+    for (int w = lane; w < (E + 31) / 32; w += 32) sm.taken[w] = 0u;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    __syncwarp();
+
+    for (int r = 0; r < R; ++r) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+      for (int e = lane; e < E; e += 32) {
+        if (sm.taken[e >> 5] & (1u << (e & 31))) continue;
+        float v = sm.buf[e];
+        if (bi == 0x7fffffff || better(v, e, bv, bi)) { bv = v; bi = e; }
+      }
+      warp_argmax(bv, bi);
+      if (lane == 0) {
+        sm.sel_i[r] = bi;
+        sm.sel_v[r] = bv;
+        sm.taken[bi >> 5] |= 1u << (bi & 31);
+      }
+      __syncwarp();
+    }
   }
 
   // ---- near-tie re-decision -------------------------------------------
@@ -282,6 +322,18 @@ __global__ void topk_kernel(TopkArgs a) {
   }
 }
 
+template <typename T, int VPL>
+cudaError_t launch_topk_t(const TopkArgs& a, int64_t blocks, int warps, size_t smem,
+                          cudaStream_t st) {
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(topk_kernel<T, VPL>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  topk_kernel<T, VPL><<<(unsigned)blocks, warps * 32, smem, st>>>(a);
+  return cudaSuccess;
+}
+
 }  // namespace
 
 cudaError_t launch_topk(const Shape& s, const float* logits, int nsplit, const void* x,
@@ -310,22 +362,32 @@ cudaError_t launch_topk(const Shape& s, const float* logits, int nsplit, const v
   a.redecided = redecided;
   const size_t per_warp = warp_smem_bytes(s.E);
   int warps = (int)((96 * 1024) / per_warp);
-  if (warps > 8) warps = 8;
+  if (warps > 4) warps = 4;
   if (warps < 1) warps = 1;
   const size_t smem = per_warp * warps;
   const int64_t blocks = (s.T + warps - 1) / warps;
+  const int R = s.k < s.E ? s.k + 1 : s.k;
+  int vpl = 0;
+  if (R <= 32) vpl = s.E <= 32 ? 1 : s.E <= 64 ? 2 : s.E <= 128 ? 4 : s.E <= 256 ? 8 : 0;
   cudaError_t e;
   if (s.dtype == MOE_F32) {
-    e = cudaFuncSetAttribute(topk_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e != cudaSuccess) return e;
-    topk_kernel<float><<<(unsigned)blocks, warps * 32, smem, st>>>(a);
+    switch (vpl) {
+      case 1: e = launch_topk_t<float, 1>(a, blocks, warps, smem, st); break;
+      case 2: e = launch_topk_t<float, 2>(a, blocks, warps, smem, st); break;
+      case 4: e = launch_topk_t<float, 4>(a, blocks, warps, smem, st); break;
+      case 8: e = launch_topk_t<float, 8>(a, blocks, warps, smem, st); break;
+      default: e = launch_topk_t<float, 0>(a, blocks, warps, smem, st); break;
+    }
   } else {
-    e = cudaFuncSetAttribute(topk_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-    if (e != cudaSuccess) return e;
-    topk_kernel<bf16><<<(unsigned)blocks, warps * 32, smem, st>>>(a);
+    switch (vpl) {
+      case 1: e = launch_topk_t<bf16, 1>(a, blocks, warps, smem, st); break;
+      case 2: e = launch_topk_t<bf16, 2>(a, blocks, warps, smem, st); break;
+      case 4: e = launch_topk_t<bf16, 4>(a, blocks, warps, smem, st); break;
+      case 8: e = launch_topk_t<bf16, 8>(a, blocks, warps, smem, st); break;
+      default: e = launch_topk_t<bf16, 0>(a, blocks, warps, smem, st); break;
+    }
   }
+  if (e != cudaSuccess) return e;
   count_launch();
   return cudaGetLastError();
 }
