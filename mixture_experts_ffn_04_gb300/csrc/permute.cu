@@ -35,20 +35,30 @@ __global__ void __launch_bounds__(256) rank_kernel(const int32_t* __restrict__ i
   __syncwarp();
   const int64_t p0 = (int64_t)c * tpc * k;
   const int64_t p1 = min(T, (int64_t)(c + 1) * tpc) * k;
-  for (int64_t pb = p0; pb < p1; pb += 32) {
-    const int64_t p = pb + lane;
-    const bool valid = p < p1;
-    const int e = valid ? idx[p] : -1;
-    const bool ok = valid && e >= 0 && e < E;
-    if (valid && !ok) set_flag(flags, kFlagRoute);
-    const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : -1 - lane);
-    const int rank = __popc(peers & ((1u << lane) - 1u));
-    int r = -1;
-    if (ok) r = cnt[e] + rank;
-    __syncwarp();
-    if (ok && rank == 0) cnt[e] += __popc(peers);
-    __syncwarp();
-    if (valid) local_rank[p] = r;
+  constexpr int kBatch = 8;   // rounds of 32 pairs whose expert ids are loaded together
+  for (int64_t pb = p0; pb < p1; pb += 32 * kBatch) {
+    int ids[kBatch];
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int64_t p = pb + 32 * b + lane;
+      ids[b] = p < p1 ? idx[p] : -1;
+    }
+#pragma unroll
+    for (int b = 0; b < kBatch; ++b) {
+      const int64_t p = pb + 32 * b + lane;
+      const bool valid = p < p1;
+      const int e = ids[b];
+      const bool ok = valid && e >= 0 && e < E;
+      if (valid && !ok) set_flag(flags, kFlagRoute);
+      const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : -1 - lane);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      int r = -1;
+      if (ok) r = cnt[e] + rank;
+      __syncwarp();
+      if (ok && rank == 0) cnt[e] += __popc(peers);
+      __syncwarp();
+      if (valid) local_rank[p] = r;
+    }
   }
   __syncwarp();
   for (int e = lane; e < E; e += 32) hist[(int64_t)c * E + e] = cnt[e];
