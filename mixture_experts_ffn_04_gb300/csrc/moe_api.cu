@@ -103,6 +103,7 @@ Layout layout_for(const Shape& s) {
   L.sched_routed = off; off += align256((E + 1) * 4);
   L.sched_shared = off; off += 256;
   L.sched_router = off; off += 256;
+  L.tie_queue = off; off += align256(T * 4);
   L.scratch_end = off;
   L.topk_idx = off; off += align256(T * k * 4);
   L.topk_w = off; off += align256(T * k * 4);
@@ -263,7 +264,9 @@ static moe_status do_route(const Shape& s, const Layout& L, char* w, const void*
   if (r != MOE_OK) return r;
   float* logits = reinterpret_cast<float*>(w + L.logits);
   uint32_t* stats = reinterpret_cast<uint32_t*>(w + L.flags) + 1;
-  CHECK_CUDA(launch_topk(s, logits, nsplit, x, router, idx, tw, gate, stats, st));
+  uint32_t* qcount = reinterpret_cast<uint32_t*>(w + L.flags) + 2;
+  int32_t* queue = reinterpret_cast<int32_t*>(w + L.tie_queue);
+  CHECK_CUDA(launch_topk(s, logits, nsplit, x, router, idx, tw, gate, stats, queue, qcount, st));
   return MOE_OK;
 }
 

@@ -28,6 +28,8 @@ REDUCED = [
     W.small(W.QWEN2_MOE, T=5, H=512, I=256, I_sh=512),            # decode-sized
     W.small(W.ADV_E0, T=300, H=512, I=256, I_sh=256),
     W.small(W.ADV_ZIPF, T=300, H=512, I=256, I_sh=256),
+    W.small(W.QWEN3_30B_A3B, T=100, H=256, I=128, E=64, k=40),    # k+1 > 32: warp top-k
+    W.small(W.QWEN3_30B_A3B, T=200, H=256, I=128, E=300, k=4),    # E > 256
 ]
 ENGINES = {0: "auto", 1: "cuda-core", 2: "tensor-core", 3: "skinny"}
 
