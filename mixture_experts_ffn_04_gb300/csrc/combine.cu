@@ -34,7 +34,11 @@ __global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y_pe
   const float g = gate ? gate[t] : 1.0f;
   constexpr int V = 16 / sizeof(T);
   const int nvec = H / V;
-  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+  // blockIdx.y / gridDim.y: this block's slice of the row (several blocks per
+  // token when there are few tokens)
+  const int v0 = (int)((int64_t)nvec * blockIdx.y / gridDim.y);
+  const int v1 = (int)((int64_t)nvec * (blockIdx.y + 1) / gridDim.y);
+  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
     float acc[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] = 0.f;
@@ -66,12 +70,17 @@ cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* sc
                            void* y, cudaStream_t st) {
   if (s.T == 0) return cudaSuccess;
   const size_t smem = (size_t)s.k * 8;
+  // few tokens: split each row over several blocks (about 2 vectors a thread)
+  const int nvec = s.H / (s.dtype == MOE_F32 ? 4 : 8);
+  int ysplit = 1;
+  if (s.T < 1024) ysplit = (nvec + 255) / 256;
+  const dim3 grid((unsigned)s.T, (unsigned)ysplit);
   if (s.dtype == MOE_F32) {
-    combine_kernel<float><<<(unsigned)s.T, 128, smem, st>>>(
+    combine_kernel<float><<<grid, 128, smem, st>>>(
         reinterpret_cast<const float*>(y_perm), scatter_index, topk_w, s.k, s.H,
         reinterpret_cast<const float*>(shared_out), gate, reinterpret_cast<float*>(y));
   } else {
-    combine_kernel<bf16><<<(unsigned)s.T, 128, smem, st>>>(
+    combine_kernel<bf16><<<grid, 128, smem, st>>>(
         reinterpret_cast<const bf16*>(y_perm), scatter_index, topk_w, s.k, s.H,
         reinterpret_cast<const bf16*>(shared_out), gate, reinterpret_cast<bf16*>(y));
   }

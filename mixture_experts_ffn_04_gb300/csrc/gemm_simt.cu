@@ -229,47 +229,80 @@ cudaError_t launch_t(const GemmArgs& a, cudaStream_t st) {
 }  // namespace
 
 // ---------------------------------------------------------------------------
-// Skinny engine for decode-sized groups (a few rows per expert): the cost is
-// reading each weight row once, so one warp owns one output column n of an
-// m-tile of up to 8 rows, streams B_g[n, :] with 16-byte loads and dots it
-// with each row of A (L1-resident, shared by the block's 8 warps).
+// Skinny engine for decode-sized calls (a few rows per group): the cost is
+// reading each weight row once, so the engine is built to keep many weight
+// loads in flight.  A block owns kSkC output columns of one m-tile of up to
+// kSkR rows; its 8 warps split K into 8 slices and stream their slice of each
+// column's weight row with 16-byte loads, dotting it with the m-tile's rows of
+// A; the 8 partial sums are added in a fixed order through shared memory.  The
+// m-tile schedule is built in shared memory by each block (no extra launch).
 // ---------------------------------------------------------------------------
 namespace {
-constexpr int kSkR = 8;   // rows per m-tile
-constexpr int kSkC = 4;   // output columns per warp
+constexpr int kSkR = 8;      // rows per m-tile
+constexpr int kSkC = 4;      // output columns per block
+constexpr int kSkW = 8;      // warps per block (K slices)
+constexpr int kSkMaxG = 1024;
 
-// One warp: kSkC consecutive output columns of one m-tile.  Each lane walks
-// its 16-byte chunks of K; a chunk of each A row is loaded once and used for
-// all kSkC columns, and the kSkC (x2 for SwiGLU) weight chunks of an
-// iteration are independent loads, so several are in flight per lane.
+__device__ void block_schedule(const GemmArgs& a, int bm, int32_t* sched, int lane) {
+  int carry = 0;
+  bool bad = false;
+  for (int base = 0; base < a.G; base += 32) {
+    const int g = base + lane;
+    int v = 0;
+    if (g < a.G) {
+      int64_t cnt = a.offsets ? (int64_t)a.offsets[g + 1] - a.offsets[g] : a.single_rows;
+      if (cnt < 0) { bad = true; cnt = 0; }
+      v = (int)((cnt + bm - 1) / bm);
+    }
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (g < a.G) sched[g] = carry + incl - v;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) {
+    if (a.offsets) bad |= a.offsets[0] != 0 || (int64_t)a.offsets[a.G] > a.rows_bound;
+    else bad |= a.single_rows > a.rows_bound || a.single_rows < 0;
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  if (lane == 0) {
+    sched[a.G] = bad ? 0 : carry;
+    if (bad && blockIdx.x == 0 && blockIdx.y == 0) set_flag(a.flags, kFlagRows);
+  }
+}
+
 template <typename T, int MODE>
-__global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a) {
-  const int total = a.sched[a.G];
+__global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched) {
+  constexpr int NU = MODE == kSwiGLU ? 2 : 1;
+  __shared__ int32_t s_sched[kSkMaxG + 1];
+  __shared__ float red[kSkW][kSkR * kSkC * NU];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int32_t* sched = a.sched;
+  if (smem_sched) {
+    if (warp == 0) block_schedule(a, kSkR, s_sched, lane);
+    __syncthreads();
+    sched = s_sched;
+  }
+  const int total = sched[a.G];
   const int j = blockIdx.x;
   if (j >= total) return;
-  const int g = find_group(a.sched, a.G, j);
+  const int g = find_group(sched, a.G, j);
   const int64_t gbeg = a.offsets ? a.offsets[g] : 0;
   const int64_t gend = a.offsets ? a.offsets[g + 1] : a.single_rows;
-  const int64_t row0 = gbeg + (int64_t)(j - a.sched[g]) * kSkR;
+  const int64_t row0 = gbeg + (int64_t)(j - sched[g]) * kSkR;
   const int nrows = (int)min((int64_t)kSkR, gend - row0);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n0 = (blockIdx.y * 8 + warp) * kSkC;
-  if (n0 >= a.N) return;
+  const int n0 = blockIdx.y * kSkC;
   const int K = a.K;
   constexpr int V = 16 / sizeof(T);
+  const int nv = K / V;
+  const int c0 = (int)((int64_t)nv * warp / kSkW), c1 = (int)((int64_t)nv * (warp + 1) / kSkW);
   const uint4* A = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.A) + row0 * K);
   const T* B0 = reinterpret_cast<const T*>(a.B0) + (int64_t)g * a.bstride;
   const T* B1 = MODE == kSwiGLU ? reinterpret_cast<const T*>(a.B1) + (int64_t)g * a.bstride
                                 : nullptr;
-  const int nv = K / V;
-  float acc[kSkR][kSkC], accu[MODE == kSwiGLU ? kSkR : 1][kSkC];
-#pragma unroll
-  for (int r = 0; r < kSkR; ++r)
-#pragma unroll
-    for (int q = 0; q < kSkC; ++q) {
-      acc[r][q] = 0.f;
-      if (MODE == kSwiGLU) accu[r][q] = 0.f;
-    }
   const uint4* Bc[kSkC];
   const uint4* Uc[kSkC];
 #pragma unroll
@@ -278,8 +311,16 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a) {
     Bc[q] = reinterpret_cast<const uint4*>(B0 + (int64_t)n * K);
     Uc[q] = MODE == kSwiGLU ? reinterpret_cast<const uint4*>(B1 + (int64_t)n * K) : nullptr;
   }
+  float acc[kSkR][kSkC], accu[MODE == kSwiGLU ? kSkR : 1][kSkC];
+#pragma unroll
+  for (int r = 0; r < kSkR; ++r)
+#pragma unroll
+    for (int q = 0; q < kSkC; ++q) {
+      acc[r][q] = 0.f;
+      if (MODE == kSwiGLU) accu[r][q] = 0.f;
+    }
 #pragma unroll 2
-  for (int c = lane; c < nv; c += 32) {
+  for (int c = c0 + lane; c < c1; c += 32) {
     float w[kSkC][V], u[MODE == kSwiGLU ? kSkC : 1][V];
 #pragma unroll
     for (int q = 0; q < kSkC; ++q) {
@@ -304,25 +345,33 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a) {
 #pragma unroll
   for (int r = 0; r < kSkR; ++r)
 #pragma unroll
-    for (int q = 0; q < kSkC; ++q)
+    for (int q = 0; q < kSkC; ++q) {
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         acc[r][q] += __shfl_xor_sync(0xffffffffu, acc[r][q], o);
         if (MODE == kSwiGLU) accu[r][q] += __shfl_xor_sync(0xffffffffu, accu[r][q], o);
       }
-  if (lane == 0) {
-#pragma unroll
-    for (int r = 0; r < kSkR; ++r) {
-      if (r >= nrows) break;
-#pragma unroll
-      for (int q = 0; q < kSkC; ++q) {
-        const int n = n0 + q;
-        if (n >= a.N) continue;
-        const int64_t o = (row0 + r) * a.ldo + n;
-        if (MODE == kStoreF32) reinterpret_cast<float*>(a.out)[o] = acc[r][q];
-        else if (MODE == kStoreAct) reinterpret_cast<T*>(a.out)[o] = from_f<T>(acc[r][q]);
-        else reinterpret_cast<T*>(a.out)[o] = from_f<T>(silu_f(acc[r][q]) * accu[r][q]);
+      if (lane == 0) {
+        red[warp][(r * kSkC + q) * NU] = acc[r][q];
+        if (MODE == kSwiGLU) red[warp][(r * kSkC + q) * NU + 1] = accu[r][q];
       }
+    }
+  __syncthreads();
+  const int tid = threadIdx.x;
+  if (tid < kSkR * kSkC) {
+    const int r = tid / kSkC, q = tid % kSkC;
+    const int n = n0 + q;
+    if (r < nrows && n < a.N) {
+      float sg = 0.f, su = 0.f;
+#pragma unroll
+      for (int w = 0; w < kSkW; ++w) {   // fixed order: deterministic
+        sg += red[w][(r * kSkC + q) * NU];
+        if (MODE == kSwiGLU) su += red[w][(r * kSkC + q) * NU + 1];
+      }
+      const int64_t o = (row0 + r) * a.ldo + n;
+      if (MODE == kStoreF32) reinterpret_cast<float*>(a.out)[o] = sg;
+      else if (MODE == kStoreAct) reinterpret_cast<T*>(a.out)[o] = from_f<T>(sg);
+      else reinterpret_cast<T*>(a.out)[o] = from_f<T>(silu_f(sg) * su);
     }
   }
 }
@@ -336,15 +385,15 @@ int64_t mtile_bound(const GemmArgs& a, int bm) {
 }
 
 template <typename T>
-cudaError_t launch_skinny_t(const GemmArgs& a, cudaStream_t st) {
+cudaError_t launch_skinny_t(const GemmArgs& a, int smem_sched, cudaStream_t st) {
   const int64_t mt_bound = mtile_bound(a, kSkR);
   if (mt_bound <= 0 || a.N <= 0) return cudaSuccess;
   if (mt_bound > 0x7fffffff) return cudaErrorInvalidValue;
-  dim3 grid((unsigned)mt_bound, (unsigned)((a.N + 8 * kSkC - 1) / (8 * kSkC)));
+  dim3 grid((unsigned)mt_bound, (unsigned)((a.N + kSkC - 1) / kSkC));
   switch (a.mode) {
-    case kSwiGLU: skinny_kernel<T, kSwiGLU><<<grid, 256, 0, st>>>(a); break;
-    case kStoreAct: skinny_kernel<T, kStoreAct><<<grid, 256, 0, st>>>(a); break;
-    default: skinny_kernel<T, kStoreF32><<<grid, 256, 0, st>>>(a); break;
+    case kSwiGLU: skinny_kernel<T, kSwiGLU><<<grid, 256, 0, st>>>(a, smem_sched); break;
+    case kStoreAct: skinny_kernel<T, kStoreAct><<<grid, 256, 0, st>>>(a, smem_sched); break;
+    default: skinny_kernel<T, kStoreF32><<<grid, 256, 0, st>>>(a, smem_sched); break;
   }
   count_launch();
   return cudaGetLastError();
@@ -353,9 +402,13 @@ cudaError_t launch_skinny_t(const GemmArgs& a, cudaStream_t st) {
 
 cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t st) {
   if (a.K % (a.dtype == MOE_F32 ? 4 : 8) != 0) return cudaErrorInvalidValue;
-  cudaError_t e = launch_schedule(a, kSkR, st);
-  if (e != cudaSuccess) return e;
-  return a.dtype == MOE_F32 ? launch_skinny_t<float>(a, st) : launch_skinny_t<bf16>(a, st);
+  const int smem_sched = a.G <= kSkMaxG;
+  if (!smem_sched) {
+    cudaError_t e = launch_schedule(a, kSkR, st);
+    if (e != cudaSuccess) return e;
+  }
+  return a.dtype == MOE_F32 ? launch_skinny_t<float>(a, smem_sched, st)
+                            : launch_skinny_t<bf16>(a, smem_sched, st);
 }
 
 cudaError_t launch_gemm_simt(const GemmArgs& a, int bm, cudaStream_t st) {

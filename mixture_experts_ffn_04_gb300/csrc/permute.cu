@@ -195,6 +195,88 @@ __global__ void __launch_bounds__(256) scatter_copy_kernel(
   }
 }
 
+// All three steps in one block, for calls whose tokens fit one chunk
+// (decode-sized): warp 0 ranks the pairs, the expert counts are scanned in
+// shared memory, then every warp turns ranks into rows and copies its tokens.
+template <typename T>
+__global__ void __launch_bounds__(256) permute_small_kernel(
+    const T* __restrict__ x, const int32_t* __restrict__ idx, int T_, int k, int E, int H,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ scatter_index, int32_t* __restrict__ row_token, T* __restrict__ x_perm,
+    uint32_t* flags) {
+  extern __shared__ int32_t sm[];
+  int32_t* cnt = sm;             // [E]
+  int32_t* off = sm + E;         // [E + 1]
+  int32_t* dst = off + E + 1;    // [T_ * k]
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int np = T_ * k;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
+  __syncthreads();
+  if (wid == 0) {
+    for (int pb = 0; pb < np; pb += 32) {
+      const int p = pb + lane;
+      const bool valid = p < np;
+      const int e = valid ? idx[p] : -1;
+      const bool ok = valid && e >= 0 && e < E;
+      if (valid && !ok) set_flag(flags, kFlagRoute);
+      const unsigned peers = __match_any_sync(0xffffffffu, ok ? e : -1 - lane);
+      const int rank = __popc(peers & ((1u << lane) - 1u));
+      int r = -1;
+      if (ok) r = cnt[e] + rank;
+      __syncwarp();
+      if (ok && rank == 0) cnt[e] += __popc(peers);
+      __syncwarp();
+      if (valid) dst[p] = r;
+    }
+    __syncwarp();
+    int carry = 0;
+    for (int b = 0; b < E; b += 32) {
+      const int e = b + lane;
+      const int v = e < E ? cnt[e] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (e < E) {
+        off[e] = carry + incl - v;
+        counts[e] = v;
+        offsets[e] = carry + incl - v;
+      }
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      off[E] = carry;
+      offsets[E] = carry;
+    }
+  }
+  __syncthreads();
+  for (int p = threadIdx.x; p < np; p += blockDim.x) {
+    const int r = dst[p];
+    int d = -1;
+    if (r >= 0) {
+      d = off[idx[p]] + r;
+      row_token[d] = p / k;
+    }
+    scatter_index[p] = d;
+    dst[p] = d;
+  }
+  __syncthreads();
+  constexpr int V = 16 / sizeof(T);
+  const int nvec = H / V;
+  for (int t = wid; t < T_; t += nw) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)t * H);
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 val = __ldg(src + v);
+      for (int s2 = 0; s2 < k; ++s2) {
+        const int d = dst[t * k + s2];
+        if (d >= 0) reinterpret_cast<uint4*>(x_perm + (int64_t)d * H)[v] = val;
+      }
+    }
+  }
+}
+
 int sm_count_cached() {
   static int n = 0;
   if (n == 0) {
@@ -219,6 +301,20 @@ cudaError_t launch_permute_scratch(const Shape& s, int nchunks, int tpc, int32_t
                                    cudaStream_t st) {
   if (s.T == 0) nchunks = 0;
   cudaError_t e;
+  const size_t small_smem = ((size_t)2 * s.E + 1 + (size_t)s.T * s.k) * 4;
+  if (nchunks == 1 && small_smem <= 48 * 1024) {
+    if (s.dtype == MOE_F32) {
+      permute_small_kernel<float><<<1, 256, small_smem, st>>>(
+          reinterpret_cast<const float*>(x), topk_idx, (int)s.T, s.k, s.E, s.H, counts, offsets,
+          scatter_index, row_token, reinterpret_cast<float*>(x_perm), flags);
+    } else {
+      permute_small_kernel<bf16><<<1, 256, small_smem, st>>>(
+          reinterpret_cast<const bf16*>(x), topk_idx, (int)s.T, s.k, s.E, s.H, counts, offsets,
+          scatter_index, row_token, reinterpret_cast<bf16*>(x_perm), flags);
+    }
+    count_launch();
+    return cudaGetLastError();
+  }
   if (nchunks > 0) {
     int wpb = (int)((48 * 1024) / ((size_t)s.E * 4));
     if (wpb > 8) wpb = 8;

@@ -361,90 +361,92 @@ __global__ void __launch_bounds__(128) topk_queue_kernel(TopkArgs a) {
     warp_token<T, VPL>(a, sm, a.queue[i], lane);
 }
 
-// One thread per token for k + 1 <= RM <= 32: stream the token's E logits
-// (split-K partials added in order) through a sorted top-(k+1) list held in
-// registers, ordered by (value desc, index asc).  A token whose list has two
+// G lanes per token (G a power of two, G tokens' groups per warp), for
+// k + 1 <= 32 and E <= 16 G: lane gl of a group holds logits gl, gl+G, ... in
+// registers; each of the k+1 rounds is a register scan plus log2(G) shuffle
+// steps inside the group.  A token whose sorted top-(k+1) list has two
 // neighbours closer than the tie bound is appended to the queue and decided
 // again by topk_queue_kernel; the others get their weights and gate here.
-template <int RM>
-__global__ void __launch_bounds__(128) topk_thread_kernel(TopkArgs a) {
-  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= a.T) return;
+template <int G, int VPL>
+__global__ void __launch_bounds__(128) topk_group_kernel(TopkArgs a) {
+  constexpr int TPB = 128 / G;            // tokens per block
+  __shared__ float s_val[TPB][32];
+  __shared__ int s_idx[TPB][32];
+  const int gl = threadIdx.x % G, tb = threadIdx.x / G;
+  const int64_t t = (int64_t)blockIdx.x * TPB + tb;
+  const bool live = t < a.T;
   const int E = a.E, k = a.k;
   const int R = k < E ? k + 1 : k;
-  float val[RM];
-  int ix[RM];
+  const float* row = a.logits + (live ? t : 0) * a.ldl;
+  float v[VPL];
+  float m = -INFINITY;
 #pragma unroll
-  for (int j = 0; j < RM; ++j) {
-    val[j] = -INFINITY;
-    ix[j] = 0x7fffffff;
-  }
-  const float* row = a.logits + t * a.ldl;
-  int filled = 0;
-  for (int e0 = 0; e0 < E; e0 += 4) {
-    float4 q = *reinterpret_cast<const float4*>(row + e0);
-    for (int sp = 1; sp < a.nsplit; ++sp) {
-      const float4 r = *reinterpret_cast<const float4*>(row + sp * a.split_stride + e0);
-      q.x += r.x; q.y += r.y; q.z += r.z; q.w += r.w;
+  for (int j = 0; j < VPL; ++j) {
+    const int e = gl + G * j;
+    float x = -INFINITY;
+    if (live && e < E) {
+      x = row[e];
+#pragma unroll 4
+      for (int sp = 1; sp < a.nsplit; ++sp) x += row[sp * a.split_stride + e];
     }
-    const float vv[4] = {q.x, q.y, q.z, q.w};
+    v[j] = x;
+    m = fmaxf(m, x);
+  }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int e = e0 + u;
-      if (e >= E) break;
-      float cv = vv[u];
-      int ci = e;
-      if (filled >= R && !better(cv, ci, val[R - 1], ix[R - 1])) continue;
-      filled += filled < R;
+  for (int o = G / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  uint32_t taken = 0u;
+  for (int r = 0; r < R; ++r) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
 #pragma unroll
-      for (int j = 0; j < RM; ++j) {
-        if (j < R && better(cv, ci, val[j], ix[j])) {
-          const float tv = val[j];
-          const int ti = ix[j];
-          val[j] = cv;
-          ix[j] = ci;
-          cv = tv;
-          ci = ti;
-        }
-      }
+    for (int j = 0; j < VPL; ++j) {
+      const int e = gl + G * j;
+      const bool free = e < E && !(taken & (1u << j));
+      if (free && (bi == 0x7fffffff || better(v[j], e, bv, bi))) { bv = v[j]; bi = e; }
+    }
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    if (bi != 0x7fffffff && bi % G == gl) taken |= 1u << (bi / G);
+    if (gl == 0) {
+      s_val[tb][r] = bv;
+      s_idx[tb][r] = bi;
     }
   }
-  const float tau = tie_bound(a, val[0], val[R - 1]);
+  __syncwarp();
+  const float tau = tie_bound(a, s_val[tb][0], s_val[tb][R - 1]);
   bool near = false;
+  for (int r = gl; r + 1 < R; r += G) near |= (s_val[tb][r] - s_val[tb][r + 1]) < tau;
 #pragma unroll
-  for (int j = 0; j + 1 < RM; ++j)
-    if (j + 1 < R) near |= (val[j] - val[j + 1]) < tau;
-  if (near && a.x != nullptr) {
-    a.queue[atomicAdd(a.qcount, 1u)] = (int32_t)t;
+  for (int o = G / 2; o > 0; o >>= 1) near |= __shfl_xor_sync(0xffffffffu, (int)near, o) != 0;
+  const bool queued = near && a.x != nullptr;
+  // lanes that finish the token here (whole groups: live and near are
+  // uniform within a group)
+  const unsigned gm = __ballot_sync(0xffffffffu, live && !queued);
+  if (!live) return;
+  if (queued) {
+    if (gl == 0) a.queue[atomicAdd(a.qcount, 1u)] = (int32_t)t;
     return;
   }
+  const float ref = a.norm ? s_val[tb][0] : m;
   float denom = 0.f;
-  const float ref = val[0];   // the largest logit
   if (a.norm) {
-#pragma unroll
-    for (int j = 0; j < RM; ++j)
-      if (j < k) denom += expf(val[j] - ref);
+    for (int r = gl; r < k; r += G) denom += expf(s_val[tb][r] - ref);
   } else {
-    for (int e0 = 0; e0 < E; e0 += 4) {
-      float4 q = *reinterpret_cast<const float4*>(row + e0);
-      for (int sp = 1; sp < a.nsplit; ++sp) {
-        const float4 r = *reinterpret_cast<const float4*>(row + sp * a.split_stride + e0);
-        q.x += r.x; q.y += r.y; q.z += r.z; q.w += r.w;
-      }
-      const float vv[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        if (e0 + u < E) denom += expf(vv[u] - ref);
-    }
+    for (int j = 0; j < VPL; ++j)
+      if (gl + G * j < E) denom += expf(v[j] - ref);
   }
 #pragma unroll
-  for (int j = 0; j < RM; ++j) {
-    if (j < k) {
-      a.idx[t * k + j] = ix[j];
-      a.wout[t * k + j] = expf(val[j] - ref) / denom;
-    }
+  for (int o = G / 2; o > 0; o >>= 1) denom += __shfl_xor_sync(gm, denom, o);
+  for (int r = gl; r < k; r += G) {
+    a.idx[t * k + r] = s_idx[tb][r];
+    a.wout[t * k + r] = expf(s_val[tb][r] - ref) / denom;
   }
-  if (a.gated) {
+  if (a.gated && gl == 0) {
     float z = row[E];
     for (int sp = 1; sp < a.nsplit; ++sp) z += row[sp * a.split_stride + E];
     a.gate[t] = 1.0f / (1.0f + expf(-z));
@@ -513,7 +515,7 @@ cudaError_t launch_topk(const Shape& s, const float* logits, int nsplit, const v
   if (R <= 32) vpl = s.E <= 32 ? 1 : s.E <= 64 ? 2 : s.E <= 128 ? 4 : s.E <= 256 ? 8 : 0;
   const size_t per_warp = warp_smem_bytes(s.E);
   cudaError_t e;
-  if (R > 32) {
+  if (R > 32 || s.E > 512 || s.T <= 256) {   // warp per token; no queue for few tokens
     e = s.dtype == MOE_F32 ? launch_warp<float>(a, vpl, false, per_warp, st)
                            : launch_warp<bf16>(a, vpl, false, per_warp, st);
     if (e != cudaSuccess) return e;
@@ -522,11 +524,19 @@ cudaError_t launch_topk(const Shape& s, const float* logits, int nsplit, const v
   }
   e = cudaMemsetAsync(qcount, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
-  const unsigned blocks = (unsigned)((s.T + 127) / 128);
-  if (R <= 4) topk_thread_kernel<4><<<blocks, 128, 0, st>>>(a);
-  else if (R <= 8) topk_thread_kernel<8><<<blocks, 128, 0, st>>>(a);
-  else if (R <= 16) topk_thread_kernel<16><<<blocks, 128, 0, st>>>(a);
-  else topk_thread_kernel<32><<<blocks, 128, 0, st>>>(a);
+  // lanes per token: the smallest power of two holding E in 16 per lane
+  int G = 1;
+  while (G < 32 && G * 16 < s.E) G *= 2;
+  const int tpb = 128 / G;
+  const unsigned blocks = (unsigned)((s.T + tpb - 1) / tpb);
+  switch (G) {
+    case 1: topk_group_kernel<1, 16><<<blocks, 128, 0, st>>>(a); break;
+    case 2: topk_group_kernel<2, 16><<<blocks, 128, 0, st>>>(a); break;
+    case 4: topk_group_kernel<4, 16><<<blocks, 128, 0, st>>>(a); break;
+    case 8: topk_group_kernel<8, 16><<<blocks, 128, 0, st>>>(a); break;
+    case 16: topk_group_kernel<16, 16><<<blocks, 128, 0, st>>>(a); break;
+    default: topk_group_kernel<32, 16><<<blocks, 128, 0, st>>>(a); break;
+  }
   count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   e = s.dtype == MOE_F32 ? launch_warp<float>(a, vpl, true, per_warp, st)
