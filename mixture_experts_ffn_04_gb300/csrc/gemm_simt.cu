@@ -275,7 +275,7 @@ __device__ void block_schedule(const GemmArgs& a, int bm, int32_t* sched, int la
 }
 
 template <typename T, int MODE>
-__global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched) {
+__global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched, int ks) {
   constexpr int NU = MODE == kSwiGLU ? 2 : 1;
   __shared__ int32_t s_sched[kSkMaxG + 1];
   __shared__ float red[kSkW][kSkR * kSkC * NU];
@@ -294,11 +294,13 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched)
   const int64_t gend = a.offsets ? a.offsets[g + 1] : a.single_rows;
   const int64_t row0 = gbeg + (int64_t)(j - sched[g]) * kSkR;
   const int nrows = (int)min((int64_t)kSkR, gend - row0);
-  const int n0 = blockIdx.y * kSkC;
+  // warp -> (column group cg, K slice sl); the block owns kSkW/ks column groups
+  const int cg = warp / ks, sl = warp % ks, ncg = kSkW / ks;
+  const int n0 = (blockIdx.y * ncg + cg) * kSkC;
   const int K = a.K;
   constexpr int V = 16 / sizeof(T);
   const int nv = K / V;
-  const int c0 = (int)((int64_t)nv * warp / kSkW), c1 = (int)((int64_t)nv * (warp + 1) / kSkW);
+  const int c0 = (int)((int64_t)nv * sl / ks), c1 = (int)((int64_t)nv * (sl + 1) / ks);
   const uint4* A = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.A) + row0 * K);
   const T* B0 = reinterpret_cast<const T*>(a.B0) + (int64_t)g * a.bstride;
   const T* B1 = MODE == kSwiGLU ? reinterpret_cast<const T*>(a.B1) + (int64_t)g * a.bstride
@@ -319,31 +321,42 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched)
       acc[r][q] = 0.f;
       if (MODE == kSwiGLU) accu[r][q] = 0.f;
     }
+  if (n0 < a.N) {
 #pragma unroll 2
-  for (int c = c0 + lane; c < c1; c += 32) {
-    float w[kSkC][V], u[MODE == kSwiGLU ? kSkC : 1][V];
+    for (int c = c0 + lane; c < c1; c += 32) {
+      float w[kSkC][V], u[MODE == kSwiGLU ? kSkC : 1][V];
 #pragma unroll
-    for (int q = 0; q < kSkC; ++q) {
-      unpack16(__ldg(Bc[q] + c), w[q], (const T*)nullptr);
-      if (MODE == kSwiGLU) unpack16(__ldg(Uc[q] + c), u[q], (const T*)nullptr);
-    }
+      for (int q = 0; q < kSkC; ++q) {
+        unpack16(__ldg(Bc[q] + c), w[q], (const T*)nullptr);
+        if (MODE == kSwiGLU) unpack16(__ldg(Uc[q] + c), u[q], (const T*)nullptr);
+      }
 #pragma unroll
-    for (int r = 0; r < kSkR; ++r) {
-      if (r < nrows) {
-        float xa[V];
-        unpack16(__ldg(A + (int64_t)r * nv + c), xa, (const T*)nullptr);
+      for (int r = 0; r < kSkR; ++r) {
+        if (r < nrows) {
+          float xa[V];
+          unpack16(__ldg(A + (int64_t)r * nv + c), xa, (const T*)nullptr);
 #pragma unroll
-        for (int q = 0; q < kSkC; ++q)
+          for (int q = 0; q < kSkC; ++q)
 #pragma unroll
-          for (int i = 0; i < V; ++i) {
-            acc[r][q] = fmaf(w[q][i], xa[i], acc[r][q]);
-            if (MODE == kSwiGLU) accu[r][q] = fmaf(u[q][i], xa[i], accu[r][q]);
-          }
+            for (int i = 0; i < V; ++i) {
+              acc[r][q] = fmaf(w[q][i], xa[i], acc[r][q]);
+              if (MODE == kSwiGLU) accu[r][q] = fmaf(u[q][i], xa[i], accu[r][q]);
+            }
+        }
       }
     }
   }
+  auto store = [&](int r, int q, float sg, float su) {
+    const int n = n0 + q;
+    if (r >= nrows || n >= a.N) return;
+    const int64_t o = (row0 + r) * a.ldo + n;
+    if (MODE == kStoreF32) reinterpret_cast<float*>(a.out)[o] = sg;
+    else if (MODE == kStoreAct) reinterpret_cast<T*>(a.out)[o] = from_f<T>(sg);
+    else reinterpret_cast<T*>(a.out)[o] = from_f<T>(silu_f(sg) * su);
+  };
 #pragma unroll
-  for (int r = 0; r < kSkR; ++r)
+  for (int r = 0; r < kSkR; ++r) {
+    if (r >= nrows) break;   // uniform over the block
 #pragma unroll
     for (int q = 0; q < kSkC; ++q) {
 #pragma unroll
@@ -352,26 +365,34 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched)
         if (MODE == kSwiGLU) accu[r][q] += __shfl_xor_sync(0xffffffffu, accu[r][q], o);
       }
       if (lane == 0) {
-        red[warp][(r * kSkC + q) * NU] = acc[r][q];
-        if (MODE == kSwiGLU) red[warp][(r * kSkC + q) * NU + 1] = accu[r][q];
+        if (ks == 1) {
+          store(r, q, acc[r][q], MODE == kSwiGLU ? accu[r][q] : 0.f);
+        } else {
+          red[warp][(r * kSkC + q) * NU] = acc[r][q];
+          if (MODE == kSwiGLU) red[warp][(r * kSkC + q) * NU + 1] = accu[r][q];
+        }
       }
     }
+  }
+  if (ks == 1) return;
   __syncthreads();
   const int tid = threadIdx.x;
-  if (tid < kSkR * kSkC) {
-    const int r = tid / kSkC, q = tid % kSkC;
-    const int n = n0 + q;
-    if (r < nrows && n < a.N) {
+  if (tid < ncg * kSkR * kSkC) {
+    const int gi = tid / (kSkR * kSkC), rem = tid % (kSkR * kSkC);
+    const int r = rem / kSkC, q = rem % kSkC;
+    if (r < nrows) {
       float sg = 0.f, su = 0.f;
-#pragma unroll
-      for (int w = 0; w < kSkW; ++w) {   // fixed order: deterministic
+      for (int w = gi * ks; w < (gi + 1) * ks; ++w) {   // fixed order: deterministic
         sg += red[w][(r * kSkC + q) * NU];
         if (MODE == kSwiGLU) su += red[w][(r * kSkC + q) * NU + 1];
       }
-      const int64_t o = (row0 + r) * a.ldo + n;
-      if (MODE == kStoreF32) reinterpret_cast<float*>(a.out)[o] = sg;
-      else if (MODE == kStoreAct) reinterpret_cast<T*>(a.out)[o] = from_f<T>(sg);
-      else reinterpret_cast<T*>(a.out)[o] = from_f<T>(silu_f(sg) * su);
+      const int n = (blockIdx.y * ncg + gi) * kSkC + q;
+      if (n < a.N) {
+        const int64_t o = (row0 + r) * a.ldo + n;
+        if (MODE == kStoreF32) reinterpret_cast<float*>(a.out)[o] = sg;
+        else if (MODE == kStoreAct) reinterpret_cast<T*>(a.out)[o] = from_f<T>(sg);
+        else reinterpret_cast<T*>(a.out)[o] = from_f<T>(silu_f(sg) * su);
+      }
     }
   }
 }
@@ -389,11 +410,16 @@ cudaError_t launch_skinny_t(const GemmArgs& a, int smem_sched, cudaStream_t st) 
   const int64_t mt_bound = mtile_bound(a, kSkR);
   if (mt_bound <= 0 || a.N <= 0) return cudaSuccess;
   if (mt_bound > 0x7fffffff) return cudaErrorInvalidValue;
-  dim3 grid((unsigned)mt_bound, (unsigned)((a.N + kSkC - 1) / kSkC));
+  // K slices per column: enough warps to keep every SM streaming weights
+  const int64_t base_warps = mt_bound * ((a.N + kSkC - 1) / kSkC);
+  int ks = 1;
+  while (ks < kSkW && base_warps * ks < 2432) ks *= 2;
+  const int cols_per_block = (kSkW / ks) * kSkC;
+  dim3 grid((unsigned)mt_bound, (unsigned)((a.N + cols_per_block - 1) / cols_per_block));
   switch (a.mode) {
-    case kSwiGLU: skinny_kernel<T, kSwiGLU><<<grid, 256, 0, st>>>(a, smem_sched); break;
-    case kStoreAct: skinny_kernel<T, kStoreAct><<<grid, 256, 0, st>>>(a, smem_sched); break;
-    default: skinny_kernel<T, kStoreF32><<<grid, 256, 0, st>>>(a, smem_sched); break;
+    case kSwiGLU: skinny_kernel<T, kSwiGLU><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
+    case kStoreAct: skinny_kernel<T, kStoreAct><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
+    default: skinny_kernel<T, kStoreF32><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
   }
   count_launch();
   return cudaGetLastError();

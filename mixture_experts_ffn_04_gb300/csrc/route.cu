@@ -348,17 +348,156 @@ __global__ void __launch_bounds__(128) topk_warp_kernel(TopkArgs a) {
   warp_token<T, VPL>(a, sm, t, lane);
 }
 
-// The tokens the thread path queued (a near-tie, or a shape it does not take),
-// one warp each.
-template <typename T, int VPL>
-__global__ void __launch_bounds__(128) topk_queue_kernel(TopkArgs a) {
+// The tokens the group kernel queued (a near-tie), one block of 4 warps each:
+// the logits go to shared memory, warp 0 finds the fp32 top-(k+1) boundary,
+// the candidates within the tie bound of it are collected and the ones close
+// to another candidate get their exact dot product (one warp per candidate),
+// then one thread orders the candidates by (exact value desc, index asc).
+// Only called for E <= 512 and k + 1 <= 32.
+template <typename T>
+__global__ void __launch_bounds__(128) topk_refine_kernel(TopkArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const WarpSmem sm = warp_smem(smem_raw + warp_smem_bytes(a.E) * wid, a.E);
+  float2* cand_v = reinterpret_cast<float2*>(smem_raw);          // [kMaxCand]
+  int* cand_i = reinterpret_cast<int*>(cand_v + kMaxCand);        // [kMaxCand]
+  int* order = cand_i + kMaxCand;                                 // [kMaxCand]
+  float* buf = reinterpret_cast<float*>(order + kMaxCand);        // [E]
+  __shared__ float s_red[4];
+  __shared__ float s_top, s_vb, s_m;
+  __shared__ int s_nc;
+  __shared__ unsigned long long s_marked;
+  __shared__ int s_sel_i[32];
+  __shared__ float s_sel_v[32];
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const int E = a.E, k = a.k;
+  const int R = k < E ? k + 1 : k;
   const uint32_t n = *a.qcount;
-  for (uint32_t i = blockIdx.x * (blockDim.x >> 5) + wid; i < n;
-       i += gridDim.x * (blockDim.x >> 5))
-    warp_token<T, VPL>(a, sm, a.queue[i], lane);
+  for (uint32_t q = blockIdx.x; q < n; q += gridDim.x) {
+    const int64_t t = a.queue[q];
+    const float* row = a.logits + t * a.ldl;
+    float m = -INFINITY;
+    for (int e = tid; e < E; e += blockDim.x) {
+      float v = row[e];
+      for (int sp = 1; sp < a.nsplit; ++sp) v += row[sp * a.split_stride + e];
+      buf[e] = v;
+      m = fmaxf(m, v);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) s_red[wid] = m;
+    if (tid == 0) s_marked = 0ull;
+    __syncthreads();
+    if (wid == 0) {
+      // fp32 selection rounds (E <= 512: 16 values a lane)
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int e = lane + 32 * j;
+        v[j] = e < E ? buf[e] : -INFINITY;
+      }
+      uint32_t taken = 0u;
+      for (int r = 0; r < R; ++r) {
+        float bv = -INFINITY;
+        int bi = 0x7fffffff;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int e = lane + 32 * j;
+          const bool free = e < E && !(taken & (1u << j));
+          if (free && (bi == 0x7fffffff || better(v[j], e, bv, bi))) { bv = v[j]; bi = e; }
+        }
+        warp_argmax(bv, bi);
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (lane == 0) {
+          s_sel_i[r] = bi;
+          s_sel_v[r] = bv;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        s_top = s_sel_v[0];
+        s_vb = s_sel_v[R - 1];
+        s_m = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
+      }
+      __syncwarp();
+      const float tau = tie_bound(a, s_top, s_vb);
+      int nc = 0;
+      for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        const bool c = e < E && buf[e] >= s_vb - tau;
+        const unsigned msk = __ballot_sync(0xffffffffu, c);
+        const int pos = nc + __popc(msk & ((1u << lane) - 1u));
+        if (c && pos < kMaxCand) cand_i[pos] = e;
+        nc += __popc(msk);
+      }
+      if (lane == 0) s_nc = nc;
+    }
+    __syncthreads();
+    const float tau = tie_bound(a, s_top, s_vb);
+    const int nc = s_nc;
+    const bool exact = nc <= kMaxCand;
+    if (exact && tid < nc) {
+      const float vc = buf[cand_i[tid]];
+      bool mk = false;
+      for (int o = 0; o < nc; ++o) mk |= (o != tid) && fabsf(vc - buf[cand_i[o]]) < tau;
+      cand_v[tid] = make_float2(vc, 0.f);
+      if (mk) atomicOr(&s_marked, 1ull << tid);
+    }
+    __syncthreads();
+    if (exact) {
+      const T* xr = reinterpret_cast<const T*>(a.x) + t * a.H;
+      int i = 0;
+      for (unsigned long long mm = s_marked; mm; mm &= mm - 1, ++i) {
+        if ((i & 3) != wid) continue;
+        const int c = __ffsll((long long)mm) - 1;
+        const T* wr = reinterpret_cast<const T*>(a.w) + (int64_t)cand_i[c] * a.H;
+        const float2 v = dot2<T>(xr, wr, a.H, lane);
+        if (lane == 0) cand_v[c] = v;
+      }
+    }
+    __syncthreads();
+    if (tid == 0) {
+      if (a.redecided) atomicAdd(a.redecided, 1u);
+      if (exact) {
+        // insertion sort of the candidates by (value desc, index asc)
+        for (int c = 0; c < nc; ++c) {
+          int p = c;
+          while (p > 0 && better2(cand_v[c], cand_i[c], cand_v[order[p - 1]], cand_i[order[p - 1]])) {
+            order[p] = order[p - 1];
+            --p;
+          }
+          order[p] = c;
+        }
+        for (int r = 0; r < R && r < nc; ++r) {
+          s_sel_i[r] = cand_i[order[r]];
+          s_sel_v[r] = buf[cand_i[order[r]]];
+        }
+      }
+    }
+    __syncthreads();
+    // weights, as the other paths form them (fp32 logits)
+    const float ref = a.norm ? s_sel_v[0] : s_m;
+    float denom = 0.f;
+    if (a.norm) {
+      for (int r = tid; r < k; r += blockDim.x) denom += expf(s_sel_v[r] - ref);
+    } else {
+      for (int e = tid; e < E; e += blockDim.x) denom += expf(buf[e] - ref);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, o);
+    __syncthreads();
+    if (lane == 0) s_red[wid] = denom;
+    __syncthreads();
+    denom = s_red[0] + s_red[1] + s_red[2] + s_red[3];
+    for (int r = tid; r < k; r += blockDim.x) {
+      a.idx[t * k + r] = s_sel_i[r];
+      a.wout[t * k + r] = expf(s_sel_v[r] - ref) / denom;
+    }
+    if (a.gated && tid == 0) {
+      float z = row[E];
+      for (int sp = 1; sp < a.nsplit; ++sp) z += row[sp * a.split_stride + E];
+      a.gate[t] = 1.0f / (1.0f + expf(-z));
+    }
+    __syncthreads();
+  }
 }
 
 // G lanes per token (G a power of two, G tokens' groups per warp), for
@@ -366,7 +505,7 @@ __global__ void __launch_bounds__(128) topk_queue_kernel(TopkArgs a) {
 // registers; each of the k+1 rounds is a register scan plus log2(G) shuffle
 // steps inside the group.  A token whose sorted top-(k+1) list has two
 // neighbours closer than the tie bound is appended to the queue and decided
-// again by topk_queue_kernel; the others get their weights and gate here.
+// again by topk_refine_kernel; the others get their weights and gate here.
 template <int G, int VPL>
 __global__ void __launch_bounds__(128) topk_group_kernel(TopkArgs a) {
   constexpr int TPB = 128 / G;            // tokens per block
@@ -454,30 +593,25 @@ __global__ void __launch_bounds__(128) topk_group_kernel(TopkArgs a) {
 }
 
 template <typename T, int VPL>
-cudaError_t launch_warp_t(const TopkArgs& a, bool queue, size_t smem, cudaStream_t st) {
+cudaError_t launch_warp_t(const TopkArgs& a, size_t smem, cudaStream_t st) {
   if (smem * 4 > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(queue ? topk_queue_kernel<T, VPL> : topk_warp_kernel<T, VPL>,
+    cudaError_t e = cudaFuncSetAttribute(topk_warp_kernel<T, VPL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)(smem * 4));
     if (e != cudaSuccess) return e;
   }
-  if (queue) {
-    int blocks = 2 * 152;
-    topk_queue_kernel<T, VPL><<<blocks, 128, smem * 4, st>>>(a);
-  } else {
-    topk_warp_kernel<T, VPL><<<(unsigned)((a.T + 3) / 4), 128, smem * 4, st>>>(a);
-  }
+  topk_warp_kernel<T, VPL><<<(unsigned)((a.T + 3) / 4), 128, smem * 4, st>>>(a);
   return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t launch_warp(const TopkArgs& a, int vpl, bool queue, size_t smem, cudaStream_t st) {
+cudaError_t launch_warp(const TopkArgs& a, int vpl, size_t smem, cudaStream_t st) {
   switch (vpl) {
-    case 1: return launch_warp_t<T, 1>(a, queue, smem, st);
-    case 2: return launch_warp_t<T, 2>(a, queue, smem, st);
-    case 4: return launch_warp_t<T, 4>(a, queue, smem, st);
-    case 8: return launch_warp_t<T, 8>(a, queue, smem, st);
-    default: return launch_warp_t<T, 0>(a, queue, smem, st);
+    case 1: return launch_warp_t<T, 1>(a, smem, st);
+    case 2: return launch_warp_t<T, 2>(a, smem, st);
+    case 4: return launch_warp_t<T, 4>(a, smem, st);
+    case 8: return launch_warp_t<T, 8>(a, smem, st);
+    default: return launch_warp_t<T, 0>(a, smem, st);
   }
 }
 
@@ -516,8 +650,8 @@ cudaError_t launch_topk(const Shape& s, const float* logits, int nsplit, const v
   const size_t per_warp = warp_smem_bytes(s.E);
   cudaError_t e;
   if (R > 32 || s.E > 512 || s.T <= 256) {   // warp per token; no queue for few tokens
-    e = s.dtype == MOE_F32 ? launch_warp<float>(a, vpl, false, per_warp, st)
-                           : launch_warp<bf16>(a, vpl, false, per_warp, st);
+    e = s.dtype == MOE_F32 ? launch_warp<float>(a, vpl, per_warp, st)
+                           : launch_warp<bf16>(a, vpl, per_warp, st);
     if (e != cudaSuccess) return e;
     count_launch();
     return cudaSuccess;
@@ -539,11 +673,12 @@ cudaError_t launch_topk(const Shape& s, const float* logits, int nsplit, const v
   }
   count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  e = s.dtype == MOE_F32 ? launch_warp<float>(a, vpl, true, per_warp, st)
-                         : launch_warp<bf16>(a, vpl, true, per_warp, st);
-  if (e != cudaSuccess) return e;
+  const size_t rsm = (size_t)kMaxCand * 16 + (size_t)s.E * 4;
+  const unsigned rblocks = (unsigned)(s.T < 1024 ? s.T : 1024);
+  if (s.dtype == MOE_F32) topk_refine_kernel<float><<<rblocks, 128, rsm, st>>>(a);
+  else topk_refine_kernel<bf16><<<rblocks, 128, rsm, st>>>(a);
   count_launch();
-  return cudaSuccess;
+  return cudaGetLastError();
 }
 
 namespace {
