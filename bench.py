@@ -94,7 +94,7 @@ class Clocks:
         try:
             self.p = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.p = None
@@ -313,7 +313,7 @@ def main():
         dist.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.05)   # let the sampler start
     t_wall = time.perf_counter()
     per_stage, step_ms = [], []
     for i in range(args.steps):

@@ -21,7 +21,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y_pe
                                                       const float* __restrict__ w, int k, int H,
                                                       const T* __restrict__ shared_out,
                                                       const float* __restrict__ gate,
-                                                      T* __restrict__ y) {
+                                                      T* __restrict__ y,
+                                                      const float* __restrict__ shared_part,
+                                                      int nsplit_sh, int64_t part_stride) {
   extern __shared__ int32_t sm[];
   int32_t* rows = sm;                                    // [k]
   float* wt = reinterpret_cast<float*>(sm + k);          // [k]
@@ -58,6 +60,21 @@ __global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y_pe
       unpack16(u, f, (const T*)nullptr);
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[i] = fmaf(g, f[i], acc[i]);
+    } else if (shared_part) {
+      // the shared output as split-K partial sums, added in order
+      float f[V];
+#pragma unroll
+      for (int i = 0; i < V; ++i) f[i] = 0.f;
+      for (int sp = 0; sp < nsplit_sh; ++sp) {
+        const float* src = shared_part + sp * part_stride + t * H + (int64_t)v * V;
+#pragma unroll
+        for (int i = 0; i < V; i += 4) {
+          const float4 q = __ldg(reinterpret_cast<const float4*>(src + i));
+          f[i] += q.x; f[i + 1] += q.y; f[i + 2] += q.z; f[i + 3] += q.w;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] = fmaf(g, f[i], acc[i]);
     }
     reinterpret_cast<uint4*>(y + t * H)[v] = pack16(acc, (const T*)nullptr);
   }
@@ -67,7 +84,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y_pe
 
 cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* scatter_index,
                            const float* topk_w, const void* shared_out, const float* gate,
-                           void* y, cudaStream_t st) {
+                           void* y, cudaStream_t st, const float* shared_part, int nsplit_sh) {
+  const int64_t part_stride = s.T * (int64_t)s.H;
   if (s.T == 0) return cudaSuccess;
   const size_t smem = (size_t)s.k * 8;
   // few tokens: split each row over several blocks (about 2 vectors a thread)
@@ -78,11 +96,13 @@ cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* sc
   if (s.dtype == MOE_F32) {
     combine_kernel<float><<<grid, 128, smem, st>>>(
         reinterpret_cast<const float*>(y_perm), scatter_index, topk_w, s.k, s.H,
-        reinterpret_cast<const float*>(shared_out), gate, reinterpret_cast<float*>(y));
+        reinterpret_cast<const float*>(shared_out), gate, reinterpret_cast<float*>(y),
+        shared_part, nsplit_sh, part_stride);
   } else {
     combine_kernel<bf16><<<grid, 128, smem, st>>>(
         reinterpret_cast<const bf16*>(y_perm), scatter_index, topk_w, s.k, s.H,
-        reinterpret_cast<const bf16*>(shared_out), gate, reinterpret_cast<bf16*>(y));
+        reinterpret_cast<const bf16*>(shared_out), gate, reinterpret_cast<bf16*>(y),
+        shared_part, nsplit_sh, part_stride);
   }
   count_launch();
   return cudaGetLastError();

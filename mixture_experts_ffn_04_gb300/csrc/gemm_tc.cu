@@ -44,7 +44,11 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
 constexpr int MAX_SMEM_G = 1024;   // larger group counts use a schedule kernel
 constexpr int SCHED_BYTES = (MAX_SMEM_G + 1) * 4;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + SCHED_BYTES;
+// epilogue staging: per epilogue warp 32 rows x (128 B + 16 B pad)
+constexpr int OUT_ROW_BYTES = 144;
+constexpr int OUT_WARP_BYTES = 32 * OUT_ROW_BYTES;
+constexpr int OUT_BYTES = 4 * OUT_WARP_BYTES;
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + OUT_BYTES + SCHED_BYTES;
 // kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
 // B bf16 (10-12 = 1), both K-major (15, 16 = 0), N >> 3 at 17-22, M >> 4 at 24-28.
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
@@ -250,7 +254,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   // bars: full[0..S), empty[S..2S), tfull[2S..2S+2), tempty[2S+2..2S+4), final[2S+4]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int32_t* s_sched = reinterpret_cast<int32_t*>(smem + STAGES * STAGE_BYTES + BAR_BYTES);
+  unsigned char* s_out = smem + STAGES * STAGE_BYTES + BAR_BYTES;
+  int32_t* s_sched = reinterpret_cast<int32_t*>(s_out + OUT_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
@@ -360,8 +365,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else {
     // ---------------- epilogue (warps 2..5) ----------------
+    // Each thread owns one accumulator row (its TMEM lane).  A 32-column
+    // chunk is finished in registers, staged in this warp's shared-memory
+    // slice, and written back row by row with 16-byte stores, 4 or 8 lanes per
+    // row, so every global write covers whole sectors.
     const int q = warp & 3;  // TMEM lanes this warp may read: 32q .. 32q+31
-    const int r = q * 32 + lane;
+    unsigned char* stage = s_out + (warp - 2) * OUT_WARP_BYTES;
+    unsigned char* my_row = stage + lane * OUT_ROW_BYTES;
     int acc = 0;
     uint32_t aph = 0;
     for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -369,80 +379,89 @@ __global__ void __launch_bounds__(THREADS, 1)
       decode_tile(a, sched, tile, ks, g, mt, nt);
       const int64_t gbeg = a.offsets ? a.offsets[g] : 0;
       const int64_t gend = a.offsets ? a.offsets[g + 1] : a.single_rows;
-      const int64_t row = gbeg + (int64_t)mt * BM + r;
-      const bool row_ok = row < gend;
+      const int64_t row0 = gbeg + (int64_t)mt * BM + q * 32;   // this warp's first row
+      const int64_t nvalid64 = gend - row0;
+      const int nvalid = nvalid64 < 0 ? 0 : (nvalid64 > 32 ? 32 : (int)nvalid64);
       // all 32 lanes must agree before the warp-collective tcgen05.ld
       if (!__all_sync(0xffffffffu, mbar_wait(tfull_bar(acc), aph, abort_flag))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * BN;
-      if (a.mode == kSwiGLU) {
-        const int n0 = nt * (BN / 2);
-        bf16* out = reinterpret_cast<bf16*>(a.out) + row * a.ldo;
+      if (a.mode != kStoreF32) {
+        const bool swiglu = a.mode == kSwiGLU;
+        const int n0 = swiglu ? nt * (BN / 2) : nt * BN;
+        const int ncols = swiglu ? BN / 2 : BN;
+        bf16* out = reinterpret_cast<bf16*>(a.out);
 #pragma unroll 1
-        for (int c = 0; c < BN / 2 && n0 + c < a.N; c += 32) {
-          uint32_t gr[32], ur[32];
+        for (int c = 0; c < ncols && n0 + c < a.N; c += 32) {
+          uint32_t gr[32];
+          uint4 packed[4];
           tmem_ld32(taddr + c, gr);
-          tmem_ld32(taddr + BN / 2 + c, ur);
-          tmem_wait_ld();
-          if (row_ok) {
+          if (swiglu) {
+            uint32_t ur[32];
+            tmem_ld32(taddr + BN / 2 + c, ur);
+            tmem_wait_ld();
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              const int n = n0 + c + v * 8;
-              if (n < a.N) {
-                float f[8];
+              float f[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                  f[e] = silu_f(__uint_as_float(gr[v * 8 + e])) * __uint_as_float(ur[v * 8 + e]);
-                *reinterpret_cast<uint4*>(out + n) = pack16(f, (const bf16*)nullptr);
-              }
+              for (int e = 0; e < 8; ++e)
+                f[e] = silu_fast(__uint_as_float(gr[v * 8 + e])) * __uint_as_float(ur[v * 8 + e]);
+              packed[v] = pack16(f, (const bf16*)nullptr);
             }
-          }
-        }
-      } else if (a.mode == kStoreAct) {
-        const int n0 = nt * BN;
-        bf16* out = reinterpret_cast<bf16*>(a.out) + row * a.ldo;
-#pragma unroll 1
-        for (int c = 0; c < BN && n0 + c < a.N; c += 32) {
-          uint32_t vr[32];
-          tmem_ld32(taddr + c, vr);
-          tmem_wait_ld();
-          if (row_ok) {
+          } else {
+            tmem_wait_ld();
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
-              const int n = n0 + c + v * 8;
-              if (n < a.N) {
-                float f[8];
+              float f[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(vr[v * 8 + e]);
-                *reinterpret_cast<uint4*>(out + n) = pack16(f, (const bf16*)nullptr);
-              }
+              for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(gr[v * 8 + e]);
+              packed[v] = pack16(f, (const bf16*)nullptr);
             }
           }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) reinterpret_cast<uint4*>(my_row)[v] = packed[v];
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int p = lane + 32 * i;      // 128 pieces: 32 rows x 4 x 16 B
+            const int rr = p >> 2, pc = p & 3;
+            const int n = n0 + c + pc * 8;
+            if (rr < nvalid && n < a.N)
+              *reinterpret_cast<uint4*>(out + (row0 + rr) * a.ldo + n) =
+                  *reinterpret_cast<const uint4*>(stage + rr * OUT_ROW_BYTES + pc * 16);
+          }
+          __syncwarp();
         }
       } else {
         // fp32 rows (router logits): ldo and split_stride are multiples of 4
         const int n0 = nt * BN;
-        float* out = reinterpret_cast<float*>(a.out) + ks * a.split_stride + row * a.ldo;
+        float* out = reinterpret_cast<float*>(a.out) + ks * a.split_stride;
 #pragma unroll 1
         for (int c = 0; c < BN && n0 + c < a.N; c += 32) {
           uint32_t vr[32];
           tmem_ld32(taddr + c, vr);
           tmem_wait_ld();
-          if (row_ok) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              const int n = n0 + c + e;
+          for (int v = 0; v < 8; ++v)
+            reinterpret_cast<uint4*>(my_row)[v] =
+                make_uint4(vr[4 * v], vr[4 * v + 1], vr[4 * v + 2], vr[4 * v + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int p = lane + 32 * i;      // 256 pieces: 32 rows x 8 x 16 B
+            const int rr = p >> 3, pc = p & 7;
+            const int n = n0 + c + pc * 4;
+            if (rr < nvalid && n < a.N) {
+              float* dst = out + (row0 + rr) * a.ldo + n;
+              const float* src = reinterpret_cast<const float*>(stage + rr * OUT_ROW_BYTES + pc * 16);
               if (n + 3 < a.N) {
-                *reinterpret_cast<float4*>(out + n) =
-                    make_float4(__uint_as_float(vr[e]), __uint_as_float(vr[e + 1]),
-                                __uint_as_float(vr[e + 2]), __uint_as_float(vr[e + 3]));
+                *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(src);
               } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-                  if (n + q < a.N) out[n + q] = __uint_as_float(vr[e + q]);
+                for (int e = 0; e < 4 && n + e < a.N; ++e) dst[e] = src[e];
               }
             }
           }
+          __syncwarp();
         }
       }
       tc_fence_before();
@@ -512,6 +531,8 @@ int sm_count() {
 }
 
 }  // namespace tc
+
+int tc_sm_count() { return tc::sm_count(); }
 
 int router_split(int64_t rows, int ncols, int K) {
   const int64_t base = ((rows + tc::BM - 1) / tc::BM) * ((ncols + tc::BN - 1) / tc::BN);

@@ -103,8 +103,15 @@ cudaError_t launch_permute_scratch(const Shape& s, int nchunks, int tpc, int32_t
 // Record why the current host call failed (read back by moe_last_error).
 void set_error_message(const char* why);
 
+// shared_part/nsplit_sh: instead of shared_out, nsplit_sh fp32 partial sums
+// of the shared MLP output ([T, H] each, T*H apart), added in order.
 cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* scatter_index,
                            const float* topk_w, const void* shared_out, const float* gate,
-                           void* y, cudaStream_t st);
+                           void* y, cudaStream_t st, const float* shared_part = nullptr,
+                           int nsplit_sh = 0);
+
+// Shared-MLP down projection split over K for at most this many tokens.
+constexpr int64_t kSharedSplitMaxT = 4096;
+int tc_sm_count();
 
 }  // namespace moe

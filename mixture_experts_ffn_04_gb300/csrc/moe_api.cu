@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <string.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "../../include/moe.h"
@@ -116,7 +117,12 @@ Layout layout_for(const Shape& s) {
   L.h = off; off += align256(T * k * (size_t)s.I * s.esize);
   L.y_perm = off; off += align256(T * k * (size_t)s.H * s.esize);
   L.sh_h = off; off += align256(T * (size_t)s.I_sh * s.esize);
-  L.sh_out = off; off += align256(s.I_sh ? T * (size_t)s.H * s.esize : 0);
+  // the shared MLP's output: bf16/fp32 rows, or (few tokens, see
+  // shared_split) up to kMaxSplit fp32 partial sums over K
+  size_t sh_bytes = s.I_sh ? T * (size_t)s.H * s.esize : 0;
+  if (s.I_sh && s.T <= kSharedSplitMaxT)
+    sh_bytes = std::max(sh_bytes, (size_t)kMaxSplit * T * (size_t)s.H * 4);
+  L.sh_out = off; off += align256(sh_bytes);
   L.total = off;
   return L;
 }
@@ -127,7 +133,29 @@ static int engine_for(const GemmArgs& a) {
   const int64_t rows = a.offsets ? a.rows_bound : a.single_rows;
   if (a.dtype == MOE_F32) return ov == 3 ? 3 : 1;
   if (ov >= 1 && ov <= 3) return ov;
-  return rows <= 16 ? 3 : 2;
+  return rows <= 4 ? 3 : 2;
+}
+
+// K split of the shared MLP's down projection on the tensor cores: its N = H
+// gives few output tiles when T is small, so the K range is split until the
+// tiles fill the SMs in whole waves (at least 8 k-blocks per split); the
+// combine kernel adds the fp32 partial sums.
+static int shared_split(const Shape& s, const GemmArgs& down) {
+  if (s.T > kSharedSplitMaxT || engine_for(down) != 2) return 1;
+  const int64_t base = ((s.T + 127) / 128) * ((s.H + 255) / 256);
+  const int kb = (s.I_sh + 63) / 64;
+  const int64_t sms = tc_sm_count();
+  int best = 1;
+  double best_eff = 0.0;
+  for (int sp = 1; sp <= kMaxSplit && kb / sp >= 8; ++sp) {
+    const int64_t tiles = base * sp;
+    const double eff = (double)tiles / (double)(((tiles + sms - 1) / sms) * sms);
+    if (eff > best_eff + 0.02) {
+      best_eff = eff;
+      best = sp;
+    }
+  }
+  return best;
 }
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t st) {
@@ -487,6 +515,7 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
 
   STAGE_EVENT(MOE_STAGE_SHARED);
   void* sh_out = nullptr;
+  int sh_split = 1;
   if (s.I_sh) {
     sh_out = w + L.sh_out;
     GemmArgs b;
@@ -515,10 +544,21 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
     b.K = s.I_sh;
     b.out = sh_out;
     b.ldo = s.H;
+    sh_split = shared_split(s, b);
+    if (sh_split > 1) {
+      b.mode = kStoreF32;
+      b.ksplit = sh_split;
+      b.split_stride = s.T * (int64_t)s.H;
+    }
     CHECK_CUDA(launch_grouped_gemm(b, st));
   }
   STAGE_EVENT(MOE_STAGE_COMBINE);
-  CHECK_CUDA(launch_combine(s, y_perm, sidx, use_w, sh_out, gate, y, st));
+  if (sh_split > 1) {
+    CHECK_CUDA(launch_combine(s, y_perm, sidx, use_w, nullptr, gate, y, st,
+                              static_cast<const float*>(sh_out), sh_split));
+  } else {
+    CHECK_CUDA(launch_combine(s, y_perm, sidx, use_w, sh_out, gate, y, st));
+  }
   STAGE_EVENT(MOE_NUM_STAGES);
 #undef STAGE_EVENT
   return MOE_OK;
