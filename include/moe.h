@@ -116,7 +116,9 @@ typedef struct {
   void *x_perm;           /* [T * k, H] */
   void *h;                /* [T * k, I] */
   void *y_perm;           /* [T * k, H] */
-  void *shared_out;       /* [T, H] (when shared_inter > 0) */
+  void *shared_out;       /* [T, H] (when shared_inter > 0); for T <= 4096 on the
+                             tensor-core engine it may hold fp32 partial sums
+                             over K instead, which the combine adds */
 } moe_route_info;
 
 /* Packed routing-shape word (compiler page, Group A: (num_experts << 8) |
