@@ -15,7 +15,8 @@
 namespace moe {
 namespace {
 
-template <typename T>
+// SH: 0 no shared term, 1 shared row of T, 2 fp32 split-K partial sums.
+template <typename T, int SH>
 __global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y_perm,
                                                       const int32_t* __restrict__ sidx,
                                                       const float* __restrict__ w, int k, int H,
@@ -44,23 +45,34 @@ __global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y_pe
     float acc[V];
 #pragma unroll
     for (int i = 0; i < V; ++i) acc[i] = 0.f;
-    for (int s = 0; s < k; ++s) {
-      const int r = rows[s];
-      if (r < 0) continue;  // pair dropped for an out-of-range route
-      const uint4 u = __ldg(reinterpret_cast<const uint4*>(y_perm + (int64_t)r * H) + v);
-      float f[V];
-      unpack16(u, f, (const T*)nullptr);
-      const float ws = wt[s];
+    // up to 8 slot rows in flight at a time, then accumulate in slot order
+    for (int s0 = 0; s0 < k; s0 += 8) {
+      uint4 u[8];
 #pragma unroll
-      for (int i = 0; i < V; ++i) acc[i] = fmaf(ws, f[i], acc[i]);
+      for (int j = 0; j < 8; ++j) {
+        const int s = s0 + j;
+        if (s < k && rows[s] >= 0)   // rows[s] < 0: pair dropped (route out of range)
+          u[j] = __ldg(reinterpret_cast<const uint4*>(y_perm + (int64_t)rows[s] * H) + v);
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int s = s0 + j;
+        if (s < k && rows[s] >= 0) {
+          float f[V];
+          unpack16(u[j], f, (const T*)nullptr);
+          const float ws = wt[s];
+#pragma unroll
+          for (int i = 0; i < V; ++i) acc[i] = fmaf(ws, f[i], acc[i]);
+        }
+      }
     }
-    if (shared_out) {
+    if (SH == 1) {
       const uint4 u = __ldg(reinterpret_cast<const uint4*>(shared_out + t * H) + v);
       float f[V];
       unpack16(u, f, (const T*)nullptr);
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[i] = fmaf(g, f[i], acc[i]);
-    } else if (shared_part) {
+    } else if (SH == 2) {
       // the shared output as split-K partial sums, added in order
       float f[V];
 #pragma unroll
@@ -93,16 +105,21 @@ cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* sc
   int ysplit = 1;
   if (s.T < 1024) ysplit = (nvec + 255) / 256;
   const dim3 grid((unsigned)s.T, (unsigned)ysplit);
+  const int sh = shared_part ? 2 : (shared_out ? 1 : 0);
   if (s.dtype == MOE_F32) {
-    combine_kernel<float><<<grid, 128, smem, st>>>(
-        reinterpret_cast<const float*>(y_perm), scatter_index, topk_w, s.k, s.H,
-        reinterpret_cast<const float*>(shared_out), gate, reinterpret_cast<float*>(y),
-        shared_part, nsplit_sh, part_stride);
+    const float* yp = reinterpret_cast<const float*>(y_perm);
+    const float* so = reinterpret_cast<const float*>(shared_out);
+    float* yo = reinterpret_cast<float*>(y);
+    if (sh == 0) combine_kernel<float, 0><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, yo, shared_part, nsplit_sh, part_stride);
+    else if (sh == 1) combine_kernel<float, 1><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, yo, shared_part, nsplit_sh, part_stride);
+    else combine_kernel<float, 2><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, yo, shared_part, nsplit_sh, part_stride);
   } else {
-    combine_kernel<bf16><<<grid, 128, smem, st>>>(
-        reinterpret_cast<const bf16*>(y_perm), scatter_index, topk_w, s.k, s.H,
-        reinterpret_cast<const bf16*>(shared_out), gate, reinterpret_cast<bf16*>(y),
-        shared_part, nsplit_sh, part_stride);
+    const bf16* yp = reinterpret_cast<const bf16*>(y_perm);
+    const bf16* so = reinterpret_cast<const bf16*>(shared_out);
+    bf16* yo = reinterpret_cast<bf16*>(y);
+    if (sh == 0) combine_kernel<bf16, 0><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, yo, shared_part, nsplit_sh, part_stride);
+    else if (sh == 1) combine_kernel<bf16, 1><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, yo, shared_part, nsplit_sh, part_stride);
+    else combine_kernel<bf16, 2><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, yo, shared_part, nsplit_sh, part_stride);
   }
   count_launch();
   return cudaGetLastError();
