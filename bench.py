@@ -37,7 +37,10 @@ METRIC = "MoE layer tokens/s and grouped-GEMM TFLOP/s (% bf16 peak) on 1 GB300"
 # dram__bytes_read.sum + dram__bytes_write.sum of one gate/up grouped-GEMM
 # launch, from an ncu capture, keyed by workload; valid only while the kernel
 # source hashes to the recorded value.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # profiles/tc_gemm_qwen3-30b-a3b-shape-T4096.md
+    "qwen3-30b-a3b-shape-T4096": {"bytes": 987602944, "kernel_hash": "6e010bc3b40da70b"},
+}
 
 
 def _kernel_hash() -> str:
