@@ -35,20 +35,26 @@
 namespace moe {
 namespace tc {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+constexpr int BM = 128, BN = 256, BK = 64;
+// Two load rings: the weight tiles (B, mostly first touches in DRAM) get a
+// deeper ring than the activation tiles (A, mostly re-read from L2), so more
+// DRAM bytes are in flight per SM within the shared-memory budget.
+constexpr int SA = 3, SB = 5;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int THREADS = 192;
+constexpr int RING_BYTES = SA * A_BYTES + SB * B_BYTES;
+// warps: 0 A producer, 1 MMA issuer, 2-5 epilogue, 6 B producer
+constexpr int THREADS = 224;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
 constexpr int MAX_SMEM_G = 1024;   // larger group counts use a schedule kernel
 constexpr int SCHED_BYTES = (MAX_SMEM_G + 1) * 4;
-// epilogue staging: per epilogue warp 32 rows x (128 B + 16 B pad)
-constexpr int OUT_ROW_BYTES = 144;
+// epilogue staging: per epilogue warp 32 rows x (64 B + 16 B pad)
+constexpr int OUT_ROW_BYTES = 80;
 constexpr int OUT_WARP_BYTES = 32 * OUT_ROW_BYTES;
 constexpr int OUT_BYTES = 4 * OUT_WARP_BYTES;
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + BAR_BYTES + OUT_BYTES + SCHED_BYTES;
+constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES + OUT_BYTES + SCHED_BYTES;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 // kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
 // B bf16 (10-12 = 1), both K-major (15, 16 = 0), N >> 3 at 17-22, M >> 4 at 24-28.
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
@@ -250,25 +256,32 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  // bars: full[0..S), empty[S..2S), tfull[2S..2S+2), tempty[2S+2..2S+4), final[2S+4]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
+  // bars: fullA[SA] emptyA[SA] fullB[SB] emptyB[SB] tfull[2] tempty[2] final
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * SA + 2 * SB + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  unsigned char* s_out = smem + STAGES * STAGE_BYTES + BAR_BYTES;
+  unsigned char* s_out = smem + RING_BYTES + BAR_BYTES;
   int32_t* s_sched = reinterpret_cast<int32_t*>(s_out + OUT_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
-  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
-  auto empty_bar = [&](int s) { return smem_u32(&bars[STAGES + s]); };
-  auto tfull_bar = [&](int b) { return smem_u32(&bars[2 * STAGES + b]); };
-  auto tempty_bar = [&](int b) { return smem_u32(&bars[2 * STAGES + 2 + b]); };
-  const uint32_t final_bar = smem_u32(&bars[2 * STAGES + 4]);
+  const uint32_t ringA = smem_base, ringB = smem_base + SA * A_BYTES;
+  auto fullA = [&](int s) { return smem_u32(&bars[s]); };
+  auto emptyA = [&](int s) { return smem_u32(&bars[SA + s]); };
+  auto fullB = [&](int s) { return smem_u32(&bars[2 * SA + s]); };
+  auto emptyB = [&](int s) { return smem_u32(&bars[2 * SA + SB + s]); };
+  auto tfull_bar = [&](int b) { return smem_u32(&bars[2 * SA + 2 * SB + b]); };
+  auto tempty_bar = [&](int b) { return smem_u32(&bars[2 * SA + 2 * SB + 2 + b]); };
+  const uint32_t final_bar = smem_u32(&bars[2 * SA + 2 * SB + 4]);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+    for (int s = 0; s < SA; ++s) {
+      mbar_init(fullA(s), 1);
+      mbar_init(emptyA(s), 1);
+    }
+    for (int s = 0; s < SB; ++s) {
+      mbar_init(fullB(s), 1);
+      mbar_init(emptyB(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -292,47 +305,51 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int64_t total = (int64_t)sched[a.G] * a.NT * a.ksplit;
 
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer ----------------
-      int s = 0;
-      uint32_t ph = 0, issued = 0, par = 0;
-      for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
-        int ks, g, mt, nt;
-        decode_tile(a, sched, tile, ks, g, mt, nt);
-        const int64_t gbase = a.offsets ? a.offsets[g] : 0;
-        const int arow = (int)(gbase + (int64_t)mt * BM);
-        const int kb0 = ks * a.KB / a.ksplit, kb1 = (ks + 1) * a.KB / a.ksplit;
-        bool ok = true;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag)) { ok = false; break; }
-          const uint32_t sa = smem_base + s * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
-          mbar_expect_tx(full_bar(s), STAGE_BYTES);
-          tma_load_2d(sa, &tmA, kb * BK, arow, full_bar(s));
+  if ((warp == 0 || warp == 6) && lane == 0) {
+    // ---------------- TMA producers: warp 0 the A ring, warp 6 the B ring ----
+    const bool is_a = warp == 0;
+    const int S = is_a ? SA : SB;
+    int s = 0;
+    uint32_t ph = 0, issued = 0, par = 0;
+    for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      int ks, g, mt, nt;
+      decode_tile(a, sched, tile, ks, g, mt, nt);
+      const int64_t gbase = a.offsets ? a.offsets[g] : 0;
+      const int arow = (int)(gbase + (int64_t)mt * BM);
+      const int kb0 = ks * a.KB / a.ksplit, kb1 = (ks + 1) * a.KB / a.ksplit;
+      bool ok = true;
+      for (int kb = kb0; kb < kb1; ++kb) {
+        const uint32_t fb = is_a ? fullA(s) : fullB(s);
+        if (!mbar_wait(is_a ? emptyA(s) : emptyB(s), ph ^ 1u, abort_flag)) { ok = false; break; }
+        if (is_a) {
+          mbar_expect_tx(fb, A_BYTES);
+          tma_load_2d(ringA + s * A_BYTES, &tmA, kb * BK, arow, fb);
+        } else {
+          const uint32_t sb = ringB + s * B_BYTES;
+          mbar_expect_tx(fb, B_BYTES);
           if (a.mode == kSwiGLU) {
-            tma_load_3d(sb, &tmB0, kb * BK, nt * (BN / 2), g, full_bar(s));
-            tma_load_3d(sb + B_BYTES / 2, &tmB1, kb * BK, nt * (BN / 2), g, full_bar(s));
+            tma_load_3d(sb, &tmB0, kb * BK, nt * (BN / 2), g, fb);
+            tma_load_3d(sb + B_BYTES / 2, &tmB1, kb * BK, nt * (BN / 2), g, fb);
           } else {
-            tma_load_3d(sb, &tmB0, kb * BK, nt * BN, g, full_bar(s));
+            tma_load_3d(sb, &tmB0, kb * BK, nt * BN, g, fb);
           }
-          issued |= 1u << s;
-          par = (par & ~(1u << s)) | (ph << s);
-          if (++s == STAGES) { s = 0; ph ^= 1u; }
         }
-        if (!ok) break;
+        issued |= 1u << s;
+        par = (par & ~(1u << s)) | (ph << s);
+        if (++s == S) { s = 0; ph ^= 1u; }
       }
-      if (*abort_flag) {
-        // let every load still in flight land before the CTA goes away
-        for (int i = 0; i < STAGES; ++i)
-          if (issued & (1u << i)) mbar_wait_quiet(full_bar(i), (par >> i) & 1u);
-      }
+      if (!ok) break;
+    }
+    if (*abort_flag) {
+      // let every load still in flight land before the CTA goes away
+      for (int i = 0; i < S; ++i)
+        if (issued & (1u << i)) mbar_wait_quiet(is_a ? fullA(i) : fullB(i), (par >> i) & 1u);
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ---------------- MMA issuer ----------------
-      int s = 0, acc = 0;
-      uint32_t ph = 0, aph = 0;
+      int sa = 0, sb = 0, acc = 0;
+      uint32_t pha = 0, phb = 0, aph = 0;
       bool ok = true;
       for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const int ks = (int)(tile / ((int64_t)sched[a.G] * a.NT));
@@ -341,17 +358,22 @@ __global__ void __launch_bounds__(THREADS, 1)
         tc_fence_after();
         const uint32_t d = tmem_base + (uint32_t)acc * BN;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(full_bar(s), ph, abort_flag)) { ok = false; break; }
+          if (!mbar_wait(fullA(sa), pha, abort_flag) || !mbar_wait(fullB(sb), phb, abort_flag)) {
+            ok = false;
+            break;
+          }
           tc_fence_after();
-          const uint32_t sa = smem_base + s * STAGE_BYTES;
-          const uint32_t sb = sa + A_BYTES;
+          const uint32_t a_addr = ringA + sa * A_BYTES;
+          const uint32_t b_addr = ringB + sb * B_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            tc_mma(d, sw128_desc(sa + kk * 32), sw128_desc(sb + kk * 32), IDESC,
+            tc_mma(d, sw128_desc(a_addr + kk * 32), sw128_desc(b_addr + kk * 32), IDESC,
                    (kb | kk) != 0 ? 1u : 0u);
           }
-          tc_commit(empty_bar(s));
-          if (++s == STAGES) { s = 0; ph ^= 1u; }
+          tc_commit(emptyA(sa));
+          tc_commit(emptyB(sb));
+          if (++sa == SA) { sa = 0; pha ^= 1u; }
+          if (++sb == SB) { sb = 0; phb ^= 1u; }
         }
         if (!ok) break;
         tc_commit(tfull_bar(acc));
@@ -363,7 +385,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         mbar_wait_quiet(final_bar, 0);
       }
     }
-  } else {
+  } else if (warp >= 2 && warp <= 5) {
     // ---------------- epilogue (warps 2..5) ----------------
     // Each thread owns one accumulator row (its TMEM lane).  A 32-column
     // chunk is finished in registers, staged in this warp's shared-memory
@@ -442,26 +464,31 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld32(taddr + c, vr);
           tmem_wait_ld();
 #pragma unroll
-          for (int v = 0; v < 8; ++v)
-            reinterpret_cast<uint4*>(my_row)[v] =
-                make_uint4(vr[4 * v], vr[4 * v + 1], vr[4 * v + 2], vr[4 * v + 3]);
-          __syncwarp();
+          for (int hf = 0; hf < 2; ++hf) {   // two 16-column halves
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int p = lane + 32 * i;      // 256 pieces: 32 rows x 8 x 16 B
-            const int rr = p >> 3, pc = p & 7;
-            const int n = n0 + c + pc * 4;
-            if (rr < nvalid && n < a.N) {
-              float* dst = out + (row0 + rr) * a.ldo + n;
-              const float* src = reinterpret_cast<const float*>(stage + rr * OUT_ROW_BYTES + pc * 16);
-              if (n + 3 < a.N) {
-                *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(src);
-              } else {
-                for (int e = 0; e < 4 && n + e < a.N; ++e) dst[e] = src[e];
+            for (int v = 0; v < 4; ++v)
+              reinterpret_cast<uint4*>(my_row)[v] =
+                  make_uint4(vr[16 * hf + 4 * v], vr[16 * hf + 4 * v + 1], vr[16 * hf + 4 * v + 2],
+                             vr[16 * hf + 4 * v + 3]);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int p = lane + 32 * i;      // 128 pieces: 32 rows x 4 x 16 B
+              const int rr = p >> 2, pc = p & 3;
+              const int n = n0 + c + 16 * hf + pc * 4;
+              if (rr < nvalid && n < a.N) {
+                float* dst = out + (row0 + rr) * a.ldo + n;
+                const float* src =
+                    reinterpret_cast<const float*>(stage + rr * OUT_ROW_BYTES + pc * 16);
+                if (n + 3 < a.N) {
+                  *reinterpret_cast<float4*>(dst) = *reinterpret_cast<const float4*>(src);
+                } else {
+                  for (int e = 0; e < 4 && n + e < a.N; ++e) dst[e] = src[e];
+                }
               }
             }
+            __syncwarp();
           }
-          __syncwarp();
         }
       }
       tc_fence_before();
