@@ -39,7 +39,7 @@ constexpr int BM = 128, BN = 256, BK = 64;
 // Two load rings: the weight tiles (B, mostly first touches in DRAM) get a
 // deeper ring than the activation tiles (A, mostly re-read from L2), so more
 // DRAM bytes are in flight per SM within the shared-memory budget.
-constexpr int SA = 3, SB = 5;
+constexpr int SA = 4, SB = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int RING_BYTES = SA * A_BYTES + SB * B_BYTES;
