@@ -28,7 +28,8 @@
  *    validated on the host before anything is launched; an invalid call
  *    launches nothing and returns an error status.
  *  - Errors only visible on the device (a direct route >= E, more rows than
- *    the stated bound, a pipeline wait that ran out) never trap: the kernel
+ *    the stated bound, a gathered row's token out of range, a pipeline wait
+ *    that ran out) never trap: the kernel
  *    sets a bit in the workspace's status word and skips the offending work.
  *    moe_get_device_status() reads and clears it.
  *  - The workspace `ws` is caller-owned device memory of at least the size
@@ -54,7 +55,8 @@ typedef enum {
   MOE_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed */
   MOE_ERR_DEVICE_ROUTE = 5, /* device flag: a route index outside [0, E) */
   MOE_ERR_TIMEOUT = 6,      /* device flag: a bounded pipeline wait ran out */
-  MOE_ERR_ROWS = 7          /* device flag: group rows exceed the stated bound */
+  MOE_ERR_ROWS = 7,         /* device flag: group rows exceed the stated bound */
+  MOE_ERR_GATHER = 8        /* device flag: a row_token entry outside [0, T) */
 } moe_status;
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
@@ -163,7 +165,9 @@ moe_status moe_route(const moe_shape *shape, const void *x, const void *w_router
  * x_perm[scatter_index[t, s]] = x[t].  Deterministic, no global atomics.
  * topk_idx [T, k] is an input: the router's output or direct routes.  A route
  * outside [0, E) sets MOE_ERR_DEVICE_ROUTE on the device; that pair is then
- * dropped from every output. */
+ * dropped from every output.  x_perm == NULL: the routing arrays only (x may
+ * then be NULL too), for moe_grouped_swiglu_gather, which reads the rows of x
+ * through row_token instead of a grouped copy. */
 moe_status moe_permute(const moe_shape *shape, const void *x, const int32_t *topk_idx,
                        int32_t *counts, int32_t *offsets, int32_t *scatter_index,
                        int32_t *row_token, void *x_perm, void *ws, size_t ws_bytes,
@@ -204,6 +208,22 @@ moe_status moe_grouped_swiglu(const moe_shape *shape, const void *x_perm,
                               const int32_t *offsets, int32_t num_groups, int64_t rows_bound,
                               int32_t inter, void *h, void *ws, size_t ws_bytes,
                               void *stream);
+
+/* moe_grouped_swiglu with the rows gathered on the fly: row r of the grouped
+ * operand is x[row_token[r]] (x [T, H], T = shape->tokens, row_token as
+ * moe_permute writes it), so the [T*k, H] copy x_perm is never written nor
+ * read back.  Same grouping, accumulation and rounding as moe_grouped_swiglu,
+ * so h is bit-identical to moe_grouped_swiglu on moe_permute's x_perm.  Only
+ * rows inside a group are read; a row_token entry outside [0, T) contributes
+ * zeros and sets MOE_ERR_GATHER on the device.  For callers that cannot
+ * spare the [T*k, H] buffer: at prefill sizes it runs slower than the copy
+ * plus moe_grouped_swiglu (moe_layer_forward takes that route). */
+moe_status moe_grouped_swiglu_gather(const moe_shape *shape, const void *x,
+                                     const int32_t *row_token, const void *w_gate,
+                                     const void *w_up, int64_t expert_stride,
+                                     const int32_t *offsets, int32_t num_groups,
+                                     int64_t rows_bound, int32_t inter, void *h, void *ws,
+                                     size_t ws_bytes, void *stream);
 
 /* Grouped GEMM down: y_perm[r, n] = h[r] . w_down_g[n] for the rows of group g,
  * w_down_g = w_down + g * expert_stride ([H, inter]); same grouping rules as
@@ -251,7 +271,8 @@ moe_status moe_workspace_init(void *ws, void *stream);
 
 /* Synchronise `stream`, then read and clear the device status word of `ws`:
  * MOE_OK, or the first of MOE_ERR_DEVICE_ROUTE / MOE_ERR_ROWS /
- * MOE_ERR_TIMEOUT that is set (*bits, if non-NULL, receives every bit). */
+ * MOE_ERR_TIMEOUT / MOE_ERR_GATHER that is set (*bits, if non-NULL, receives
+ * every bit: 1 route, 2 rows, 4 timeout, 8 gather). */
 moe_status moe_get_device_status(void *ws, void *stream, uint32_t *bits);
 
 /* Synchronise `stream`, then read and clear the workspace's count of tokens

@@ -24,6 +24,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_DEVICE_ROUTE, MOE_ERR_TIMEOUT, MOE_ERR_ROWS = 4, 5, 6, 7
+MOE_ERR_GATHER = 8
 MOE_F32, MOE_BF16 = 0, 1
 STAGES = ("route", "permute", "gate_up", "down", "shared", "combine")
 
@@ -80,6 +81,7 @@ def lib():
         "moe_permute": (i32, [S, P, P, P, P, P, P, P, P, sz, P]),
         "moe_permute_static": (i32, [S, P, P, P, P, P, P, P, P]),
         "moe_grouped_swiglu": (i32, [S, P, P, P, i64, P, i32, i64, i32, P, P, sz, P]),
+        "moe_grouped_swiglu_gather": (i32, [S, P, P, P, P, i64, P, i32, i64, i32, P, P, sz, P]),
         "moe_grouped_down": (i32, [S, P, P, i64, P, i32, i64, i32, P, P, sz, P]),
         "moe_combine": (i32, [S, P, P, P, P, P, P, P]),
         "moe_layer_forward": (i32, [S, ctypes.POINTER(MoEWeights), P, P, P, P, P, sz, P]),
@@ -216,6 +218,16 @@ def moe_grouped_swiglu(shape, x_perm, w_gate, w_up, expert_stride, offsets, num_
                                     expert_stride, _p(offsets), num_groups, rows_bound, inter,
                                     _p(h), _p(ws), ws.numel() * ws.element_size(),
                                     _stream(stream)), "moe_grouped_swiglu")
+
+
+def moe_grouped_swiglu_gather(shape, x, row_token, w_gate, w_up, expert_stride, offsets,
+                              num_groups, rows_bound, inter, h, ws, stream=None, w_up_ptr=None):
+    up = w_up_ptr if w_up_ptr is not None else _p(w_up)
+    _check(lib().moe_grouped_swiglu_gather(ctypes.byref(shape), _p(x), _p(row_token), _p(w_gate),
+                                           up, expert_stride, _p(offsets), num_groups,
+                                           rows_bound, inter, _p(h), _p(ws),
+                                           ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_grouped_swiglu_gather")
 
 
 def moe_grouped_down(shape, h, w_down, expert_stride, offsets, num_groups, rows_bound, inter,

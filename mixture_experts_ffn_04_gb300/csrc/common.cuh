@@ -14,6 +14,7 @@ enum : uint32_t {
   kFlagRoute = 1u << 0,    // route index outside [0, E)
   kFlagRows = 1u << 1,     // group rows exceed the stated bound
   kFlagTimeout = 1u << 2,  // a bounded pipeline wait ran out
+  kFlagGather = 1u << 3,   // a gathered row's token outside [0, tokens)
 };
 
 typedef __nv_bfloat16 bf16;

@@ -102,6 +102,7 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(GemmArgs a) {
   __shared__ __align__(16) float As[kBK][BM + 4];
   __shared__ __align__(16) float Bs[kBK][kBN + 4];
   __shared__ __align__(16) float Us[MODE == kSwiGLU ? kBK : 1][kBN + 4];
+  __shared__ int64_t s_src[BM];   // source row of each tile row, -1: zeros
 
   const int total = a.sched[a.G];
   const int j = blockIdx.x;
@@ -118,6 +119,19 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(GemmArgs a) {
   const T* B1 = MODE == kSwiGLU ? reinterpret_cast<const T*>(a.B1) + (int64_t)g * a.bstride : nullptr;
 
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  for (int r = tid; r < BM; r += kThreads) {
+    const int64_t row = row0 + r;
+    int64_t src = -1;
+    if (row < gend) {
+      src = a.gather ? (int64_t)a.gather[row] : row;
+      if (a.gather && (src < 0 || src >= a.a_rows)) {
+        set_flag(a.flags, kFlagGather);
+        src = -1;
+      }
+    }
+    s_src[r] = src;
+  }
+  __syncthreads();
   float acc[TM][4], accu[MODE == kSwiGLU ? TM : 1][4];
 #pragma unroll
   for (int i = 0; i < TM; ++i)
@@ -135,8 +149,8 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(GemmArgs a) {
 #pragma unroll
     for (int q = 0; q < EA; ++q) {
       const int e = tid + q * kThreads, r = e / kBK, kk = e % kBK;
-      const int64_t row = row0 + r;
-      ra[q] = (row < gend && k0 + kk < K) ? to_f(A[row * K + k0 + kk]) : 0.f;
+      const int64_t src = s_src[r];
+      ra[q] = (src >= 0 && k0 + kk < K) ? to_f(A[src * K + k0 + kk]) : 0.f;
     }
 #pragma unroll
     for (int q = 0; q < EB; ++q) {
@@ -301,7 +315,21 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched,
   constexpr int V = 16 / sizeof(T);
   const int nv = K / V;
   const int c0 = (int)((int64_t)nv * sl / ks), c1 = (int)((int64_t)nv * (sl + 1) / ks);
-  const uint4* A = reinterpret_cast<const uint4*>(reinterpret_cast<const T*>(a.A) + row0 * K);
+  // row r of this tile reads A row arow[r] (gathered or contiguous); -1: zeros
+  int64_t arow[kSkR];
+#pragma unroll
+  for (int r = 0; r < kSkR; ++r) {
+    int64_t src = r < nrows ? row0 + r : -1;
+    if (src >= 0 && a.gather) {
+      src = a.gather[src];
+      if (src < 0 || src >= a.a_rows) {
+        if (threadIdx.x == 0) set_flag(a.flags, kFlagGather);
+        src = -1;
+      }
+    }
+    arow[r] = src;
+  }
+  const uint4* A = reinterpret_cast<const uint4*>(a.A);
   const T* B0 = reinterpret_cast<const T*>(a.B0) + (int64_t)g * a.bstride;
   const T* B1 = MODE == kSwiGLU ? reinterpret_cast<const T*>(a.B1) + (int64_t)g * a.bstride
                                 : nullptr;
@@ -332,9 +360,9 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched,
       }
 #pragma unroll
       for (int r = 0; r < kSkR; ++r) {
-        if (r < nrows) {
+        if (arow[r] >= 0) {
           float xa[V];
-          unpack16(__ldg(A + (int64_t)r * nv + c), xa, (const T*)nullptr);
+          unpack16(__ldg(A + arow[r] * nv + c), xa, (const T*)nullptr);
 #pragma unroll
           for (int q = 0; q < kSkC; ++q)
 #pragma unroll

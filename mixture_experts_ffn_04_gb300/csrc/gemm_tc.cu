@@ -5,10 +5,15 @@
 // m-tile schedule comes from the real group sizes, never from the token count).
 //
 // Design (one CTA per SM, persistent over a device-built tile list):
-//   warp 0     TMA producer: A tile [128 rows x 64 k] from the grouped
-//              activations (2-D tensor map), B tile [256 rows x 64 k] from the
-//              expert-major weights (3-D tensor map {k, n, expert}); both in
-//              the 128-byte swizzled K-major layout the MMA reads directly.
+//   warp 0     A producer: tile [128 rows x 64 k] of the grouped activations,
+//              by TMA (2-D tensor map); or, when the rows are gathered from
+//              the token matrix through a row -> token table, warps 0, 7, 8
+//              and 9, one per ring slot, with 16-byte cp.async copies written
+//              straight into the swizzled layout (so the grouped copy of x
+//              never exists);
+//   warp 6     B producer: TMA tile [256 rows x 64 k] of the expert-major
+//              weights (3-D tensor map {k, n, expert}); both tiles in the
+//              128-byte swizzled K-major layout the MMA reads directly.
 //   warp 1     TMEM owner and MMA issuer: one thread issues
 //              tcgen05.mma.cta_group::1.kind::f16 (M=128, N=256, K=16, bf16 in,
 //              fp32 accumulate in TMEM), 4 per 64-wide k-block, and commits to
@@ -43,17 +48,19 @@ constexpr int SA = 4, SB = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int RING_BYTES = SA * A_BYTES + SB * B_BYTES;
-// warps: 0 A producer, 1 MMA issuer, 2-5 epilogue, 6 B producer
-constexpr int THREADS = 224;
+// warps: 0 A producer, 1 MMA issuer, 2-5 epilogue, 6 B producer, 7-9 the other
+// three A producers when the A rows are gathered (one warp per ring slot)
+constexpr int THREADS = 320;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
 constexpr int MAX_SMEM_G = 1024;   // larger group counts use a schedule kernel
 constexpr int SCHED_BYTES = (MAX_SMEM_G + 1) * 4;
+constexpr int GATHER_BYTES = SA * BM * 4;   // per gathering warp: source token of each tile row
 // epilogue staging: per epilogue warp 32 rows x (64 B + 16 B pad)
 constexpr int OUT_ROW_BYTES = 80;
 constexpr int OUT_WARP_BYTES = 32 * OUT_ROW_BYTES;
 constexpr int OUT_BYTES = 4 * OUT_WARP_BYTES;
-constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES + OUT_BYTES + SCHED_BYTES;
+constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES + OUT_BYTES + SCHED_BYTES + GATHER_BYTES;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 // kind::f16 instruction descriptor: D fp32 (bits 4-5 = 1), A bf16 (7-9 = 1),
 // B bf16 (10-12 = 1), both K-major (15, 16 = 0), N >> 3 at 17-22, M >> 4 at 24-28.
@@ -72,6 +79,9 @@ struct TcArgs {
   uint32_t* flags;
   int ksplit;             // >1 only for fp32 outputs: partial sums per K range
   int64_t split_stride;   // floats between partial outputs
+  const bf16* gA;         // gathered A: row r of the operand is gA[gather[r]]
+  const int32_t* gather;  // or NULL: A through the tensor map
+  int64_t a_rows;         // rows of gA (bound on gather values)
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -134,6 +144,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
 }
+
+// 16-byte copy global -> shared; src_bytes 0 writes zeros without reading.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+static_assert(SA == 4, "one gathering warp per A ring slot: warps 0, 7, 8, 9");
 
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -262,6 +280,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   unsigned char* s_out = smem + RING_BYTES + BAR_BYTES;
   int32_t* s_sched = reinterpret_cast<int32_t*>(s_out + OUT_BYTES);
+  int32_t* s_rows = s_sched + (MAX_SMEM_G + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t smem_base = smem_u32(smem);
@@ -276,7 +295,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < SA; ++s) {
-      mbar_init(fullA(s), 1);
+      mbar_init(fullA(s), a.gather ? 32 : 1);   // gathered: one arrival per lane
       mbar_init(emptyA(s), 1);
     }
     for (int s = 0; s < SB; ++s) {
@@ -305,7 +324,67 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   const int64_t total = (int64_t)sched[a.G] * a.NT * a.ksplit;
 
-  if ((warp == 0 || warp == 6) && lane == 0) {
+  if (a.gather != nullptr && (warp == 0 || warp >= 7)) {
+    // ---------------- A ring by row gather (warps 0, 7, 8, 9) ----------------
+    // The warp of slot `slot` fills every SA-th stage.  Lane l copies 16-byte
+    // chunk (l & 7) of rows (l >> 3) + 4 i of the tile to its place in the
+    // 128-byte swizzle (chunk c of row r at c ^ (r & 7)).  cp.async writes are
+    // generic-proxy stores: each lane waits for its own copies, fences them
+    // against the async proxy the MMA reads through, and arrives (32
+    // arrivals a phase).  While one warp waits for its stage to land, the
+    // other slots' warps keep copies in flight.
+    const int slot = warp == 0 ? 0 : warp - 6;
+    int32_t* rows = s_rows + slot * BM;
+    const int ck = lane & 7, rl = lane >> 3;
+    uint32_t use = 0;   // fills of this slot so far (phase = use & 1)
+    int64_t n = 0;      // stage number in the MMA's order
+    bool ok = true, bad = false;
+    for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      int ks, g, mt, nt;
+      decode_tile(a, sched, tile, ks, g, mt, nt);
+      const int kb0 = ks * a.KB / a.ksplit, kb1 = (ks + 1) * a.KB / a.ksplit;
+      const int64_t first = n;
+      n += kb1 - kb0;
+      // this slot's first k-block of the tile, if any
+      int kb = kb0 + (int)((slot - first % SA + SA) % SA);
+      if (kb >= kb1) continue;
+      const int64_t gbeg = a.offsets ? a.offsets[g] : 0;
+      const int64_t gend = a.offsets ? a.offsets[g + 1] : a.single_rows;
+      const int64_t tr0 = gbeg + (int64_t)mt * BM;
+      __syncwarp();   // the previous tile's table is no longer read
+      for (int i = lane; i < BM; i += 32) {
+        int32_t src = -1;   // rows past the group are zero-filled
+        if (tr0 + i < gend) {
+          src = a.gather[tr0 + i];
+          if (src < 0 || src >= a.a_rows) { bad = true; src = -1; }
+        }
+        rows[i] = src;
+      }
+      __syncwarp();
+      for (; kb < kb1; kb += SA) {
+        int w = 0;
+        if (lane == 0) w = mbar_wait(emptyA(slot), (use & 1u) ^ 1u, abort_flag) ? 1 : 0;
+        if (!__shfl_sync(0xffffffffu, w, 0)) { ok = false; break; }
+        const uint32_t dst0 = ringA + slot * A_BYTES;
+        const int k0 = kb * BK + ck * 8;
+        const bool kin = k0 < a.K;
+#pragma unroll 8
+        for (int i = 0; i < BM / 4; ++i) {
+          const int r = rl + 4 * i;
+          const int32_t src = rows[r];
+          const bool in = kin && src >= 0;
+          const bf16* p = a.gA + (in ? (int64_t)src * a.K + k0 : 0);
+          cp_async16(dst0 + r * 128 + ((ck ^ (r & 7)) << 4), p, in ? 16u : 0u);
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        mbar_arrive(fullA(slot));
+        ++use;
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");   // no copy outlives the CTA
+    if (bad) set_flag(a.flags, kFlagGather);
+  } else if ((warp == 0 || warp == 6) && lane == 0) {
     // ---------------- TMA producers: warp 0 the A ring, warp 6 the B ring ----
     const bool is_a = warp == 0;
     const int S = is_a ? SA : SB;
@@ -587,7 +666,12 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   if (rows <= 0) return cudaSuccess;
   const int brows = a.mode == kSwiGLU ? BN / 2 : BN;
   CUtensorMap mA, mB0, mB1;
-  if (!make_map_2d(&mA, a.A, rows, a.K, BM)) return cudaErrorInvalidValue;
+  if (a.gather) {
+    // the A map is unused; any valid map will do
+    if (!make_map_2d(&mA, a.A, a.a_rows > 0 ? a.a_rows : 1, a.K, BM)) return cudaErrorInvalidValue;
+  } else if (!make_map_2d(&mA, a.A, rows, a.K, BM)) {
+    return cudaErrorInvalidValue;
+  }
   if (!make_map_3d(&mB0, a.B0, a.N, a.K, a.G, a.bstride, brows)) return cudaErrorInvalidValue;
   if (a.mode == kSwiGLU) {
     if (!make_map_3d(&mB1, a.B1, a.N, a.K, a.G, a.bstride, brows)) return cudaErrorInvalidValue;
@@ -610,6 +694,9 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   t.out = a.out;
   t.ldo = a.ldo;
   t.flags = a.flags;
+  t.gA = reinterpret_cast<const bf16*>(a.A);
+  t.gather = a.gather;
+  t.a_rows = a.a_rows;
   int64_t mt_bound = a.offsets ? (a.rows_bound + BM - 1) / BM + a.G : (a.single_rows + BM - 1) / BM;
   if (a.offsets && mt_bound > a.rows_bound) mt_bound = a.rows_bound;  // >= 1 row per tile
   const int64_t tiles_bound = mt_bound * t.NT * t.ksplit;

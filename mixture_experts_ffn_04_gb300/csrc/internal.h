@@ -27,8 +27,7 @@ moe_status decode_shape(const moe_shape* s, Shape* out, const char** why);
 // Byte offsets of every region inside the workspace (all 256-byte aligned).
 struct Layout {
   // scratch
-  size_t flags, logits, hist, base, sched_routed, sched_shared, sched_router, tie_queue,
-      scratch_end;
+  size_t flags, logits, hist, base, sched_routed, sched_shared, sched_router, scratch_end;
   int nchunks, tokens_per_chunk;
   // layer-forward intermediates
   size_t topk_idx, topk_w, gate, counts, offsets, sidx, row_token, x_perm, h, y_perm, sh_h,
@@ -67,6 +66,8 @@ struct GemmArgs {
   uint32_t* flags;
   int ksplit = 1;          // kStoreF32 only: partial sums over K ranges,
   int64_t split_stride = 0;  // written split_stride floats apart
+  const int32_t* gather = nullptr;  // non-NULL: row r of the operand is A[gather[r]]
+  int64_t a_rows = 0;               // rows of A when gathered (bound on gather values)
 };
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t st);
@@ -76,11 +77,10 @@ cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_schedule(const GemmArgs& a, int bm, cudaStream_t st);
 
 // logits: nsplit partial sums of [T, ldl] floats, T * ldl apart.
-// queue: [T] int32 scratch, qcount: one uint32 (both in the workspace).
+// redecided: count of tokens whose near tie was re-decided exactly.
 cudaError_t launch_topk(const Shape& s, const float* logits, int nsplit, const void* x,
                         const void* w_router, int32_t* topk_idx, float* topk_w, float* gate,
-                        uint32_t* redecided, int32_t* queue, uint32_t* qcount,
-                        cudaStream_t st);
+                        uint32_t* redecided, cudaStream_t st);
 cudaError_t launch_sum_partials(const Shape& s, const float* logits, int nsplit, float* out,
                                 cudaStream_t st);
 

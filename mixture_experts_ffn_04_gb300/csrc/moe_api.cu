@@ -104,7 +104,6 @@ Layout layout_for(const Shape& s) {
   L.sched_routed = off; off += align256((E + 1) * 4);
   L.sched_shared = off; off += 256;
   L.sched_router = off; off += 256;
-  L.tie_queue = off; off += align256(T * 4);
   L.scratch_end = off;
   L.topk_idx = off; off += align256(T * k * 4);
   L.topk_w = off; off += align256(T * k * 4);
@@ -292,9 +291,7 @@ static moe_status do_route(const Shape& s, const Layout& L, char* w, const void*
   if (r != MOE_OK) return r;
   float* logits = reinterpret_cast<float*>(w + L.logits);
   uint32_t* stats = reinterpret_cast<uint32_t*>(w + L.flags) + 1;
-  uint32_t* qcount = reinterpret_cast<uint32_t*>(w + L.flags) + 2;
-  int32_t* queue = reinterpret_cast<int32_t*>(w + L.tie_queue);
-  CHECK_CUDA(launch_topk(s, logits, nsplit, x, router, idx, tw, gate, stats, queue, qcount, st));
+  CHECK_CUDA(launch_topk(s, logits, nsplit, x, router, idx, tw, gate, stats, st));
   return MOE_OK;
 }
 
@@ -323,8 +320,9 @@ moe_status moe_permute(const moe_shape* shape, const void* x, const int32_t* top
   reset_launch_count();
   DECODE(shape, s);
   if (!counts || !offsets) return fail(MOE_ERR_INVALID_ARG, "counts and offsets must be non-NULL");
-  if (s.T > 0 && (!x || !topk_idx || !scatter_index || !row_token || !x_perm))
-    return fail(MOE_ERR_INVALID_ARG, "x, topk_idx, scatter_index, row_token, x_perm must be non-NULL");
+  if (s.T > 0 && (!topk_idx || !scatter_index || !row_token))
+    return fail(MOE_ERR_INVALID_ARG, "topk_idx, scatter_index and row_token must be non-NULL");
+  if (s.T > 0 && x_perm && !x) return fail(MOE_ERR_INVALID_ARG, "x_perm needs x");
   if (!aligned16(x) || !aligned16(x_perm))
     return fail(MOE_ERR_INVALID_ARG, "x and x_perm must be 16-byte aligned");
   const Layout L = layout_for(s);
@@ -338,7 +336,7 @@ moe_status moe_permute(const moe_shape* shape, const void* x, const int32_t* top
 static moe_status grouped(int mode, const moe_shape* shape, const void* A, const void* B0,
                           const void* B1, int64_t stride, const int32_t* offsets, int32_t G,
                           int64_t rows_bound, int32_t inter, void* out, void* ws,
-                          size_t ws_bytes, void* stream) {
+                          size_t ws_bytes, void* stream, const int32_t* gather = nullptr) {
   reset_launch_count();
   DECODE(shape, s);
   if (G < 1 || (G > s.E && G != 1)) return fail(MOE_ERR_INVALID_ARG, "num_groups must be in [1, E]");
@@ -372,6 +370,8 @@ static moe_status grouped(int mode, const moe_shape* shape, const void* A, const
   a.ldo = a.N;
   a.sched = reinterpret_cast<int32_t*>(w + (G > 1 ? L.sched_routed : L.sched_shared));
   a.flags = reinterpret_cast<uint32_t*>(w + L.flags);
+  a.gather = gather;
+  a.a_rows = s.T;
   CHECK_CUDA(launch_grouped_gemm(a, (cudaStream_t)stream));
   return MOE_OK;
 }
@@ -382,6 +382,20 @@ moe_status moe_grouped_swiglu(const moe_shape* shape, const void* x_perm, const 
                               void* ws, size_t ws_bytes, void* stream) {
   return grouped(kSwiGLU, shape, x_perm, w_gate, w_up, expert_stride, offsets, num_groups,
                  rows_bound, inter, h, ws, ws_bytes, stream);
+}
+
+moe_status moe_grouped_swiglu_gather(const moe_shape* shape, const void* x,
+                                     const int32_t* row_token, const void* w_gate,
+                                     const void* w_up, int64_t expert_stride,
+                                     const int32_t* offsets, int32_t num_groups,
+                                     int64_t rows_bound, int32_t inter, void* h, void* ws,
+                                     size_t ws_bytes, void* stream) {
+  if (rows_bound > 0 && !row_token) {
+    reset_launch_count();
+    return fail(MOE_ERR_INVALID_ARG, "row_token must be non-NULL");
+  }
+  return grouped(kSwiGLU, shape, x, w_gate, w_up, expert_stride, offsets, num_groups,
+                 rows_bound, inter, h, ws, ws_bytes, stream, row_token);
 }
 
 moe_status moe_grouped_down(const moe_shape* shape, const void* h, const void* w_down,
@@ -480,6 +494,10 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
   void* h = w + L.h;
   void* y_perm = w + L.y_perm;
   STAGE_EVENT(MOE_STAGE_PERMUTE);
+  // The grouped copy x_perm is written once here and read by the gate/up GEMM
+  // through a TMA tensor map: at prefill sizes that is faster than gathering
+  // the rows inside the GEMM (moe_grouped_swiglu_gather), whose cp.async
+  // producers cannot keep the tensor cores fed.
   CHECK_CUDA(launch_permute(s, L, w, x, use_idx, counts, offsets, sidx, row_token, x_perm, st));
   STAGE_EVENT(MOE_STAGE_GATE_UP);
 
@@ -504,6 +522,7 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
   STAGE_EVENT(MOE_STAGE_DOWN);
   a.mode = kStoreAct;
   a.A = h;
+  a.gather = nullptr;
   a.B0 = W->down;
   a.B1 = nullptr;
   a.bstride = W->down_stride;
@@ -602,6 +621,7 @@ moe_status moe_get_device_status(void* ws, void* stream, uint32_t* bits) {
   if (v & kFlagRoute) return MOE_ERR_DEVICE_ROUTE;
   if (v & kFlagRows) return MOE_ERR_ROWS;
   if (v & kFlagTimeout) return MOE_ERR_TIMEOUT;
+  if (v & kFlagGather) return MOE_ERR_GATHER;
   return MOE_OK;
 }
 
@@ -615,6 +635,7 @@ const char* moe_status_string(moe_status st) {
     case MOE_ERR_DEVICE_ROUTE: return "MOE_ERR_DEVICE_ROUTE";
     case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
     case MOE_ERR_ROWS: return "MOE_ERR_ROWS";
+    case MOE_ERR_GATHER: return "MOE_ERR_GATHER";
   }
   return "MOE_ERR_UNKNOWN";
 }

@@ -195,6 +195,25 @@ __global__ void __launch_bounds__(256) scatter_copy_kernel(
   }
 }
 
+// 3'. scatter only (no grouped copy of x: the gate/up GEMM gathers its rows
+//     through row_token): one thread per (token, slot) pair.
+__global__ void __launch_bounds__(256) scatter_index_kernel(
+    const int32_t* __restrict__ idx, int64_t npairs, int k, int E, int tpc,
+    const int32_t* __restrict__ base, int32_t* __restrict__ scatter_index,
+    int32_t* __restrict__ row_token) {
+  for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < npairs;
+       p += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = p / k;
+    const int r = scatter_index[p];
+    int d = -1;
+    if (r >= 0) {
+      d = base[(t / tpc) * E + idx[p]] + r;
+      row_token[d] = (int32_t)t;
+    }
+    scatter_index[p] = d;
+  }
+}
+
 // All three steps in one block, for calls whose tokens fit one chunk
 // (decode-sized): warp 0 ranks the pairs, the expert counts are scanned in
 // shared memory, then every warp turns ranks into rows and copies its tokens.
@@ -263,6 +282,7 @@ __global__ void __launch_bounds__(256) permute_small_kernel(
     dst[p] = d;
   }
   __syncthreads();
+  if (x_perm == nullptr) return;   // routing arrays only
   constexpr int V = 16 / sizeof(T);
   const int nvec = H / V;
   for (int t = wid; t < T_; t += nw) {
@@ -340,6 +360,16 @@ cudaError_t launch_permute_scratch(const Shape& s, int nchunks, int tpc, int32_t
   count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (nchunks == 0) return cudaSuccess;
+  if (x_perm == nullptr) {
+    const int64_t np = s.T * s.k;
+    int64_t blocks = (np + 255) / 256;
+    const int64_t cap = (int64_t)sm_count_cached() * 16;
+    if (blocks > cap) blocks = cap;
+    scatter_index_kernel<<<(unsigned)blocks, 256, 0, st>>>(topk_idx, np, s.k, s.E, tpc, base,
+                                                            scatter_index, row_token);
+    count_launch();
+    return cudaGetLastError();
+  }
   const size_t csm = (size_t)8 * s.k * 4;
   int64_t blocks = (s.T + 7) / 8;
   const int64_t cap = (int64_t)sm_count_cached() * 8;

@@ -5,10 +5,12 @@
 // so this kernel takes any E <= 16383 and k <= 255 from the packed shape word.
 //
 //   selection  the k largest logits, equal values resolved to the lower
-//              expert index; slot s = (s+1)-th largest.  For k + 1 <= 32 one
-//              thread per token streams the E logits and keeps a sorted
-//              top-(k+1) list in registers; otherwise one warp per token runs
-//              k+1 rounds of a shuffle arg-max;
+//              expert index; slot s = (s+1)-th largest.  One warp per token:
+//              for k + 1 <= 32 and at most 512 router columns the logits sit
+//              in registers and each of the k+1 rounds is one warp
+//              max-reduction of order-preserving integer keys plus one
+//              min-reduction of the expert index; otherwise the rounds run
+//              over shared memory with a shuffle arg-max;
 //   weights    norm_topk: exp(l_s - l_max) / sum over the k selected;
 //              otherwise: exp(l_s - l_max) / sum over all E;
 //   gate       Qwen2-MoE shared gate sigmoid(z), z = logit column E
@@ -33,7 +35,6 @@ namespace {
 
 constexpr int kMaxRounds = 256;  // k <= 255 plus one round for the boundary
 constexpr int kMaxCand = 64;     // experts re-evaluated in a near tie
-
 struct TopkArgs {
   const float* logits;  // nsplit partial sums, split_stride floats apart
   int ldl;
@@ -48,8 +49,6 @@ struct TopkArgs {
   float* wout;
   float* gate;
   uint32_t* redecided;  // count of tokens whose order was re-decided exactly
-  int32_t* queue;       // tokens handed from the thread path to the warp path
-  uint32_t* qcount;
 };
 
 struct WarpSmem {
@@ -58,6 +57,7 @@ struct WarpSmem {
   int* sel_i;        // [kMaxRounds]
   float* sel_v;      // [kMaxRounds]
   int* cand_i;       // [kMaxCand]
+  float* cand_f;     // [kMaxCand] fp32 logits of the candidates
   float2* cand_v;    // [kMaxCand] exact values as (hi, lo) float pairs
 };
 
@@ -67,7 +67,7 @@ __host__ __device__ inline size_t warp_smem_bytes(int E) {
   b += (size_t)E * 4;                   // buf
   b += (size_t)((E + 31) / 32) * 4;     // taken
   b += (size_t)kMaxRounds * 8;          // sel_i + sel_v
-  b += (size_t)kMaxCand * 4;            // cand_i
+  b += (size_t)kMaxCand * 8;            // cand_i + cand_f
   return (b + 15) & ~(size_t)15;
 }
 
@@ -79,6 +79,7 @@ __device__ __forceinline__ WarpSmem warp_smem(unsigned char* base, int E) {
   sm.sel_i = reinterpret_cast<int*>(sm.taken + (E + 31) / 32);
   sm.sel_v = reinterpret_cast<float*>(sm.sel_i + kMaxRounds);
   sm.cand_i = reinterpret_cast<int*>(sm.sel_v + kMaxRounds);
+  sm.cand_f = reinterpret_cast<float*>(sm.cand_i + kMaxCand);
   return sm;
 }
 
@@ -164,79 +165,138 @@ __device__ __forceinline__ float tie_bound(const TopkArgs& a, float top, float b
   return a.tau_scale * (fabsf(top) + fabsf(boundary) + 1.0f);
 }
 
-// One token, one warp.  VPL > 0: register selection for E <= 32 * VPL and
-// k + 1 <= 32 (lane l holds logits l, l+32, ...); VPL == 0: any shape, over
-// shared memory.  Then the near-tie re-decision, the weights and the gate.
-template <typename T, int VPL>
+// Near-tie re-decision of one token, in three steps.  sm.buf holds the E
+// fp32 logits and sm.sel_i / sm.sel_v the fp32 order of the top R; vb is the
+// boundary value sel_v[R-1] and tau the tie bound.
+//
+// 1. tie_candidates (one warp): L = every expert within tau below vb (so all
+//    of the top R, plus the ones just under it) into sm.cand_i / sm.cand_v.
+//    Only members of L closer than tau to another member can swap places;
+//    they are marked for exact evaluation, the rest keep their fp32 value
+//    (every comparison they take part in is decided by a margin of at least
+//    tau).  Returns |L|; above kMaxCand the fp32 order stands.
+// 2. the marked members get their exact dot product (Dot2) into sm.cand_v;
+// 3. tie_reselect (one warp) redoes the R rounds among L on those keys: every
+//    expert outside L lies more than tau below the boundary, so the top R are
+//    all in L.  sel_v keeps the fp32 logits of the chosen experts.
+__device__ int tie_candidates(const TopkArgs& a, const WarpSmem& sm, int lane, float vb,
+                              float tau, unsigned long long& marked) {
+  const int E = a.E;
+  int nc = 0;
+  for (int e0 = 0; e0 < E; e0 += 32) {
+    int e = e0 + lane;
+    bool c = e < E && sm.buf[e] >= vb - tau;
+    unsigned msk = __ballot_sync(0xffffffffu, c);
+    int pos = nc + __popc(msk & ((1u << lane) - 1u));
+    if (c && pos < kMaxCand) sm.cand_i[pos] = e;
+    nc += __popc(msk);
+  }
+  __syncwarp();
+  marked = 0ull;
+  if (nc > kMaxCand) return nc;
+  for (int c = lane; c < nc; c += 32) {
+    const float vc = sm.buf[sm.cand_i[c]];
+    bool mk = false;
+    for (int o = 0; o < nc; ++o) mk |= (o != c) && fabsf(vc - sm.buf[sm.cand_i[o]]) < tau;
+    sm.cand_f[c] = vc;
+    sm.cand_v[c] = make_float2(vc, 0.f);
+    if (mk) marked |= 1ull << c;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) marked |= __shfl_xor_sync(0xffffffffu, marked, o);
+  __syncwarp();
+  return nc;
+}
+
+template <typename T>
+__device__ __forceinline__ void tie_exact(const TopkArgs& a, const WarpSmem& sm, int64_t t,
+                                          int c, int lane) {
+  const T* xr = reinterpret_cast<const T*>(a.x) + t * a.H;
+  const T* wr = reinterpret_cast<const T*>(a.w) + (int64_t)sm.cand_i[c] * a.H;
+  const float2 v = dot2<T>(xr, wr, a.H, lane);
+  if (lane == 0) sm.cand_v[c] = v;
+}
+
+__device__ void tie_reselect(const WarpSmem& sm, int lane, int R, int nc) {
+  unsigned long long used = 0ull;
+  for (int r = 0; r < R && r < nc; ++r) {
+    float2 bv2 = make_float2(-INFINITY, 0.f);
+    int bi2 = 0x7fffffff, bc = -1;
+    for (int c = lane; c < nc; c += 32) {
+      if (used & (1ull << c)) continue;
+      const float2 v = sm.cand_v[c];
+      const int e = sm.cand_i[c];
+      if (bc < 0 || better2(v, e, bv2, bi2)) { bv2 = v; bi2 = e; bc = c; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      float2 ov;
+      ov.x = __shfl_xor_sync(0xffffffffu, bv2.x, o);
+      ov.y = __shfl_xor_sync(0xffffffffu, bv2.y, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi2, o);
+      const int oc = __shfl_xor_sync(0xffffffffu, bc, o);
+      const bool take = oc >= 0 && (bc < 0 || better2(ov, oi, bv2, bi2));
+      if (take) { bv2 = ov; bi2 = oi; bc = oc; }
+    }
+    if (bc < 0) break;
+    used |= 1ull << bc;
+    if (lane == 0) {
+      sm.sel_i[r] = bi2;
+      sm.sel_v[r] = sm.cand_f[bc];
+    }
+    __syncwarp();
+  }
+}
+
+// All three steps by one warp.
+template <typename T>
+__device__ void redecide(const TopkArgs& a, const WarpSmem& sm, int64_t t, int lane, int R,
+                         float vb, float tau) {
+  unsigned long long marked;
+  const int nc = tie_candidates(a, sm, lane, vb, tau, marked);
+  if (nc > kMaxCand) return;
+  for (unsigned long long mm = marked; mm; mm &= mm - 1)
+    tie_exact<T>(a, sm, t, __ffsll((long long)mm) - 1, lane);
+  __syncwarp();
+  tie_reselect(sm, lane, R, nc);
+}
+
+// One token, one warp, any shape (k + 1 > 32 or more than 512 router
+// columns): selection rounds over shared memory, then the near-tie
+// re-decision, the weights and the gate.
+template <typename T>
 __device__ void warp_token(const TopkArgs& a, const WarpSmem& sm, int64_t t, int lane) {
   const int E = a.E, k = a.k;
   const int R = k < E ? k + 1 : k;
   const float* row = a.logits + t * a.ldl;
   float m = -INFINITY;
-  if constexpr (VPL > 0) {
-    float v[VPL];
+  for (int e = lane; e < E; e += 32) {
+    float v = row[e];
+    for (int sp = 1; sp < a.nsplit; ++sp) v += row[sp * a.split_stride + e];
+    sm.buf[e] = v;
+    m = fmaxf(m, v);
+  }
+  for (int w = lane; w < (E + 31) / 32; w += 32) sm.taken[w] = 0u;
 #pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      const int e = lane + 32 * j;
-      v[j] = -INFINITY;
-      if (e < E) {
-        float x = row[e];
-        for (int sp = 1; sp < a.nsplit; ++sp) x += row[sp * a.split_stride + e];
-        v[j] = x;
-        sm.buf[e] = x;
-        m = fmaxf(m, x);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    uint32_t taken = 0u;
-    for (int r = 0; r < R; ++r) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-#pragma unroll
-      for (int j = 0; j < VPL; ++j) {
-        const int e = lane + 32 * j;
-        const bool free = e < E && !(taken & (1u << j));
-        if (free && (bi == 0x7fffffff || better(v[j], e, bv, bi))) { bv = v[j]; bi = e; }
-      }
-      warp_argmax(bv, bi);
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == r) {
-        sm.sel_i[r] = bi;
-        sm.sel_v[r] = bv;
-      }
-    }
-    __syncwarp();
-  } else {
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  __syncwarp();
+  for (int r = 0; r < R; ++r) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
     for (int e = lane; e < E; e += 32) {
-      float v = row[e];
-      for (int sp = 1; sp < a.nsplit; ++sp) v += row[sp * a.split_stride + e];
-      sm.buf[e] = v;
-      m = fmaxf(m, v);
+      if (sm.taken[e >> 5] & (1u << (e & 31))) continue;
+      float v = sm.buf[e];
+      if (bi == 0x7fffffff || better(v, e, bv, bi)) { bv = v; bi = e; }
     }
-    for (int w = lane; w < (E + 31) / 32; w += 32) sm.taken[w] = 0u;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    warp_argmax(bv, bi);
+    if (lane == 0) {
+      sm.sel_i[r] = bi;
+      sm.sel_v[r] = bv;
+      sm.taken[bi >> 5] |= 1u << (bi & 31);
+    }
     __syncwarp();
-    for (int r = 0; r < R; ++r) {
-      float bv = -INFINITY;
-      int bi = 0x7fffffff;
-      for (int e = lane; e < E; e += 32) {
-        if (sm.taken[e >> 5] & (1u << (e & 31))) continue;
-        float v = sm.buf[e];
-        if (bi == 0x7fffffff || better(v, e, bv, bi)) { bv = v; bi = e; }
-      }
-      warp_argmax(bv, bi);
-      if (lane == 0) {
-        sm.sel_i[r] = bi;
-        sm.sel_v[r] = bv;
-        sm.taken[bi >> 5] |= 1u << (bi & 31);
-      }
-      __syncwarp();
-    }
   }
 
-  // ---- near-tie re-decision -------------------------------------------
   const float vb = sm.sel_v[R - 1];
   const float tau = tie_bound(a, sm.sel_v[0], vb);
   bool near = false;
@@ -244,77 +304,10 @@ __device__ void warp_token(const TopkArgs& a, const WarpSmem& sm, int64_t t, int
   near = __any_sync(0xffffffffu, near);
   if (near && a.x != nullptr) {
     if (lane == 0 && a.redecided) atomicAdd(a.redecided, 1u);
-    // L = every expert within tau below the boundary value (so all of the
-    // top R, plus the ones just under it).  Only members of L closer than tau
-    // to another member can swap places; they are re-evaluated exactly, the
-    // rest keep their fp32 value (every comparison they take part in is
-    // decided by a margin of at least tau).
-    int nc = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-      int e = e0 + lane;
-      bool c = e < E && sm.buf[e] >= vb - tau;
-      unsigned msk = __ballot_sync(0xffffffffu, c);
-      int pos = nc + __popc(msk & ((1u << lane) - 1u));
-      if (c && pos < kMaxCand) sm.cand_i[pos] = e;
-      nc += __popc(msk);
-    }
-    __syncwarp();
-    if (nc <= kMaxCand) {
-      unsigned long long marked = 0ull;
-      for (int c = lane; c < nc; c += 32) {
-        const float vc = sm.buf[sm.cand_i[c]];
-        bool mk = false;
-        for (int o = 0; o < nc; ++o)
-          mk |= (o != c) && fabsf(vc - sm.buf[sm.cand_i[o]]) < tau;
-        sm.cand_v[c] = make_float2(vc, 0.f);
-        if (mk) marked |= 1ull << c;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) marked |= __shfl_xor_sync(0xffffffffu, marked, o);
-      __syncwarp();
-      const T* xr = reinterpret_cast<const T*>(a.x) + t * a.H;
-      for (unsigned long long mm = marked; mm; mm &= mm - 1) {
-        const int c = __ffsll((long long)mm) - 1;
-        const T* wr = reinterpret_cast<const T*>(a.w) + (int64_t)sm.cand_i[c] * a.H;
-        const float2 v = dot2<T>(xr, wr, a.H, lane);
-        if (lane == 0) sm.cand_v[c] = v;
-      }
-      __syncwarp();
-      // Redo the R rounds among L on these keys (every expert outside L lies
-      // more than tau below the boundary, so the top R are all in L).
-      unsigned long long used = 0ull;
-      for (int r = 0; r < R && r < nc; ++r) {
-        float2 bv2 = make_float2(-INFINITY, 0.f);
-        int bi2 = 0x7fffffff, bc = -1;
-        for (int c = lane; c < nc; c += 32) {
-          if (used & (1ull << c)) continue;
-          const float2 v = sm.cand_v[c];
-          const int e = sm.cand_i[c];
-          if (bc < 0 || better2(v, e, bv2, bi2)) { bv2 = v; bi2 = e; bc = c; }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          float2 ov;
-          ov.x = __shfl_xor_sync(0xffffffffu, bv2.x, o);
-          ov.y = __shfl_xor_sync(0xffffffffu, bv2.y, o);
-          const int oi = __shfl_xor_sync(0xffffffffu, bi2, o);
-          const int oc = __shfl_xor_sync(0xffffffffu, bc, o);
-          const bool take = oc >= 0 && (bc < 0 || better2(ov, oi, bv2, bi2));
-          if (take) { bv2 = ov; bi2 = oi; bc = oc; }
-        }
-        if (bc < 0) break;
-        used |= 1ull << bc;
-        if (lane == 0) {
-          sm.sel_i[r] = bi2;
-          sm.sel_v[r] = sm.buf[bi2];
-        }
-        __syncwarp();
-      }
-    }
+    redecide<T>(a, sm, t, lane, R, vb, tau);
     __syncwarp();
   }
 
-  // ---- weights ------------------------------------------------------------
   float denom = 0.f;
   if (a.norm) {
     const float top = sm.sel_v[0];
@@ -337,281 +330,303 @@ __device__ void warp_token(const TopkArgs& a, const WarpSmem& sm, int64_t t, int
   __syncwarp();
 }
 
-// One warp per token (k + 1 > 32).
-template <typename T, int VPL>
+template <typename T>
 __global__ void __launch_bounds__(128) topk_warp_kernel(TopkArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const WarpSmem sm = warp_smem(smem_raw + warp_smem_bytes(a.E) * wid, a.E);
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + wid;
   if (t >= a.T) return;
-  warp_token<T, VPL>(a, sm, t, lane);
+  warp_token<T>(a, sm, t, lane);
 }
 
-// The tokens the group kernel queued (a near-tie), one block of 4 warps each:
-// the logits go to shared memory, warp 0 finds the fp32 top-(k+1) boundary,
-// the candidates within the tie bound of it are collected and the ones close
-// to another candidate get their exact dot product (one warp per candidate),
-// then one thread orders the candidates by (exact value desc, index asc).
-// Only called for E <= 512 and k + 1 <= 32.
+// Order-preserving key of a logit: the unsigned order of keys is the numeric
+// order of the values.  -0 is folded into +0 first so that equal values get
+// equal keys.  Key 0 (reached by one NaN bit pattern only) marks a slot that
+// is taken or outside [0, E).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  const uint32_t b = __float_as_uint(__fadd_rn(v, 0.0f));
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
+// Exact values of the marked candidates of a block's near-tie tokens.  Pair p
+// = (warp pw[p], candidate pc[p]) of that warp's token.  Warp q of the block
+// takes quarter q of the hidden dimension for every pair, two pairs at a
+// time, so each lane keeps 8 loads of 16 bytes in flight; per pair a lane
+// accumulates its products with TwoProduct / TwoSum into one (sum,
+// compensation) pair, the lanes are merged with TwoSum, and the quarter's
+// result goes to part[p][q].  The caller adds the four quarters in order.
+constexpr int kPairs = 2;   // pairs a warp evaluates side by side
+
 template <typename T>
-__global__ void __launch_bounds__(128) topk_refine_kernel(TopkArgs a) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  float2* cand_v = reinterpret_cast<float2*>(smem_raw);          // [kMaxCand]
-  int* cand_i = reinterpret_cast<int*>(cand_v + kMaxCand);        // [kMaxCand]
-  int* order = cand_i + kMaxCand;                                 // [kMaxCand]
-  float* buf = reinterpret_cast<float*>(order + kMaxCand);        // [E]
-  __shared__ float s_red[4];
-  __shared__ float s_top, s_vb, s_m;
-  __shared__ int s_nc;
-  __shared__ unsigned long long s_marked;
-  __shared__ int s_sel_i[32];
-  __shared__ float s_sel_v[32];
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int E = a.E, k = a.k;
-  const int R = k < E ? k + 1 : k;
-  const uint32_t n = *a.qcount;
-  for (uint32_t q = blockIdx.x; q < n; q += gridDim.x) {
-    const int64_t t = a.queue[q];
-    const float* row = a.logits + t * a.ldl;
-    float m = -INFINITY;
-    for (int e = tid; e < E; e += blockDim.x) {
-      float v = row[e];
-      for (int sp = 1; sp < a.nsplit; ++sp) v += row[sp * a.split_stride + e];
-      buf[e] = v;
-      m = fmaxf(m, v);
-    }
+__device__ void block_exact(const TopkArgs& a, const unsigned char* smem_raw, size_t per_warp,
+                            int np, const uint8_t* pw, const uint8_t* pc, float2 (*part)[4],
+                            int lane, int wid) {
+  constexpr int V = 16 / sizeof(T);
+  const int nv = a.H / V;   // 16-byte chunks in a row
+  const int c0 = (int)((int64_t)nv * wid / 4), c1 = (int)((int64_t)nv * (wid + 1) / 4);
+  const uint4* xb = reinterpret_cast<const uint4*>(a.x);
+  const uint4* wb = reinterpret_cast<const uint4*>(a.w);
+  for (int pb = 0; pb < np; pb += kPairs) {
+    const uint4* xr[kPairs];
+    const uint4* wr[kPairs];
+    bool on[kPairs];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    if (lane == 0) s_red[wid] = m;
-    if (tid == 0) s_marked = 0ull;
-    __syncthreads();
-    if (wid == 0) {
-      // fp32 selection rounds (E <= 512: 16 values a lane)
-      float v[16];
+    for (int b = 0; b < kPairs; ++b) {
+      const int p = pb + b;
+      on[b] = p < np;
+      const int w = on[b] ? pw[p] : 0;
+      const WarpSmem smw = warp_smem(const_cast<unsigned char*>(smem_raw) + per_warp * w, a.E);
+      const int e = on[b] ? smw.cand_i[pc[p]] : 0;
+      xr[b] = xb + ((int64_t)blockIdx.x * 4 + w) * nv;
+      wr[b] = wb + (int64_t)e * nv;
+    }
+    float P[kPairs], S[kPairs];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int e = lane + 32 * j;
-        v[j] = e < E ? buf[e] : -INFINITY;
-      }
-      uint32_t taken = 0u;
-      for (int r = 0; r < R; ++r) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
+    for (int b = 0; b < kPairs; ++b) P[b] = S[b] = 0.f;
+    for (int c = c0 + lane; c < c1; c += 64) {
+      const bool second = c + 32 < c1;
+      uint4 xv[kPairs][2], wv[kPairs][2];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int e = lane + 32 * j;
-          const bool free = e < E && !(taken & (1u << j));
-          if (free && (bi == 0x7fffffff || better(v[j], e, bv, bi))) { bv = v[j]; bi = e; }
-        }
-        warp_argmax(bv, bi);
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (lane == 0) {
-          s_sel_i[r] = bi;
-          s_sel_v[r] = bv;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) {
-        s_top = s_sel_v[0];
-        s_vb = s_sel_v[R - 1];
-        s_m = fmaxf(fmaxf(s_red[0], s_red[1]), fmaxf(s_red[2], s_red[3]));
-      }
-      __syncwarp();
-      const float tau = tie_bound(a, s_top, s_vb);
-      int nc = 0;
-      for (int e0 = 0; e0 < E; e0 += 32) {
-        const int e = e0 + lane;
-        const bool c = e < E && buf[e] >= s_vb - tau;
-        const unsigned msk = __ballot_sync(0xffffffffu, c);
-        const int pos = nc + __popc(msk & ((1u << lane) - 1u));
-        if (c && pos < kMaxCand) cand_i[pos] = e;
-        nc += __popc(msk);
-      }
-      if (lane == 0) s_nc = nc;
-    }
-    __syncthreads();
-    const float tau = tie_bound(a, s_top, s_vb);
-    const int nc = s_nc;
-    const bool exact = nc <= kMaxCand;
-    if (exact && tid < nc) {
-      const float vc = buf[cand_i[tid]];
-      bool mk = false;
-      for (int o = 0; o < nc; ++o) mk |= (o != tid) && fabsf(vc - buf[cand_i[o]]) < tau;
-      cand_v[tid] = make_float2(vc, 0.f);
-      if (mk) atomicOr(&s_marked, 1ull << tid);
-    }
-    __syncthreads();
-    if (exact) {
-      const T* xr = reinterpret_cast<const T*>(a.x) + t * a.H;
-      int i = 0;
-      for (unsigned long long mm = s_marked; mm; mm &= mm - 1, ++i) {
-        if ((i & 3) != wid) continue;
-        const int c = __ffsll((long long)mm) - 1;
-        const T* wr = reinterpret_cast<const T*>(a.w) + (int64_t)cand_i[c] * a.H;
-        const float2 v = dot2<T>(xr, wr, a.H, lane);
-        if (lane == 0) cand_v[c] = v;
-      }
-    }
-    __syncthreads();
-    if (tid == 0) {
-      if (a.redecided) atomicAdd(a.redecided, 1u);
-      if (exact) {
-        // insertion sort of the candidates by (value desc, index asc)
-        for (int c = 0; c < nc; ++c) {
-          int p = c;
-          while (p > 0 && better2(cand_v[c], cand_i[c], cand_v[order[p - 1]], cand_i[order[p - 1]])) {
-            order[p] = order[p - 1];
-            --p;
+      for (int b = 0; b < kPairs; ++b) {
+        if (on[b]) {
+          xv[b][0] = __ldg(xr[b] + c);
+          wv[b][0] = __ldg(wr[b] + c);
+          if (second) {
+            xv[b][1] = __ldg(xr[b] + c + 32);
+            wv[b][1] = __ldg(wr[b] + c + 32);
           }
-          order[p] = c;
         }
-        for (int r = 0; r < R && r < nc; ++r) {
-          s_sel_i[r] = cand_i[order[r]];
-          s_sel_v[r] = buf[cand_i[order[r]]];
+      }
+#pragma unroll
+      for (int b = 0; b < kPairs; ++b) {
+        if (!on[b]) continue;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          if (h == 1 && !second) break;
+          float xf[V], wf[V];
+          unpack16(xv[b][h], xf, (const T*)nullptr);
+          unpack16(wv[b][h], wf, (const T*)nullptr);
+#pragma unroll
+          for (int i = 0; i < V; ++i) {
+            float hp, r, q;
+            two_prod(xf[i], wf[i], hp, r);
+            two_sum(P[b], hp, P[b], q);
+            S[b] = __fadd_rn(S[b], __fadd_rn(q, r));
+          }
         }
       }
     }
-    __syncthreads();
-    // weights, as the other paths form them (fp32 logits)
-    const float ref = a.norm ? s_sel_v[0] : s_m;
-    float denom = 0.f;
-    if (a.norm) {
-      for (int r = tid; r < k; r += blockDim.x) denom += expf(s_sel_v[r] - ref);
-    } else {
-      for (int e = tid; e < E; e += blockDim.x) denom += expf(buf[e] - ref);
-    }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, o);
-    __syncthreads();
-    if (lane == 0) s_red[wid] = denom;
-    __syncthreads();
-    denom = s_red[0] + s_red[1] + s_red[2] + s_red[3];
-    for (int r = tid; r < k; r += blockDim.x) {
-      a.idx[t * k + r] = s_sel_i[r];
-      a.wout[t * k + r] = expf(s_sel_v[r] - ref) / denom;
+    for (int b = 0; b < kPairs; ++b) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float op = __shfl_xor_sync(0xffffffffu, P[b], o);
+        const float os = __shfl_xor_sync(0xffffffffu, S[b], o);
+        float q;
+        two_sum(P[b], op, P[b], q);
+        S[b] = __fadd_rn(__fadd_rn(S[b], os), q);
+      }
+      if (lane == 0 && on[b]) part[pb + b][wid] = make_float2(P[b], S[b]);
     }
-    if (a.gated && tid == 0) {
-      float z = row[E];
-      for (int sp = 1; sp < a.nsplit; ++sp) z += row[sp * a.split_stride + E];
-      a.gate[t] = 1.0f / (1.0f + expf(-z));
-    }
-    __syncthreads();
   }
 }
 
-// G lanes per token (G a power of two, G tokens' groups per warp), for
-// k + 1 <= 32 and E <= 16 G: lane gl of a group holds logits gl, gl+G, ... in
-// registers; each of the k+1 rounds is a register scan plus log2(G) shuffle
-// steps inside the group.  A token whose sorted top-(k+1) list has two
-// neighbours closer than the tie bound is appended to the queue and decided
-// again by topk_refine_kernel; the others get their weights and gate here.
-template <int G, int VPL>
-__global__ void __launch_bounds__(128) topk_group_kernel(TopkArgs a) {
-  constexpr int TPB = 128 / G;            // tokens per block
-  __shared__ float s_val[TPB][32];
-  __shared__ int s_idx[TPB][32];
-  const int gl = threadIdx.x % G, tb = threadIdx.x / G;
-  const int64_t t = (int64_t)blockIdx.x * TPB + tb;
+// One warp per token for k + 1 <= 32 and at most 128 J router columns.  Lane
+// l holds columns 128 j + 4 l + c (c < 4) of every chunk j < J, read as
+// 16-byte loads of each split-K partial sum and added in split order.  Round
+// r takes the largest remaining key (warp max-reduction) and the lowest
+// expert index that holds it (warp min-reduction); lane r keeps the r-th
+// choice.  Tokens whose top-R list has two neighbours closer than the tie
+// bound are re-decided in shared memory: the exact values of all marked
+// candidates of the block are computed by its four warps together
+// (block_exact), then each such token redoes its rounds on them.
+template <typename T, int J>
+__global__ void __launch_bounds__(128, 6) topk_fast_kernel(TopkArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ unsigned long long s_marked[4];
+  __shared__ uint8_t s_pw[4 * kMaxCand], s_pc[4 * kMaxCand];
+  __shared__ float2 s_part[4 * kMaxCand][4];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int64_t t = (int64_t)blockIdx.x * 4 + wid;
   const bool live = t < a.T;
   const int E = a.E, k = a.k;
   const int R = k < E ? k + 1 : k;
   const float* row = a.logits + (live ? t : 0) * a.ldl;
-  float v[VPL];
-  float m = -INFINITY;
+  float v[J][4];
 #pragma unroll
-  for (int j = 0; j < VPL; ++j) {
-    const int e = gl + G * j;
-    float x = -INFINITY;
-    if (live && e < E) {
-      x = row[e];
-#pragma unroll 4
-      for (int sp = 1; sp < a.nsplit; ++sp) x += row[sp * a.split_stride + e];
+  for (int sp = 0; sp < kMaxSplit; ++sp) {
+    if (sp < a.nsplit) {
+      const float* src = row + sp * a.split_stride;
+#pragma unroll
+      for (int j = 0; j < J; ++j) {
+        const int e0 = 128 * j + 4 * lane;
+        float4 q = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live && e0 < a.ldl) q = __ldg(reinterpret_cast<const float4*>(src + e0));
+        if (sp == 0) {
+          v[j][0] = q.x; v[j][1] = q.y; v[j][2] = q.z; v[j][3] = q.w;
+        } else {
+          v[j][0] += q.x; v[j][1] += q.y; v[j][2] += q.z; v[j][3] += q.w;
+        }
+      }
     }
-    v[j] = x;
-    m = fmaxf(m, x);
   }
+  if (live && a.gated) {
+    // column E (the shared gate's logit) lies in one lane's registers
 #pragma unroll
-  for (int o = G / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  uint32_t taken = 0u;
+    for (int j = 0; j < J; ++j)
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (128 * j + 4 * lane + c == E) a.gate[t] = 1.0f / (1.0f + expf(-v[j][c]));
+  }
+  uint32_t key[J][4];
+#pragma unroll
+  for (int j = 0; j < J; ++j)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) key[j][c] = 128 * j + 4 * lane + c < E ? order_key(v[j][c]) : 0u;
+  float my_v = -INFINITY;
+  int my_i = 0x7fffffff;
   for (int r = 0; r < R; ++r) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
+    uint32_t lk = 0u;
+    int li = 0x7fffffff;
 #pragma unroll
-    for (int j = 0; j < VPL; ++j) {
-      const int e = gl + G * j;
-      const bool free = e < E && !(taken & (1u << j));
-      if (free && (bi == 0x7fffffff || better(v[j], e, bv, bi))) { bv = v[j]; bi = e; }
-    }
+    for (int j = 0; j < J; ++j)
 #pragma unroll
-    for (int o = G / 2; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-    }
-    if (bi != 0x7fffffff && bi % G == gl) taken |= 1u << (bi / G);
-    if (gl == 0) {
-      s_val[tb][r] = bv;
-      s_idx[tb][r] = bi;
+      for (int c = 0; c < 4; ++c)
+        if (key[j][c] > lk) { lk = key[j][c]; li = 128 * j + 4 * lane + c; }
+    const uint32_t mk = __reduce_max_sync(0xffffffffu, lk);
+    const int wi = (int)__reduce_min_sync(0xffffffffu, lk == mk ? (uint32_t)li : 0xffffffffu);
+#pragma unroll
+    for (int j = 0; j < J; ++j)
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (128 * j + 4 * lane + c == wi) key[j][c] = 0u;
+    if (lane == r) {
+      my_v = key_value(mk);
+      my_i = wi;
     }
   }
-  __syncwarp();
-  const float tau = tie_bound(a, s_val[tb][0], s_val[tb][R - 1]);
-  bool near = false;
-  for (int r = gl; r + 1 < R; r += G) near |= (s_val[tb][r] - s_val[tb][r + 1]) < tau;
+  const float m = __shfl_sync(0xffffffffu, my_v, 0);   // the largest fp32 logit
+  const float vb = __shfl_sync(0xffffffffu, my_v, R - 1);
+  const float tau = tie_bound(a, m, vb);
+  const float nxt = __shfl_down_sync(0xffffffffu, my_v, 1);
+  const bool near = live && a.x != nullptr &&
+                    __any_sync(0xffffffffu, lane + 1 < R && my_v - nxt < tau);
+  const size_t per_warp = warp_smem_bytes(E);
+  const WarpSmem sm = warp_smem(smem_raw + per_warp * wid, E);
+  int nc = 0;
+  unsigned long long marked = 0ull;
+  if (near) {
+    if (lane == 0 && a.redecided) atomicAdd(a.redecided, 1u);
 #pragma unroll
-  for (int o = G / 2; o > 0; o >>= 1) near |= __shfl_xor_sync(0xffffffffu, (int)near, o) != 0;
-  const bool queued = near && a.x != nullptr;
-  // lanes that finish the token here (whole groups: live and near are
-  // uniform within a group)
-  const unsigned gm = __ballot_sync(0xffffffffu, live && !queued);
+    for (int j = 0; j < J; ++j)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int e = 128 * j + 4 * lane + c;
+        if (e < E) sm.buf[e] = v[j][c];
+      }
+    if (lane < R) {
+      sm.sel_i[lane] = my_i;
+      sm.sel_v[lane] = my_v;
+    }
+    __syncwarp();
+    nc = tie_candidates(a, sm, lane, vb, tau, marked);
+  }
+  if (lane == 0) s_marked[wid] = marked;
+  if (__syncthreads_or(near)) {
+    // the block's pair list: warp 0's marked candidates, then warp 1's, ...
+    int base = 0, np = 0;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const int cnt = __popcll(s_marked[w]);
+      if (w < wid) base += cnt;
+      np += cnt;
+    }
+    for (int c = lane; c < kMaxCand; c += 32) {
+      if (marked & (1ull << c)) {
+        const int p = base + __popcll(marked & ((1ull << c) - 1ull));
+        s_pw[p] = (uint8_t)wid;
+        s_pc[p] = (uint8_t)c;
+      }
+    }
+    __syncthreads();
+    block_exact<T>(a, smem_raw, per_warp, np, s_pw, s_pc, s_part, lane, wid);
+    __syncthreads();
+    if (near && nc <= kMaxCand) {
+      for (int c = lane; c < nc; c += 32) {
+        if (marked & (1ull << c)) {
+          const int p = base + __popcll(marked & ((1ull << c) - 1ull));
+          float P = s_part[p][0].x, Sc = s_part[p][0].y;
+#pragma unroll
+          for (int q = 1; q < 4; ++q) {
+            float qq;
+            two_sum(P, s_part[p][q].x, P, qq);
+            Sc = __fadd_rn(__fadd_rn(Sc, s_part[p][q].y), qq);
+          }
+          float hi, lo;
+          two_sum(P, Sc, hi, lo);
+          sm.cand_v[c] = make_float2(hi, lo);
+        }
+      }
+      __syncwarp();
+      tie_reselect(sm, lane, R, nc);
+      __syncwarp();
+      if (lane < R) {
+        my_i = sm.sel_i[lane];
+        my_v = sm.sel_v[lane];
+      }
+    }
+  }
   if (!live) return;
-  if (queued) {
-    if (gl == 0) a.queue[atomicAdd(a.qcount, 1u)] = (int32_t)t;
-    return;
-  }
-  const float ref = a.norm ? s_val[tb][0] : m;
+  // weights: norm_topk over the k chosen (reference: the top chosen value),
+  // otherwise the full softmax (reference: the largest logit)
+  const float ref = a.norm ? __shfl_sync(0xffffffffu, my_v, 0) : m;
   float denom = 0.f;
   if (a.norm) {
-    for (int r = gl; r < k; r += G) denom += expf(s_val[tb][r] - ref);
+    if (lane < k) denom = expf(my_v - ref);
   } else {
 #pragma unroll
-    for (int j = 0; j < VPL; ++j)
-      if (gl + G * j < E) denom += expf(v[j] - ref);
+    for (int j = 0; j < J; ++j)
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        if (128 * j + 4 * lane + c < E) denom += expf(v[j][c] - ref);
   }
 #pragma unroll
-  for (int o = G / 2; o > 0; o >>= 1) denom += __shfl_xor_sync(gm, denom, o);
-  for (int r = gl; r < k; r += G) {
-    a.idx[t * k + r] = s_idx[tb][r];
-    a.wout[t * k + r] = expf(s_val[tb][r] - ref) / denom;
-  }
-  if (a.gated && gl == 0) {
-    float z = row[E];
-    for (int sp = 1; sp < a.nsplit; ++sp) z += row[sp * a.split_stride + E];
-    a.gate[t] = 1.0f / (1.0f + expf(-z));
+  for (int o = 16; o > 0; o >>= 1) denom += __shfl_xor_sync(0xffffffffu, denom, o);
+  if (lane < k) {
+    a.idx[t * k + lane] = my_i;
+    a.wout[t * k + lane] = expf(my_v - ref) / denom;
   }
 }
 
-template <typename T, int VPL>
-cudaError_t launch_warp_t(const TopkArgs& a, size_t smem, cudaStream_t st) {
+template <typename T>
+cudaError_t launch_warp(const TopkArgs& a, size_t smem, cudaStream_t st) {
   if (smem * 4 > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(topk_warp_kernel<T, VPL>,
+    cudaError_t e = cudaFuncSetAttribute(topk_warp_kernel<T>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)(smem * 4));
     if (e != cudaSuccess) return e;
   }
-  topk_warp_kernel<T, VPL><<<(unsigned)((a.T + 3) / 4), 128, smem * 4, st>>>(a);
+  topk_warp_kernel<T><<<(unsigned)((a.T + 3) / 4), 128, smem * 4, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename T, int J>
+cudaError_t launch_fast_t(const TopkArgs& a, size_t smem, cudaStream_t st) {
+  topk_fast_kernel<T, J><<<(unsigned)((a.T + 3) / 4), 128, smem * 4, st>>>(a);
   return cudaGetLastError();
 }
 
 template <typename T>
-cudaError_t launch_warp(const TopkArgs& a, int vpl, size_t smem, cudaStream_t st) {
-  switch (vpl) {
-    case 1: return launch_warp_t<T, 1>(a, smem, st);
-    case 2: return launch_warp_t<T, 2>(a, smem, st);
-    case 4: return launch_warp_t<T, 4>(a, smem, st);
-    case 8: return launch_warp_t<T, 8>(a, smem, st);
-    default: return launch_warp_t<T, 0>(a, smem, st);
+cudaError_t launch_fast(const TopkArgs& a, int J, size_t smem, cudaStream_t st) {
+  switch (J) {
+    case 1: return launch_fast_t<T, 1>(a, smem, st);
+    case 2: return launch_fast_t<T, 2>(a, smem, st);
+    case 3: return launch_fast_t<T, 3>(a, smem, st);
+    default: return launch_fast_t<T, 4>(a, smem, st);
   }
 }
 
@@ -619,9 +634,9 @@ cudaError_t launch_warp(const TopkArgs& a, int vpl, size_t smem, cudaStream_t st
 
 cudaError_t launch_topk(const Shape& s, const float* logits, int nsplit, const void* x,
                         const void* w_router, int32_t* topk_idx, float* topk_w, float* gate,
-                        uint32_t* redecided, int32_t* queue, uint32_t* qcount,
-                        cudaStream_t st) {
+                        uint32_t* redecided, cudaStream_t st) {
   if (s.T == 0) return cudaSuccess;
+  if (nsplit < 1 || nsplit > kMaxSplit) return cudaErrorInvalidValue;
   TopkArgs a;
   a.logits = logits;
   a.ldl = s.ldl;
@@ -642,43 +657,20 @@ cudaError_t launch_topk(const Shape& s, const float* logits, int nsplit, const v
   a.wout = topk_w;
   a.gate = gate;
   a.redecided = redecided;
-  a.queue = queue;
-  a.qcount = qcount;
   const int R = s.k < s.E ? s.k + 1 : s.k;
-  int vpl = 0;
-  if (R <= 32) vpl = s.E <= 32 ? 1 : s.E <= 64 ? 2 : s.E <= 128 ? 4 : s.E <= 256 ? 8 : 0;
   const size_t per_warp = warp_smem_bytes(s.E);
   cudaError_t e;
-  if (R > 32 || s.E > 512 || s.T <= 256) {   // warp per token; no queue for few tokens
-    e = s.dtype == MOE_F32 ? launch_warp<float>(a, vpl, per_warp, st)
-                           : launch_warp<bf16>(a, vpl, per_warp, st);
-    if (e != cudaSuccess) return e;
-    count_launch();
-    return cudaSuccess;
+  if (R <= 32 && s.ldl <= 512) {   // ldl: router columns rounded up to 4
+    const int J = (s.ldl + 127) / 128;
+    e = s.dtype == MOE_F32 ? launch_fast<float>(a, J, per_warp, st)
+                           : launch_fast<bf16>(a, J, per_warp, st);
+  } else {
+    e = s.dtype == MOE_F32 ? launch_warp<float>(a, per_warp, st)
+                           : launch_warp<bf16>(a, per_warp, st);
   }
-  e = cudaMemsetAsync(qcount, 0, sizeof(uint32_t), st);
   if (e != cudaSuccess) return e;
-  // lanes per token: the smallest power of two holding E in 16 per lane
-  int G = 1;
-  while (G < 32 && G * 16 < s.E) G *= 2;
-  const int tpb = 128 / G;
-  const unsigned blocks = (unsigned)((s.T + tpb - 1) / tpb);
-  switch (G) {
-    case 1: topk_group_kernel<1, 16><<<blocks, 128, 0, st>>>(a); break;
-    case 2: topk_group_kernel<2, 16><<<blocks, 128, 0, st>>>(a); break;
-    case 4: topk_group_kernel<4, 16><<<blocks, 128, 0, st>>>(a); break;
-    case 8: topk_group_kernel<8, 16><<<blocks, 128, 0, st>>>(a); break;
-    case 16: topk_group_kernel<16, 16><<<blocks, 128, 0, st>>>(a); break;
-    default: topk_group_kernel<32, 16><<<blocks, 128, 0, st>>>(a); break;
-  }
   count_launch();
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const size_t rsm = (size_t)kMaxCand * 16 + (size_t)s.E * 4;
-  const unsigned rblocks = (unsigned)(s.T < 1024 ? s.T : 1024);
-  if (s.dtype == MOE_F32) topk_refine_kernel<float><<<rblocks, 128, rsm, st>>>(a);
-  else topk_refine_kernel<bf16><<<rblocks, 128, rsm, st>>>(a);
-  count_launch();
-  return cudaGetLastError();
+  return cudaSuccess;
 }
 
 namespace {

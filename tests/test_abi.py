@@ -126,6 +126,6 @@ def test_workspace_layout_scales(m):
     from mixture_experts_ffn_04_gb300 import workloads as W
     s = m.shape_for(W.DEEPSEEK_V3)
     T, k, H, I = 8192, 8, 7168, 2048
-    inter = 2 * T * k * H * 2 + T * k * I * 2
+    inter = 2 * T * k * H * 2 + T * k * I * 2     # x_perm, y_perm and h
     assert inter <= m.moe_workspace_bytes(s) <= inter * 1.2
     assert m.moe_scratch_bytes(s) < 128 << 20   # split-K router partials dominate

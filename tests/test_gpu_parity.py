@@ -119,6 +119,86 @@ def test_step_api_matches_layer_and_merged_fc1():
     assert torch.equal(y, y_ref)
 
 
+@pytest.mark.parametrize("engine", [1, 2, 3])
+def test_gathered_rows_match_copied_rows(engine):
+    """moe_permute without x_perm writes the same routing arrays, and
+    moe_grouped_swiglu_gather on x + row_token gives h bit for bit equal to
+    moe_grouped_swiglu on the grouped copy, on every engine (ragged K: H is not
+    a multiple of 64; groups span several 128-row tiles)."""
+    wl = W.small(W.QWEN3_30B_A3B, T=333, H=328, I=136, E=12, k=4)
+    dev = to_dev(W.make_inputs(wl, seed=5, device="cpu"))
+    s = m.shape_for(wl)
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    ws = m.alloc_workspace(s, full=False)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    idx, tw = torch.empty(T, k, **i32), torch.empty(T, k, dtype=torch.float32, device="cuda")
+    m.moe_route(s, dev["x"], dev["w_router"], idx, tw, None, ws)
+    outs = []
+    for copy in (True, False):
+        counts, offsets = torch.full((E,), -7, **i32), torch.full((E + 1,), -7, **i32)
+        sidx, row_token = torch.full((T, k), -7, **i32), torch.full((T * k,), -7, **i32)
+        x_perm = torch.empty(T * k, H, dtype=torch.bfloat16, device="cuda") if copy else None
+        m.moe_permute(s, dev["x"] if copy else None, idx, counts, offsets, sidx, row_token,
+                      x_perm, ws)
+        h = torch.full((T * k, I), float("nan"), dtype=torch.bfloat16, device="cuda")
+        prev = m.moe_testing_set_gemm_engine(engine)
+        try:
+            if copy:
+                m.moe_grouped_swiglu(s, x_perm, dev["w_gate"], dev["w_up"], I * H, offsets, E,
+                                     T * k, I, h, ws)
+            else:
+                m.moe_grouped_swiglu_gather(s, dev["x"], row_token, dev["w_gate"], dev["w_up"],
+                                            I * H, offsets, E, T * k, I, h, ws)
+        finally:
+            m.moe_testing_set_gemm_engine(prev)
+        torch.cuda.synchronize()
+        assert m.moe_get_device_status(ws)[0] == m.MOE_OK
+        outs.append((counts, offsets, sidx, row_token, h))
+    for a, b in zip(*outs):
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b)
+    assert torch.isfinite(outs[1][4].float()).all()
+
+
+@pytest.mark.parametrize("engine", [1, 2, 3])
+def test_bad_gather_token_sets_device_flag(engine):
+    """A row_token entry outside [0, T) reads nothing, gives a zero row of h
+    and raises MOE_ERR_GATHER; the other rows are unaffected."""
+    wl = W.small(W.QWEN3_30B_A3B, T=150, H=256, I=128, E=8, k=2)
+    dev = to_dev(W.make_inputs(wl, seed=6, device="cpu"))
+    s = m.shape_for(wl)
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    ws = m.alloc_workspace(s, full=False)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    idx, tw = torch.empty(T, k, **i32), torch.empty(T, k, dtype=torch.float32, device="cuda")
+    m.moe_route(s, dev["x"], dev["w_router"], idx, tw, None, ws)
+    counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
+    sidx, row_token = torch.empty(T, k, **i32), torch.empty(T * k, **i32)
+    m.moe_permute(s, None, idx, counts, offsets, sidx, row_token, None, ws)
+    hs = []
+    prev = m.moe_testing_set_gemm_engine(engine)
+    try:
+        for bad in (False, True):
+            rt = row_token.clone()
+            if bad:
+                rt[5] = T + 7
+                rt[9] = -3
+            h = torch.full((T * k, I), float("nan"), dtype=torch.bfloat16, device="cuda")
+            m.moe_grouped_swiglu_gather(s, dev["x"], rt, dev["w_gate"], dev["w_up"], I * H,
+                                        offsets, E, T * k, I, h, ws)
+            st, bits = m.moe_get_device_status(ws)
+            assert (st, bits) == ((m.MOE_ERR_GATHER, 8) if bad else (m.MOE_OK, 0))
+            hs.append(h)
+    finally:
+        m.moe_testing_set_gemm_engine(prev)
+    good, bad = hs
+    assert torch.equal(bad[5].float(), torch.zeros(I, device="cuda"))
+    assert torch.equal(bad[9].float(), torch.zeros(I, device="cuda"))
+    keep = torch.ones(T * k, dtype=torch.bool, device="cuda")
+    keep[5] = keep[9] = False
+    assert torch.equal(good[keep].view(torch.int16), bad[keep].view(torch.int16))
+
+
 def test_bad_direct_route_sets_device_flag():
     wl = W.small(W.ADV_ZIPF, T=64, H=256, I=128, I_sh=256)
     dev = to_dev(W.make_inputs(wl, seed=0, device="cpu"))
