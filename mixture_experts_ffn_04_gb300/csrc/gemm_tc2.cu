@@ -1,0 +1,503 @@
+// gemm_tc2.cu -- grouped bf16 GEMM on pairs of SMs (tcgen05 cta_group::2).
+//
+// Same contract as the one-SM engine in gemm_tc.cu ("Fused MoE Kernel Notes",
+// group_gemm_same_nk: groups of rows with shared N and K, the m-tile schedule
+// built from the real group sizes).  The two CTAs of a cluster share one
+// 256 x 256 output tile: CTA r keeps rows 128r .. 128r+127 of the A tile and
+// rows (N) 128r .. 128r+127 of the B tile in its own shared memory, and the
+// even CTA's MMA thread issues tcgen05.mma.cta_group::2 (M = 256, N = 256,
+// K = 16), which reads both CTAs' operands and writes each CTA's 128 rows x
+// 256 columns of the fp32 accumulator into that CTA's TMEM.  Per SM a 64-wide
+// k-block then needs 32 KB of operands instead of the 48 KB of a one-SM
+// 128 x 256 tile, so six stages fit where four did and the loads in flight per
+// SM cover 50 % more latency.  For SwiGLU CTA 0 loads the 128 gate rows and
+// CTA 1 the 128 up rows of the n-tile, so accumulator columns 0-127 are gate
+// and 128-255 up in both CTAs, as in the one-SM engine.
+//
+// Roles, in each CTA of the pair:
+//   warp 0     TMA A producer (its 128 rows), warp 6 TMA B producer (its half);
+//              the loads of both CTAs complete on the even CTA's "full"
+//              barrier of the stage (cta_group::2 TMA), on which the even
+//              CTA's producers expect the pair's bytes;
+//   warp 1     TMEM allocation, collective over the pair; in the even CTA
+//              also the MMA issuer;
+//   warps 2-5  epilogue over the CTA's own TMEM lanes; they tell the even CTA
+//              that an accumulator is drained (remote arrive, 256 a phase).
+// The MMA completion (tcgen05.commit ... multicast) frees the stage in both
+// CTAs and marks the accumulator full in both.  Every wait is bounded as in
+// the one-SM engine; a CTA that gives up raises its abort flag, its partner's
+// waits run out in turn, and both meet at the closing cluster barrier before
+// TMEM is released.
+#include "common.cuh"
+#include "internal.h"
+#include "tcgen05.cuh"
+
+namespace moe {
+namespace tc2 {
+
+using namespace tc;
+
+constexpr int BMP = 256, BMC = 128;     // rows of a pair tile, of one CTA's half
+constexpr int BN = 256, BNC = 128, BK = 64;
+constexpr int S = 6;                    // stages
+constexpr int A_BYTES = BMC * BK * 2;   // 16 KB
+constexpr int B_BYTES = BNC * BK * 2;   // 16 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int RING_BYTES = S * STAGE_BYTES;
+constexpr int THREADS = 224;            // warps 0-6
+constexpr uint32_t TMEM_COLS = 512;     // two 256-column accumulators
+constexpr int BAR_BYTES = 256;
+constexpr int MAX_SMEM_G = 1024;
+constexpr int SCHED_BYTES = (MAX_SMEM_G + 1) * 4;
+constexpr int OUT_ROW_BYTES = 80;
+constexpr int OUT_WARP_BYTES = 32 * OUT_ROW_BYTES;
+constexpr int OUT_BYTES = 4 * OUT_WARP_BYTES;
+constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES + OUT_BYTES + SCHED_BYTES;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
+static_assert((2 * S + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+// kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major,
+// N >> 3 at bits 17-22, M >> 4 at bits 24-28 (M = 256 across the pair).
+constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
+                           ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BMP >> 4) << 24);
+
+struct Args {
+  int mode, N, K, G, NT, KB;
+  const int32_t* offsets;
+  int64_t single_rows;
+  int64_t rows_bound;
+  const int32_t* sched;   // global pair-tile prefix, or NULL: built in shared memory
+  void* out;
+  int64_t ldo;
+  uint32_t* flags;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The same shared-memory offset in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+// Cluster-scope test of a barrier phase (test_wait: never suspends the
+// thread).  Every wait of this kernel polls with it.
+__device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait (about 2 s of SM clocks, then the abort flag).
+__device__ __forceinline__ bool wait2(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_test_cluster(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_test_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      return false;
+    }
+  }
+}
+__device__ __forceinline__ void wait2_quiet(uint32_t bar, uint32_t parity) {
+  const long long t0 = clock64();
+  while (!mbar_test_cluster(bar, parity))
+    if (clock64() - t0 > kWaitCycles) return;
+}
+// TMA tile loads into this CTA's shared memory whose completion is counted
+// on a barrier of the even CTA (cta_group::2 form: the barrier may sit in
+// either CTA of the pair; `bar` is its cluster address).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0,
+                                                 int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int c0,
+                                                 int c1, int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_alloc2(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish2() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void mma2(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                     uint32_t accum) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
+      : "memory");
+}
+// Arrive (once) on the barrier at this offset in both CTAs of the pair when
+// every tcgen05 operation issued so far by this thread has completed.
+__device__ __forceinline__ void commit2_both(uint32_t bar) {
+  const uint16_t mask = 0x3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ void commit2_self(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+// Pair tile -> (group, pair m-tile, n-tile): n-tile major, pair m-tile minor
+// within a group.
+__device__ __forceinline__ void decode_tile(const Args& a, const int32_t* sched, int64_t tile,
+                                            int& g, int& mp, int& nt) {
+  int lo = 0, hi = a.G;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if ((int64_t)sched[mid] * a.NT <= tile) lo = mid; else hi = mid;
+  }
+  g = lo;
+  const int mtg = sched[g + 1] - sched[g];
+  const int64_t local = tile - (int64_t)sched[g] * a.NT;
+  nt = (int)(local / mtg);
+  mp = (int)(local % mtg);
+}
+
+// Prefix of ceil(rows_g / 256) over the groups (one warp, shared memory);
+// sched[G] = 0 when the offsets are inconsistent or exceed the row bound.
+__device__ void build_schedule(const Args& a, int32_t* sched, int lane) {
+  int carry = 0;
+  bool bad = false;
+  for (int base = 0; base < a.G; base += 32) {
+    const int g = base + lane;
+    int v = 0;
+    if (g < a.G) {
+      int64_t cnt = a.offsets ? (int64_t)a.offsets[g + 1] - a.offsets[g] : a.single_rows;
+      if (cnt < 0) { bad = true; cnt = 0; }
+      v = (int)((cnt + BMP - 1) / BMP);
+    }
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (g < a.G) sched[g] = carry + incl - v;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) {
+    if (a.offsets) bad |= a.offsets[0] != 0 || (int64_t)a.offsets[a.G] > a.rows_bound;
+    else bad |= a.single_rows > a.rows_bound || a.single_rows < 0;
+  }
+  bad = __any_sync(0xffffffffu, bad);
+  if (lane == 0) {
+    sched[a.G] = bad ? 0 : carry;
+    if (bad && blockIdx.x == 0) set_flag(a.flags, kFlagRows);
+  }
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                    const __grid_constant__ CUtensorMap tmB1, const Args a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem =
+      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
+  // bars: full[S] empty[S] tfull[2] tempty[2] final
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  unsigned char* s_out = smem + RING_BYTES + BAR_BYTES;
+  int32_t* s_sched = reinterpret_cast<int32_t*>(s_out + OUT_BYTES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const uint32_t ring = smem_u32(smem);
+  auto full = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty = [&](int s) { return smem_u32(&bars[S + s]); };
+  auto tfull = [&](int b) { return smem_u32(&bars[2 * S + b]); };
+  auto tempty = [&](int b) { return smem_u32(&bars[2 * S + 2 + b]); };
+  const uint32_t final_bar = smem_u32(&bars[2 * S + 4]);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full(s), 2);      // the even CTA's A and B producers (pair's bytes)
+      mbar_init(empty(s), 1);     // the pair's MMA commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull(b), 1);
+      mbar_init(tempty(b), 2 * 128);   // both CTAs' epilogue threads
+    }
+    mbar_init(final_bar, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 2 && a.sched == nullptr) build_schedule(a, s_sched, lane);
+  cluster_sync();   // barriers of both CTAs initialised before any remote arrive
+  if (warp == 1) {
+    tmem_alloc2(smem_u32(tmem_slot), TMEM_COLS);   // collective over the pair
+    tmem_relinquish2();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int32_t* sched = a.sched ? a.sched : s_sched;
+  const int64_t total = (int64_t)sched[a.G] * a.NT;
+  const int64_t cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+
+  if ((warp == 0 || warp == 6) && lane == 0) {
+    // ---------------- TMA producers ----------------
+    const bool is_a = warp == 0;
+    int s = 0;
+    uint32_t ph = 0, issued = 0, par = 0;
+    bool ok = true;
+    for (int64_t tile = cl; tile < total && ok; tile += ncl) {
+      int g, mp, nt;
+      decode_tile(a, sched, tile, g, mp, nt);
+      const int64_t gbase = a.offsets ? a.offsets[g] : 0;
+      const int arow = (int)(gbase + (int64_t)mp * BMP + (int64_t)rank * BMC);
+      const int brow = a.mode == kSwiGLU ? nt * BNC : nt * BN + (int)rank * BNC;
+      const CUtensorMap* bmap = (a.mode == kSwiGLU && rank == 1) ? &tmB1 : &tmB0;
+      for (int kb = 0; kb < a.KB; ++kb) {
+        if (!wait2(empty(s), ph ^ 1u, abort_flag)) { ok = false; break; }
+        const uint32_t st = ring + s * STAGE_BYTES;
+        // the even CTA's "full" barrier counts both CTAs' bytes; only the
+        // even CTA's producers arrive on it (with the pair's byte count)
+        const uint32_t fb = map_to_rank(full(s), 0);
+        if (leader) mbar_expect_tx(full(s), 2 * (is_a ? A_BYTES : B_BYTES));
+        if (is_a) tma_load_2d_pair(st, &tmA, kb * BK, arow, fb);
+        else tma_load_3d_pair(st + A_BYTES, bmap, kb * BK, brow, g, fb);
+        issued |= 1u << s;
+        par = (par & ~(1u << s)) | (ph << s);
+        if (++s == S) { s = 0; ph ^= 1u; }
+      }
+    }
+    if (*abort_flag && leader) {
+      // loads still in flight land before the pair goes away (the odd CTA's
+      // are counted on these barriers too; its own waits run out seconds
+      // after any load of its could have landed)
+      for (int i = 0; i < S; ++i)
+        if (issued & (1u << i)) wait2_quiet(full(i), (par >> i) & 1u);
+    }
+  } else if (warp == 1 && lane == 0 && leader) {
+    // ---------------- even CTA: MMA issuer for the pair ----------------
+    int s = 0, acc = 0;
+    uint32_t ph = 0, aph = 0;
+    bool ok = true;
+    for (int64_t tile = cl; tile < total && ok; tile += ncl) {
+      if (!wait2(tempty(acc), aph ^ 1u, abort_flag)) break;
+      tc_fence_after();
+      const uint32_t d = tmem_base + (uint32_t)acc * BN;
+      for (int kb = 0; kb < a.KB; ++kb) {
+        if (!wait2(full(s), ph, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t st = ring + s * STAGE_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk)
+          mma2(d, sw128_desc(st + kk * 32), sw128_desc(st + A_BYTES + kk * 32), IDESC,
+               (kb | kk) != 0 ? 1u : 0u);
+        commit2_both(empty(s));
+        if (++s == S) { s = 0; ph ^= 1u; }
+      }
+      if (!ok) break;
+      commit2_both(tfull(acc));
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
+    if (*abort_flag) {
+      commit2_self(final_bar);
+      wait2_quiet(final_bar, 0);
+    }
+  } else if (warp >= 2 && warp <= 5) {
+    // ---------------- epilogue (warps 2..5, both CTAs) ----------------
+    const int q = warp & 3;   // TMEM lanes 32q .. 32q+31 of this CTA
+    unsigned char* stage = s_out + (warp - 2) * OUT_WARP_BYTES;
+    unsigned char* my_row = stage + lane * OUT_ROW_BYTES;
+    int acc = 0;
+    uint32_t aph = 0;
+    for (int64_t tile = cl; tile < total; tile += ncl) {
+      int g, mp, nt;
+      decode_tile(a, sched, tile, g, mp, nt);
+      const int64_t gbeg = a.offsets ? a.offsets[g] : 0;
+      const int64_t gend = a.offsets ? a.offsets[g + 1] : a.single_rows;
+      const int64_t row0 = gbeg + (int64_t)mp * BMP + (int64_t)rank * BMC + q * 32;
+      const int64_t nvalid64 = gend - row0;
+      const int nvalid = nvalid64 < 0 ? 0 : (nvalid64 > 32 ? 32 : (int)nvalid64);
+      int okw = 0;   // one lane polls; the warp follows its result
+      if (lane == 0) okw = wait2(tfull(acc), aph, abort_flag) ? 1 : 0;
+      if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * BN;
+      const bool swiglu = a.mode == kSwiGLU;
+      const int n0 = swiglu ? nt * BNC : nt * BN;
+      const int ncols = swiglu ? BN / 2 : BN;
+      bf16* out = reinterpret_cast<bf16*>(a.out);
+#pragma unroll 1
+      for (int c = 0; c < ncols && n0 + c < a.N; c += 32) {
+        uint32_t gr[32];
+        uint4 packed[4];
+        tmem_ld32(taddr + c, gr);
+        if (swiglu) {
+          uint32_t ur[32];
+          tmem_ld32(taddr + BN / 2 + c, ur);
+          tmem_wait_ld();
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              f[e] = silu_fast(__uint_as_float(gr[v * 8 + e])) * __uint_as_float(ur[v * 8 + e]);
+            packed[v] = pack16(f, (const bf16*)nullptr);
+          }
+        } else {
+          tmem_wait_ld();
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(gr[v * 8 + e]);
+            packed[v] = pack16(f, (const bf16*)nullptr);
+          }
+        }
+#pragma unroll
+        for (int v = 0; v < 4; ++v) reinterpret_cast<uint4*>(my_row)[v] = packed[v];
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int p = lane + 32 * i;   // 128 pieces: 32 rows x 4 x 16 B
+          const int rr = p >> 2, pc = p & 3;
+          const int n = n0 + c + pc * 8;
+          if (rr < nvalid && n < a.N)
+            *reinterpret_cast<uint4*>(out + (row0 + rr) * a.ldo + n) =
+                *reinterpret_cast<const uint4*>(stage + rr * OUT_ROW_BYTES + pc * 16);
+        }
+        __syncwarp();
+      }
+      tc_fence_before();
+      mbar_arrive_cluster(map_to_rank(tempty(acc), 0));
+      acc ^= 1;
+      if (acc == 0) aph ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // no MMA, TMEM load or remote arrive of the pair in flight
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc2(tmem_base, TMEM_COLS);
+  }
+  if (threadIdx.x == 0 && *abort_flag) set_flag(a.flags, kFlagTimeout);
+}
+
+}  // namespace tc2
+
+cudaError_t launch_gemm_tc2(const GemmArgs& a, cudaStream_t st) {
+  using namespace tc2;
+  if (a.dtype != MOE_BF16 || a.mode == kStoreF32 || a.ksplit != 1 || a.gather)
+    return cudaErrorNotSupported;
+  if ((a.K % 8) != 0 || (a.N % 8) != 0 || a.K <= 0 || a.N <= 0) return cudaErrorInvalidValue;
+  cudaError_t e;
+  const bool smem_sched = a.G <= MAX_SMEM_G;
+  if (!smem_sched) {
+    e = launch_schedule(a, BMP, st);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t rows = a.offsets ? a.rows_bound : a.single_rows;
+  if (rows <= 0) return cudaSuccess;
+  CUtensorMap mA, mB0, mB1;
+  if (!tc::make_map_2d(&mA, a.A, rows, a.K, BMC)) return cudaErrorInvalidValue;
+  if (!tc::make_map_3d(&mB0, a.B0, a.N, a.K, a.G, a.bstride, BNC)) return cudaErrorInvalidValue;
+  if (a.mode == kSwiGLU) {
+    if (!tc::make_map_3d(&mB1, a.B1, a.N, a.K, a.G, a.bstride, BNC)) return cudaErrorInvalidValue;
+  } else {
+    mB1 = mB0;
+  }
+  Args t;
+  t.mode = a.mode;
+  t.N = a.N;
+  t.K = a.K;
+  t.G = a.G;
+  t.NT = a.mode == kSwiGLU ? (a.N + BNC - 1) / BNC : (a.N + BN - 1) / BN;
+  t.KB = (a.K + BK - 1) / BK;
+  t.offsets = a.offsets;
+  t.single_rows = a.single_rows;
+  t.rows_bound = a.rows_bound;
+  t.sched = smem_sched ? nullptr : a.sched;
+  t.out = a.out;
+  t.ldo = a.ldo;
+  t.flags = a.flags;
+  int64_t mt_bound = a.offsets ? (a.rows_bound + BMP - 1) / BMP + a.G : (a.single_rows + BMP - 1) / BMP;
+  if (a.offsets && mt_bound > a.rows_bound) mt_bound = a.rows_bound;
+  const int64_t tiles_bound = mt_bound * t.NT;
+
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // clusters that fit on the GPU at once (per device, queried once)
+  static int max_clusters[64] = {0};
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (max_clusters[dev] == 0) {
+    e = cudaFuncSetAttribute(tc2_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, (void*)tc2_gemm_kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    max_clusters[dev] = n > 0 ? n : -1;
+  }
+  if (max_clusters[dev] < 0) return cudaErrorNotSupported;
+  const int64_t ncl = tiles_bound < max_clusters[dev] ? tiles_bound : max_clusters[dev];
+  cfg.gridDim = dim3((unsigned)(2 * ncl));
+  e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel, mA, mB0, mB1, t);
+  if (e != cudaSuccess) return e;
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -73,6 +73,7 @@ struct GemmArgs {
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_simt(const GemmArgs& a, int bm, cudaStream_t st);
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st);
+cudaError_t launch_gemm_tc2(const GemmArgs& a, cudaStream_t st);   // SM pairs
 cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_schedule(const GemmArgs& a, int bm, cudaStream_t st);
 

@@ -126,13 +126,24 @@ Layout layout_for(const Shape& s) {
   return L;
 }
 
-// Engine for a grouped GEMM: 1 CUDA-core tiles, 2 tensor cores, 3 skinny.
+// Engine for a grouped GEMM: 1 CUDA-core tiles, 2 tensor cores, 3 skinny,
+// 4 tensor cores on SM pairs.
 static int engine_for(const GemmArgs& a) {
   const int ov = gemm_path_override();
   const int64_t rows = a.offsets ? a.rows_bound : a.single_rows;
   if (a.dtype == MOE_F32) return ov == 3 ? 3 : 1;
+  const bool pair_ok = a.mode != kStoreF32 && a.ksplit == 1 && a.gather == nullptr;
+  if (ov == 4) return pair_ok ? 4 : 2;
   if (ov >= 1 && ov <= 3) return ov;
-  return rows <= 4 ? 3 : 2;
+  if (rows <= 4) return 3;
+  // SM pairs halve the weight bytes each SM buffers (more loads in flight)
+  // but round every group up to 256 rows instead of 128: they pay off for one
+  // big group (the shared MLP) and for large routed groups.  Measured on the
+  // layer: DeepSeek-V3-shaped routed GEMMs (256 rows a group) 4-7 % slower on
+  // pairs, its shared MLP about a third faster; all-to-one and Zipf routing
+  // 9-11 % faster end to end.
+  if (pair_ok && rows >= 512 && (a.G == 1 || (a.offsets && rows / a.G >= 1024))) return 4;
+  return 2;
 }
 
 // K split of the shared MLP's down projection on the tensor cores: its N = H
@@ -161,6 +172,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t st) {
   switch (engine_for(a)) {
     case 1: return launch_gemm_simt(a, 64, st);
     case 2: return launch_gemm_tc(a, st);
+    case 4: return launch_gemm_tc2(a, st);
     default: return launch_gemm_skinny(a, st);
   }
 }
@@ -652,7 +664,7 @@ const char* moe_stage_name(int32_t stage) {
 int32_t moe_last_launch_count(void) { return tl_launches; }
 
 int32_t moe_testing_set_gemm_engine(int32_t engine) {
-  if (engine < 0 || engine > 3) engine = 0;
+  if (engine < 0 || engine > 4) engine = 0;
   return g_engine.exchange(engine);
 }
 

@@ -31,12 +31,12 @@ REDUCED = [
     W.small(W.QWEN3_30B_A3B, T=100, H=256, I=128, E=64, k=40),    # k+1 > 32: warp top-k
     W.small(W.QWEN3_30B_A3B, T=200, H=256, I=128, E=300, k=4),    # E > 256
 ]
-ENGINES = {0: "auto", 1: "cuda-core", 2: "tensor-core", 3: "skinny"}
+ENGINES = {0: "auto", 1: "cuda-core", 2: "tensor-core", 3: "skinny", 4: "tensor-core-pairs"}
 
 
 def _cases():
     for wl in REDUCED:
-        engines = [0, 3] if wl.dtype == "f32" else [0, 1, 2, 3]
+        engines = [0, 3] if wl.dtype == "f32" else [0, 1, 2, 3, 4]
         for e in engines:
             yield pytest.param(wl, e, id="%s-%s" % (wl.name, ENGINES[e]))
 
