@@ -39,13 +39,15 @@ METRIC = "MoE layer tokens/s and grouped-GEMM TFLOP/s (% bf16 peak) on 1 GB300"
 # source hashes to the recorded value.
 NCU_TRAFFIC = {
     # profiles/tc_gemm_qwen3-30b-a3b-shape-T4096.md
-    "qwen3-30b-a3b-shape-T4096": {"bytes": 987602944, "kernel_hash": "6e010bc3b40da70b"},
+    "qwen3-30b-a3b-shape-T4096": {"bytes": 988770816, "kernel_hash": "6ac50c5a9b200603"},
 }
 
 
 def _kernel_hash() -> str:
-    p = os.path.join(ROOT, "mixture_experts_ffn_04_gb300", "csrc", "gemm_tc.cu")
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for f in ("gemm_tc.cu", "tcgen05.cuh"):
+        h.update(open(os.path.join(ROOT, "mixture_experts_ffn_04_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def _peaks():
