@@ -288,30 +288,49 @@ def main():
         raise RuntimeError("device status %d (bits %#x) after warm-up" % (st, bits))
     launches_per_step = m.moe_last_launch_count()
 
-    # One step = [L2 flush, traced layer forward].  With --graph (default) the
-    # step is captured once as a CUDA graph and replayed, so the device never
-    # waits on host-side launch work; the kernels are the same.
-    graph = None
+    # A timed step = L2 flush (untimed), then moe_layer_forward between two
+    # CUDA events.  With --graph (default) the forward is captured once as a
+    # CUDA graph and replayed, so the device never waits on host-side launch
+    # work; the kernels are the same.  Stage times come from a second pass of
+    # the same steps through moe_layer_forward_traced (events between stages,
+    # which also separate the stages' launches).
+    graph = graph_traced = None
     if not args.no_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
+            m.moe_layer_forward(layer.shape, layer.weights, x, ridx, rw, y, layer.ws)
+        graph_traced = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_traced):
             flush.fill_(1)
             m.moe_layer_forward_traced(layer.shape, layer.weights, x, ridx, rw, y, layer.ws,
                                        evs)
         for _ in range(args.warmup):
+            flush.fill_(1)
             graph.replay()
+            graph_traced.replay()
         torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def one_step():
+        flush.fill_(1)
+        ev0.record(stream)
         if graph is not None:
             graph.replay()
+        else:
+            m.moe_layer_forward(layer.shape, layer.weights, x, ridx, rw, y, layer.ws, stream)
+        ev1.record(stream)
+        ev1.synchronize()
+        return ev0.elapsed_time(ev1)
+
+    def one_traced_step():
+        if graph_traced is not None:
+            graph_traced.replay()
         else:
             flush.fill_(1)
             m.moe_layer_forward_traced(layer.shape, layer.weights, x, ridx, rw, y, layer.ws,
                                        evs, stream)
         evs[nst].synchronize()
-        return ([evs[s].elapsed_time(evs[s + 1]) for s in range(nst)],
-                evs[0].elapsed_time(evs[nst]))
+        return [evs[s].elapsed_time(evs[s + 1]) for s in range(nst)]
 
     clocks = Clocks(local)
     if dist is not None:
@@ -320,11 +339,7 @@ def main():
     clocks.start()
     time.sleep(0.05)   # let the sampler start
     t_wall = time.perf_counter()
-    per_stage, step_ms = [], []
-    for i in range(args.steps):
-        ps, tot = one_step()
-        per_stage.append(ps)
-        step_ms.append(tot)
+    step_ms = [one_step() for _ in range(args.steps)]
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     if dist is not None:
@@ -334,6 +349,7 @@ def main():
     if st != m.MOE_OK:
         raise RuntimeError("device status %d (bits %#x) in the timed region" % (st, bits))
 
+    per_stage = [one_traced_step() for _ in range(args.steps)]
     stage_ms = [statistics.mean(p[s] for p in per_stage) for s in range(nst)]
     total_ms = max_over_ranks(sum(step_ms), dist)
     ms_per_step = total_ms / args.steps
