@@ -30,6 +30,7 @@ REDUCED = [
     W.small(W.ADV_ZIPF, T=300, H=512, I=256, I_sh=256),
     W.small(W.QWEN3_30B_A3B, T=100, H=256, I=128, E=64, k=40),    # k+1 > 32: warp top-k
     W.small(W.QWEN3_30B_A3B, T=200, H=256, I=128, E=300, k=4),    # E > 256
+    W.small(W.QWEN3_30B_A3B, T=600, H=256, I=128, E=2048, k=4),   # > 1024 groups, > 512 columns
 ]
 ENGINES = {0: "auto", 1: "cuda-core", 2: "tensor-core", 3: "skinny", 4: "tensor-core-pairs"}
 
@@ -212,7 +213,8 @@ def test_bad_direct_route_sets_device_flag():
     assert layer.device_status()[0] == m.MOE_OK  # read-and-clear
 
 
-def test_rows_beyond_bound_set_device_flag():
+@pytest.mark.parametrize("engine", [1, 2, 3, 4])
+def test_rows_beyond_bound_set_device_flag(engine):
     wl = W.small(W.QWEN3_30B_A3B, T=64, H=256, I=128, E=4, k=2)
     s = m.shape_for(wl)
     ws = m.alloc_workspace(s, full=False)
@@ -220,9 +222,50 @@ def test_rows_beyond_bound_set_device_flag():
     xp = torch.randn(128, 256, device="cuda").bfloat16()
     wg = torch.randn(4, 128, 256, device="cuda").bfloat16()
     h = torch.full((128, 128), 7.0, device="cuda").bfloat16()
-    m.moe_grouped_swiglu(s, xp, wg, wg, 128 * 256, offsets, 4, 100, 128, h, ws)
+    prev = m.moe_testing_set_gemm_engine(engine)
+    try:
+        m.moe_grouped_swiglu(s, xp, wg, wg, 128 * 256, offsets, 4, 100, 128, h, ws)
+    finally:
+        m.moe_testing_set_gemm_engine(prev)
     assert m.moe_get_device_status(ws)[0] == m.MOE_ERR_ROWS
     assert bool((h.float() == 7.0).all())  # nothing was computed
+
+
+@pytest.mark.parametrize("groups", [[1000], [300, 0, 513, 7, 256, 257]],
+                         ids=["one-group", "ragged-groups"])
+def test_sm_pair_engine_matches_one_sm_engine(groups):
+    """The SM-pair engine (256-row tiles over two CTAs) gives the one-SM
+    engine's h and y_perm bit for bit: the same fp32 sums in the same k order,
+    one rounding.  Ragged N and K (N = 200, K = 328), empty groups, groups of
+    one tile and of one row past a tile."""
+    G = len(groups)
+    rows = sum(groups)
+    H, I = 328, 200
+    wl = W.small(W.QWEN3_30B_A3B, T=rows, H=H, I=I, E=max(G, 2), k=1)
+    s = m.shape_for(wl)
+    ws = m.alloc_workspace(s, full=False)
+    g = torch.Generator(device="cuda").manual_seed(11)
+    offs = torch.tensor([0] + list(np.cumsum(groups)), dtype=torch.int32, device="cuda")
+    xp = torch.randn(rows, H, device="cuda", generator=g).bfloat16()
+    wg = (torch.randn(G, I, H, device="cuda", generator=g) * 0.05).bfloat16()
+    wu = (torch.randn(G, I, H, device="cuda", generator=g) * 0.05).bfloat16()
+    wd = (torch.randn(G, H, I, device="cuda", generator=g) * 0.05).bfloat16()
+    out = {}
+    for e in (2, 4):
+        h = torch.full((rows, I), float("nan"), device="cuda").bfloat16()
+        yp = torch.full((rows, H), float("nan"), device="cuda").bfloat16()
+        prev = m.moe_testing_set_gemm_engine(e)
+        try:
+            m.moe_grouped_swiglu(s, xp, wg, wu, I * H, offs, G, rows, I, h, ws)
+            m.moe_grouped_down(s, h, wd, H * I, offs, G, rows, I, yp, ws)
+        finally:
+            m.moe_testing_set_gemm_engine(prev)
+        torch.cuda.synchronize()
+        assert m.moe_get_device_status(ws)[0] == m.MOE_OK
+        assert torch.isfinite(yp.float()).all()
+        out[e] = (h, yp)
+    assert torch.equal(out[2][0].view(torch.int16), out[4][0].view(torch.int16))
+    assert torch.equal(out[2][1].view(torch.int16), out[4][1].view(torch.int16))
 
 
 def test_zero_tokens_is_a_no_op():
