@@ -39,14 +39,17 @@ METRIC = "MoE layer tokens/s and grouped-GEMM TFLOP/s (% bf16 peak) on 1 GB300"
 # source hashes to the recorded value.
 NCU_TRAFFIC = {
     # profiles/tc_gemm_qwen3-30b-a3b-shape-T4096.md
-    "qwen3-30b-a3b-shape-T4096": {"bytes": 988770816, "kernel_hash": "6ac50c5a9b200603"},
+    "qwen3-30b-a3b-shape-T4096": {"bytes": 988770816, "kernel_hash": "a6becc622b303cea"},
 }
 
 
 def _kernel_hash() -> str:
-    h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "tcgen05.cuh"):
-        h.update(open(os.path.join(ROOT, "mixture_experts_ffn_04_gb300", "csrc", f), "rb").read())
+    """Hash of the one-SM GEMM's device code: its PTX wrappers and the part of
+    gemm_tc.cu above the host-side launcher."""
+    d = os.path.join(ROOT, "mixture_experts_ffn_04_gb300", "csrc")
+    src = open(os.path.join(d, "gemm_tc.cu"), "rb").read()
+    h = hashlib.sha256(open(os.path.join(d, "tcgen05.cuh"), "rb").read())
+    h.update(src[:src.index(b"// host side")])
     return h.hexdigest()[:16]
 
 
@@ -228,7 +231,8 @@ def _config(wl, graph=None):
     return {"workload": wl.name, "cuda_graph": graph, "tokens": wl.T, "hidden": wl.H, "experts": wl.E,
             "top_k": wl.k, "moe_inter": wl.I, "shared_inter": wl.I_sh,
             "shared_gate": wl.shared_gate, "norm_topk": wl.norm_topk, "routing": wl.routing,
-            "l2": "flushed before every timed step (256 MiB device write)",
+            "l2": "flushed before every timed step (256 MiB device write); e2e steps "
+                  "unflushed, weights larger than L2",
             "description": wl.description}
 
 
@@ -356,28 +360,57 @@ def main():
     value = replica_throughput(world, wl.T, ms_per_step)
 
     # ---- end to end through the public API, host buffers -------------------
+    # Every step copies its tokens in from pinned host memory, runs
+    # moe_layer_forward on them and copies its output back, on three streams
+    # so that step i+1's upload and step i-1's download overlap step i's
+    # forward (double-buffered device and host tensors; the forwards run in
+    # order on one stream and share the workspace).  No L2 flush here: the
+    # expert weights are larger than L2.
     x_host = x.cpu().pin_memory()
-    y_host = torch.empty_like(x_host).pin_memory()
+    y_host = [torch.empty_like(x_host).pin_memory() for _ in range(2)]
     ridx_h = ridx.cpu().pin_memory() if ridx is not None else None
     rw_h = rw.cpu().pin_memory() if rw is not None else None
-    xd, yd = torch.empty_like(x), torch.empty_like(x)
-    rid = torch.empty_like(ridx) if ridx is not None else None
-    rwd = torch.empty_like(rw) if rw is not None else None
-    e2e_ms = []
-    for i in range(args.warmup + args.steps):
-        flush.fill_(1)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        xd.copy_(x_host, non_blocking=True)
-        if rid is not None:
-            rid.copy_(ridx_h, non_blocking=True)
-            rwd.copy_(rw_h, non_blocking=True)
-        layer.forward(xd, yd, rid, rwd)
-        y_host.copy_(yd, non_blocking=True)
-        e1.record(stream)
-        e1.synchronize()
-        if i >= args.warmup:
-            e2e_ms.append(e0.elapsed_time(e1))
+    xd = [torch.empty_like(x) for _ in range(2)]
+    yd = [torch.empty_like(x) for _ in range(2)]
+    rid = [torch.empty_like(ridx) for _ in range(2)] if ridx is not None else [None, None]
+    rwd = [torch.empty_like(rw) for _ in range(2)] if rw is not None else [None, None]
+    s_in, s_cmp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    for e in ev_cmp + ev_out:
+        e.record(stream)
+    torch.cuda.synchronize()
+
+    def e2e_steps(n):
+        for i in range(n):
+            b = i % 2
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_cmp[b])          # the forward that read xd[b] is done
+                xd[b].copy_(x_host, non_blocking=True)
+                if rid[b] is not None:
+                    rid[b].copy_(ridx_h, non_blocking=True)
+                    rwd[b].copy_(rw_h, non_blocking=True)
+                ev_in[b].record(s_in)
+            s_cmp.wait_event(ev_in[b])
+            s_cmp.wait_event(ev_out[b])             # yd[b]'s last download is done
+            layer.forward(xd[b], yd[b], rid[b], rwd[b], stream=s_cmp)
+            ev_cmp[b].record(s_cmp)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_cmp[b])
+                y_host[b].copy_(yd[b], non_blocking=True)
+                ev_out[b].record(s_out)
+
+    e2e_steps(args.warmup)
+    torch.cuda.synchronize()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(s_in)
+    e2e_steps(args.steps)
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(s_cmp)
+    e_end.record(s_out)
+    e_end.synchronize()
+    e2e_ms = [e_start.elapsed_time(e_end) / args.steps]
     h2d = x.numel() * x.element_size() + (0 if ridx is None else
                                             ridx.numel() * 4 + rw.numel() * 4)
     d2h = y.numel() * y.element_size()

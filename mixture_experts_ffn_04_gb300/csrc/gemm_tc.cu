@@ -572,11 +572,14 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   int64_t mt_bound = a.offsets ? (a.rows_bound + BM - 1) / BM + a.G : (a.single_rows + BM - 1) / BM;
   if (a.offsets && mt_bound > a.rows_bound) mt_bound = a.rows_bound;  // >= 1 row per tile
   const int64_t tiles_bound = mt_bound * t.NT * t.ksplit;
-  static bool attr_done = false;
-  if (!attr_done) {
+  static bool attr_done[64] = {false};   // the attribute is per device
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev]) {
     e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    attr_done[dev] = true;
   }
   const int grid = (int)(tiles_bound < sm_count() ? tiles_bound : sm_count());
   tc_gemm_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(mA, mB0, mB1, t);
