@@ -9,6 +9,7 @@ Value recipe (per workload):
   shared gate/up ~ N(0, 1/sqrt(H)); shared down ~ N(0, 1/sqrt(I_sh));
   router rows ~ N(0, router_std) (1/sqrt(H) when unset); the Qwen2-MoE-style
   shared-gate weight (router row E) ~ N(0, 1/sqrt(H)), so its logit is ~N(0, 1).
+  Input RMSNorm weight (workloads with input preparation) ~ 1 + N(0, 0.1^2).
   Direct routes: "all_to_e0" sends every slot to expert 0 with weight 1/k;
   "zipf" draws each slot independently with P(e) proportional to (e+1)^-s
   (duplicates allowed) and per-slot weights U(0,1) normalised to sum 1.
@@ -44,6 +45,9 @@ class Workload:
     routing: str = "router"      # "router", "all_to_e0" or "zipf"
     router_std: Optional[float] = None
     zipf_s: float = 1.2
+    input_norm: bool = False     # input RMSNorm before the router and experts
+    residual: bool = False       # y = x + MoE(x_norm)
+    norm_eps: float = 1e-6
     description: str = ""
 
     @property
@@ -106,6 +110,14 @@ ADV_ZIPF = _add(Workload(
     description="adversarial direct routes: Zipf(1.2) expert popularity, duplicates "
                 "allowed; H=4096, E=64, k=6, I=1408, shared width 2816"))
 _add(ADV_ZIPF.with_tokens(16384))
+GEMMA4_26B_A4B = _add(Workload(
+    "gemma4-26b-a4b-shape-T512", T=512, H=2816, E=128, k=8, I=704, norm_topk=False,
+    router_std=0.02, input_norm=True, residual=True,
+    description="Gemma-4-26B-A4B-shaped prefill with the sublayer's input preparation: "
+                "T=512 (also 4096), H=2816, E=128, k=8, I=704, no shared expert, input "
+                "RMSNorm (eps 1e-6) before routing and experts, residual added after "
+                "the combine, top-k of the full softmax"))
+_add(GEMMA4_26B_A4B.with_tokens(4096))
 
 
 def get(name: str) -> Workload:
@@ -171,7 +183,8 @@ def _routes(w: Workload, seed: int):
 def make_inputs(w: Workload, seed: int = 0, device="cpu", with_experts: bool = True):
     """All input tensors of one workload, drawn on ``device``.
 
-    Keys: x [T,H]; w_router [E(+1),H] or None; w_gate, w_up [E,I,H];
+    Keys: x [T,H]; norm_weight [H] or None; w_router [E(+1),H] or None;
+    w_gate, w_up [E,I,H];
     w_down [E,H,I]; sh_gate, sh_up [I_sh,H] and sh_down [H,I_sh] or None;
     routes_idx [T,k] int32 and routes_w [T,k] fp32 (direct routes) or None.
     """
@@ -179,6 +192,11 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu", with_experts: bool = T
     T, H, E, k, I, I_sh = w.T, w.H, w.E, w.k, w.I, w.I_sh
     d = {}
     d["x"] = _normal(seed, "x", (T, H), 1.0, dt, device)
+    if w.input_norm:
+        d["norm_weight"] = (_normal(seed, "norm_weight", (H,), 0.1, torch.float32, device)
+                            + 1.0).to(dt)
+    else:
+        d["norm_weight"] = None
     if w.routing == "router":
         std = w.router_std if w.router_std is not None else 1.0 / math.sqrt(H)
         wr = _normal(seed, "w_router", (E, H), std, dt, device)

@@ -21,6 +21,9 @@
  *  - "MoE: timing-replay harnesses, shared experts, parameterized V_TOPK
  *    routing", Part 2 (topk_softmax generic in (num_experts, top_k); a missing
  *    shape word is an error, never top_k = 0; SwiGLU = silu(g) * u).
+ *  - "MoE: shared experts, arbitrary V_TOPK expert shapes, and an enforced
+ *    stage-marker contract", Group E (residual_setup: the residual copy, the
+ *    input RMSNorm and its norm-weight multiply before the MoE FFN).
  *  - "Fused MoE Kernel Notes", Scatter/gather layout (scatter_index maps each
  *    (token, slot) into the expert-grouped [tokens*topk, hidden] buffer;
  *    gather sums the routed outputs back), Duplicate top-k routes (one expert
@@ -33,6 +36,8 @@
  *    norm_topk = 0 -> full softmax over all E logits, taken at the selected k.
  *  - rows inside an expert group are in row-major (token, slot) order.
  *  - silu(g) = g / (1 + exp(-g)); sigmoid gate = 1 / (1 + exp(-z)).
+ *  - input RMSNorm: x / sqrt(mean(x^2) + eps) * w, rounded once to the
+ *    activation type; the residual added after the combine is x itself.
  *  - weight shapes follow the [out, in] convention: router [E(+1), H],
  *    gate/up [E, I, H] (expert stride given), down [E, H, I], shared gate/up
  *    [I_sh, H], shared down [H, I_sh]; the shared-gate logit weight is row E
@@ -227,6 +232,80 @@ int32_t oracle_topk_softmax(int64_t n, uint32_t shape_word, int32_t norm_topk,
  * computes exactly this). */
 void oracle_sigmoid(int64_t n, const double *z, int64_t ld_z, double *gate) {
   for (int64_t t = 0; t < n; t++) gate[t] = 1.0 / (1.0 + exp(-z[t * ld_z]));
+}
+
+/* ---------------------------------------------------------------------------
+ * Rounding of a double to the activation type, round to nearest, ties to
+ * even: what the layer stores its activations in.  bf16 keeps 8 significant
+ * bits with fp32's exponent range; a value is written as its bf16 bit pattern
+ * (the top 16 bits of the fp32 with that value).  fp32 values are written as
+ * fp32 (C's double -> float conversion rounds to nearest even).
+ * ------------------------------------------------------------------------- */
+static void st_act(void *p, int dtype, int64_t i, double v) {
+  if (dtype != OR_BF16) {
+    ((float *)p)[i] = (float)v;
+    return;
+  }
+  double r;
+  if (isnan(v)) {
+    ((uint16_t *)p)[i] = 0x7FC0;   /* the canonical quiet NaN */
+    return;
+  } else if (v == 0.0 || isinf(v)) {
+    r = v;
+  } else {
+    const double a = fabs(v);
+    double q;   /* the spacing of bf16 values around a */
+    if (a < ldexp(1.0, -126)) {
+      q = ldexp(1.0, -133);   /* subnormal range: fixed spacing */
+    } else {
+      int e;
+      frexp(a, &e);           /* a = m 2^e, 0.5 <= m < 1 */
+      q = ldexp(1.0, e - 8);  /* 8 significant bits */
+    }
+    r = rint(a / q) * q;      /* rint: nearest, ties to even */
+    if (r > ldexp(255.0, 120)) r = INFINITY;   /* beyond the largest finite bf16 */
+    r = copysign(r, v);
+  }
+  const float f = (float)r;   /* exact: r has at most 8 significant bits */
+  uint32_t bits;
+  memcpy(&bits, &f, 4);
+  ((uint16_t *)p)[i] = (uint16_t)(bits >> 16);
+}
+
+/* One value, for tests of the rounding rule: the activation-type value
+ * nearest to v (ties to even), returned as a double. */
+double oracle_round_act(double v, int32_t dtype) {
+  if (dtype == OR_BF16) {
+    uint16_t b;
+    st_act(&b, OR_BF16, 0, v);
+    return ld(&b, OR_BF16, 0);
+  }
+  float f;
+  st_act(&f, OR_F32, 0, v);
+  return (double)f;
+}
+
+/* ---------------------------------------------------------------------------
+ * Input preparation of the MoE sublayer (Group E of the PLENA compiler page:
+ * the "residual_setup" stage -- residual copy, input RMSNorm and its
+ * norm-weight multiply; the residual itself is x):
+ *   x_norm[t, h] = x[t, h] / sqrt((1/H) sum_h' x[t, h']^2 + eps) * w[h]
+ * in double, then rounded once to the activation type (`out`, [T, H], same
+ * type as x).  The router and the experts then see exactly these values, as
+ * on the GPU, so both sides decide the routing on the same inputs.
+ * ------------------------------------------------------------------------- */
+void oracle_rmsnorm(int64_t T, int64_t H, const void *x, int32_t dtype, const void *w,
+                    double eps, void *out) {
+  for (int64_t t = 0; t < T; t++) {
+    double ss = 0.0;
+    for (int64_t h = 0; h < H; h++) {
+      const double v = ld(x, dtype, t * H + h);
+      ss += v * v;
+    }
+    const double inv = 1.0 / sqrt(ss / (double)H + eps);
+    for (int64_t h = 0; h < H; h++)
+      st_act(out, dtype, t * H + h, ld(x, dtype, t * H + h) * inv * ld(w, dtype, h));
+  }
 }
 
 /* ---------------------------------------------------------------------------

@@ -61,6 +61,10 @@ def _bind(lib):
     lib.oracle_sigmoid.argtypes = [c.c_int64, P, c.c_int64, P]
     lib.oracle_permute.restype = c.c_int32
     lib.oracle_permute.argtypes = [c.c_int64, c.c_int32, c.c_int32, P, P, P, P, P]
+    lib.oracle_round_act.restype = c.c_double
+    lib.oracle_round_act.argtypes = [c.c_double, c.c_int32]
+    lib.oracle_rmsnorm.restype = None
+    lib.oracle_rmsnorm.argtypes = [c.c_int64, c.c_int64, P, c.c_int32, P, c.c_double, P]
     lib.oracle_moe_ffn.restype = None
     lib.oracle_moe_ffn.argtypes = [c.c_int64, P, c.c_int64, c.c_int64, c.c_int64, c.c_int32,
                                    P, c.c_int32, c.c_int32, P, P, P, P, c.c_int64, P,
@@ -214,9 +218,36 @@ def moe_ffn(x, idx, weights, gate, w_gate, w_up, w_down, sh_gate=None, sh_up=Non
     return y
 
 
-def route(wl, inputs, tokens=None, nthreads: int = 0):
+def round_act(v: float, dtype: str) -> float:
+    """The activation-type value nearest to v (ties to even), as a float."""
+    return load().oracle_round_act(float(v), BF16 if dtype == "bf16" else F32)
+
+
+def rmsnorm(x, w, eps: float):
+    """x / sqrt(mean(x^2) + eps) * w per row, in fp64, rounded once to x's
+    type; returns a host tensor of that type (the values the layer's router
+    and experts see)."""
+    import torch
+    xk, xp, xdt = _host(x)
+    wk, wp, wdt = _host(w)
+    assert xdt == wdt
+    out = torch.empty(tuple(x.shape), dtype=xk.dtype)
+    T, H = x.shape
+    load().oracle_rmsnorm(T, H, xp, xdt, wp, float(eps), out.data_ptr())
+    return out
+
+
+def layer_input(wl, inputs):
+    """The activations the MoE FFN sees: x, or its input RMSNorm."""
+    if getattr(wl, "input_norm", False):
+        return rmsnorm(inputs["x"], inputs["norm_weight"], wl.norm_eps)
+    return inputs["x"]
+
+
+def route(wl, inputs, tokens=None, nthreads: int = 0, xin=None):
     """Routing for the listed tokens (all tokens when None): dict with idx,
-    weights, gate (or None) and gap.  Direct routes are returned as given."""
+    weights, gate (or None) and gap.  Direct routes are returned as given.
+    xin: the layer input (layer_input), computed here when None."""
     E, k = wl.E, wl.k
     if inputs.get("routes_idx") is not None:
         ridx = inputs["routes_idx"].cpu().numpy()
@@ -226,18 +257,25 @@ def route(wl, inputs, tokens=None, nthreads: int = 0):
         n = ridx.shape[0]
         return dict(idx=ridx.astype(np.int32), weights=rw, gate=None,
                     gap=np.full(n, np.inf), logits=None)
-    lg = router_logits(inputs["x"], inputs["w_router"], tokens, nthreads)
+    if xin is None:
+        xin = layer_input(wl, inputs)
+    lg = router_logits(xin, inputs["w_router"], tokens, nthreads)
     idx, w, gap = topk_softmax(lg, E, k, wl.norm_topk)
     gate = sigmoid(lg[:, E]) if wl.shared_gate else None
     return dict(idx=idx, weights=w, gate=gate, gap=gap, logits=lg)
 
 
 def forward(wl, inputs, tokens=None, nthreads: int = 0):
-    """Whole layer for the listed tokens: routing then expert FFNs + combine."""
-    r = route(wl, inputs, tokens, nthreads)
-    y = moe_ffn(inputs["x"], r["idx"], r["weights"], r["gate"], inputs["w_gate"],
+    """Whole layer for the listed tokens: input preparation (RMSNorm) when the
+    workload has it, routing, expert FFNs + combine, then the residual x."""
+    xin = layer_input(wl, inputs)
+    r = route(wl, inputs, tokens, nthreads, xin=xin)
+    y = moe_ffn(xin, r["idx"], r["weights"], r["gate"], inputs["w_gate"],
                 inputs["w_up"], inputs["w_down"], inputs.get("sh_gate"),
                 inputs.get("sh_up"), inputs.get("sh_down"), tokens=tokens,
                 nthreads=nthreads)
+    if getattr(wl, "residual", False):
+        x = inputs["x"].cpu().double().numpy()
+        y = y + (x if tokens is None else x[np.asarray(tokens)])
     r["y"] = y
     return r

@@ -49,6 +49,16 @@ MUTANTS = [
      "ld(c->wr, c->wdt, h * c->ncols + col)", [pins.check_dense_masked_form]),
     ("sigmoid sign", "gate[t] = 1.0 / (1.0 + exp(-z[t * ld_z]));",
      "gate[t] = 1.0 / (1.0 + exp(z[t * ld_z]));", [pins.check_gate]),
+    ("rmsnorm eps dropped", "1.0 / sqrt(ss / (double)H + eps)", "1.0 / sqrt(ss / (double)H)",
+     [pins.check_rmsnorm_closed_forms, pins.check_rmsnorm_high_precision]),
+    ("rmsnorm mean of x, not x^2", "ss += v * v;", "ss += fabs(v);",
+     [pins.check_rmsnorm_closed_forms, pins.check_rmsnorm_high_precision]),
+    ("norm weight ignored", "* inv * ld(w, dtype, h)", "* inv",
+     [pins.check_rmsnorm_closed_forms]),
+    ("rounding truncates", "r = rint(a / q) * q;", "r = floor(a / q) * q;",
+     [pins.check_round_act, pins.check_rmsnorm_high_precision]),
+    ("rounding keeps 7 bits", "q = ldexp(1.0, e - 8);", "q = ldexp(1.0, e - 7);",
+     [pins.check_round_act]),
 ]
 
 

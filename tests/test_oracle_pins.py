@@ -393,3 +393,132 @@ def test_workload_gate_stays_interior():
     z = (d["x"].double() @ d["w_router"][wl.E].double())
     g = torch.sigmoid(z).to(torch.bfloat16).float()
     assert bool(((g > 0) & (g < 1)).all())
+
+
+# ---------------------------------------------------------------------------
+# Input preparation: activation rounding, input RMSNorm, residual
+# ("MoE: shared experts, arbitrary V_TOPK expert shapes, and an enforced
+# stage-marker contract", Group E: residual_setup = residual copy + input
+# RMSNorm + norm-weight multiply)
+# ---------------------------------------------------------------------------
+def _bf16_nearest_exact(v):
+    """Nearest bf16 value to v with ties to even, by exact rational
+    arithmetic (Fraction) -- an independent statement of the rounding rule."""
+    from fractions import Fraction
+    if v == 0:
+        return 0.0
+    a = Fraction(abs(v))
+    if a < Fraction(2) ** -126:
+        q = Fraction(2) ** -133
+    else:
+        e = 0
+        while Fraction(2) ** (e + 1) <= a:
+            e += 1
+        while Fraction(2) ** e > a:
+            e -= 1
+        q = Fraction(2) ** (e - 7)        # 8 significant bits over [2^e, 2^(e+1))
+    r = round(a / q) * q                  # Python rounds Fractions half to even
+    if r > Fraction(255) * Fraction(2) ** 120:
+        return math.copysign(math.inf, v)
+    return math.copysign(float(r), v)
+
+
+def check_round_act():
+    rng = _rng(21)
+    vals = list(rng.standard_normal(400) * 10.0 ** rng.integers(-6, 6, size=400))
+    one = 1.0
+    for m in range(128, 256, 7):           # exact midpoints and just either side
+        mid = (m + 0.5) / 128.0
+        vals += [mid, mid + 2 ** -30, mid - 2 ** -30, -mid]
+    vals += [1 + 2 ** -8 + 2 ** -30, one, 2.0 ** -130, 3.3e-39, 3.0e38, 3.4e38, -7.0e-41]
+    for v in vals:
+        got = O.round_act(v, "bf16")
+        want = _bf16_nearest_exact(v)
+        assert got == want, (v, got, want)
+        assert O.round_act(v, "f32") == float(np.float32(v)), v
+
+
+def test_round_act(orc):
+    check_round_act()
+
+
+def check_rmsnorm_closed_forms():
+    H = 16
+    w1 = torch.ones(H, dtype=torch.bfloat16)
+    # constant rows: x / |x| = sign(x), for eps = 0
+    x = torch.tensor([[3.0] * H, [-0.25] * H], dtype=torch.bfloat16)
+    out = O.rmsnorm(x, w1, 0.0).float()
+    assert torch.equal(out, torch.tensor([[1.0] * H, [-1.0] * H]))
+    # alternating +-a: rms = a; the norm weight multiplies per column
+    x = torch.tensor([[5.0, -5.0] * (H // 2)], dtype=torch.bfloat16)
+    w = torch.tensor([0.5, 2.0, -1.0, 1.5] * (H // 4), dtype=torch.bfloat16)
+    out = O.rmsnorm(x, w, 0.0).float()
+    assert torch.equal(out, torch.tensor([[1.0, -1.0] * (H // 2)]) * w.float())
+    # eps enters under the square root: x = 1 everywhere, eps = 3 -> 1/2
+    out = O.rmsnorm(torch.ones(1, H, dtype=torch.bfloat16), w1, 3.0).float()
+    assert torch.equal(out, torch.full((1, H), 0.5))
+    # scale invariance (eps = 0, power-of-two scale: exact)
+    x = torch.from_numpy(_rng(22).standard_normal((3, H)).astype(np.float32)).to(torch.bfloat16)
+    a = O.rmsnorm(x, w1, 0.0)
+    b = O.rmsnorm(x * 8.0, w1, 0.0)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_rmsnorm_closed_forms(orc):
+    check_rmsnorm_closed_forms()
+
+
+def check_rmsnorm_high_precision():
+    """Random rows against a 60-digit evaluation of the definition, rounded
+    by the exact rule above: bit for bit."""
+    import mpmath
+    mpmath.mp.dps = 60
+    rng = _rng(23)
+    T, H = 5, 24
+    x = torch.from_numpy(rng.standard_normal((T, H)).astype(np.float32)).to(torch.bfloat16)
+    w = torch.from_numpy((1 + 0.2 * rng.standard_normal(H)).astype(np.float32)).to(torch.bfloat16)
+    eps = 1e-3
+    got = O.rmsnorm(x, w, eps).float().numpy()
+    xs, ws = x.float().numpy().astype(np.float64), w.float().numpy().astype(np.float64)
+    for t in range(T):
+        ms = mpmath.fsum([mpmath.mpf(float(v)) ** 2 for v in xs[t]]) / H
+        inv = 1 / mpmath.sqrt(ms + mpmath.mpf(eps))
+        for h in range(H):
+            exact = mpmath.mpf(float(xs[t, h])) * inv * mpmath.mpf(float(ws[h]))
+            want = _bf16_nearest_exact(float(exact))
+            # float(exact) is within 2^-53 relative; no case lands that close
+            # to a bf16 midpoint here (checked below)
+            q = abs(want) * 2.0 ** -8
+            assert abs(abs(float(exact)) - abs(want)) < q, (t, h)
+            assert got[t, h] == want, (t, h, got[t, h], want)
+
+
+def test_rmsnorm_high_precision(orc):
+    check_rmsnorm_high_precision()
+
+
+def check_residual_identity():
+    """y = x + MoE(rmsnorm(x)): with every expert weight zero the output is x
+    exactly; otherwise the residual run minus x is the run without it."""
+    import dataclasses
+    from mixture_experts_ffn_04_gb300 import workloads as W
+    wl = W.small(W.GEMMA4_26B_A4B, T=12, H=64, I=32, E=8, k=2)
+    inp = W.make_inputs(wl, seed=4)
+    zero = dict(inp, w_gate=torch.zeros_like(inp["w_gate"]),
+                w_up=torch.zeros_like(inp["w_up"]), w_down=torch.zeros_like(inp["w_down"]))
+    y0 = O.forward(wl, zero)["y"]
+    np.testing.assert_array_equal(y0, inp["x"].double().numpy())
+    y = O.forward(wl, inp)["y"]
+    ynr = O.forward(dataclasses.replace(wl, residual=False), inp)["y"]
+    np.testing.assert_allclose(y - inp["x"].double().numpy(), ynr, rtol=0, atol=1e-12)
+    # the routed part sees the normalised input, not x
+    xn = O.rmsnorm(inp["x"], inp["norm_weight"], wl.norm_eps)
+    r = O.route(wl, dict(inp, x=xn, norm_weight=None),
+                xin=xn)
+    ym = O.moe_ffn(xn, r["idx"], r["weights"], None, inp["w_gate"], inp["w_up"],
+                   inp["w_down"])
+    np.testing.assert_allclose(ynr, ym, rtol=0, atol=0)
+
+
+def test_residual_identity(orc):
+    check_residual_identity()
