@@ -149,6 +149,10 @@ def algorithmic(wl, counts: np.ndarray):
     layer_flops = wl.flops()
     layer_bytes = (touched * 3.0 * I * H * b + 3.0 * Ish * H * b + T * H * b * 2
                    + (wl.E + (1 if wl.shared_gate else 0)) * H * b)
+    if getattr(wl, "input_norm", False):   # x_norm written once (x itself read already)
+        layer_bytes += T * H * b + H * b
+    if getattr(wl, "residual", False):     # x read again by the combine
+        layer_bytes += T * H * b
     return dict(gu_flops=gu_flops, gu_bytes=gu_bytes, dn_flops=dn_flops,
                 gemm_flops=gu_flops + dn_flops + 6.0 * T * H * Ish,
                 layer_flops=layer_flops, layer_bytes=layer_bytes, touched=touched)

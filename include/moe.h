@@ -64,13 +64,15 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 /* Stages of the forward pass, in execution order.  Their names (see
  * moe_stage_name) label the benchmark's per-stage timings. */
 typedef enum {
-  MOE_STAGE_ROUTE = 0,   /* router GEMM + top-k softmax (+ shared gate) */
-  MOE_STAGE_PERMUTE = 1, /* histogram, offsets, scatter_index, row copy */
-  MOE_STAGE_GATE_UP = 2, /* grouped GEMM gate/up with fused SwiGLU */
-  MOE_STAGE_DOWN = 3,    /* grouped GEMM down */
-  MOE_STAGE_SHARED = 4,  /* shared-expert MLP (one group of T rows) */
-  MOE_STAGE_COMBINE = 5, /* route-weighted gather + shared add */
-  MOE_NUM_STAGES = 6
+  MOE_STAGE_RESIDUAL_SETUP = 0, /* input RMSNorm (compiler page, Group E:
+                                   residual_setup); empty without input_norm */
+  MOE_STAGE_ROUTE = 1,          /* router GEMM + top-k softmax (+ shared gate) */
+  MOE_STAGE_PERMUTE = 2,        /* histogram, offsets, scatter_index, row copy */
+  MOE_STAGE_GATE_UP = 3,        /* grouped GEMM gate/up with fused SwiGLU */
+  MOE_STAGE_DOWN = 4,           /* grouped GEMM down */
+  MOE_STAGE_SHARED = 5,         /* shared-expert MLP (one group of T rows) */
+  MOE_STAGE_COMBINE = 6,        /* route-weighted gather + shared and residual add */
+  MOE_NUM_STAGES = 7
 } moe_stage;
 
 /* Layer shape.  topk_shape is the packed routing-shape word
@@ -80,7 +82,12 @@ typedef enum {
  * as top_k = 0).  shared_gate = 1 needs shared_inter > 0 (a half-specified
  * shared branch is rejected, as the route-trace validator of the simulator
  * page does).  norm_topk = 1: weights = softmax over the k selected logits;
- * 0: the full softmax over all E logits, taken at the k selected. */
+ * 0: the full softmax over all E logits, taken at the k selected.
+ * input_norm = 1 prepares the input as the compiler page's residual_setup
+ * stage does (Group E): x_norm = x / sqrt(mean_h x^2 + norm_eps) * norm_weight
+ * (stored in the activation type, computed to about 2^-44 relative accuracy
+ * and rounded once), and the router, experts and shared MLP see x_norm;
+ * residual = 1 adds x to the output (y = x + MoE), inside the combine. */
 typedef struct {
   int64_t tokens;       /* T >= 0 */
   int32_t hidden;       /* H, multiple of 8 */
@@ -90,6 +97,9 @@ typedef struct {
   int32_t shared_gate;  /* 1: y's shared term is scaled by sigmoid(x . router[E]) */
   int32_t norm_topk;    /* 1: renormalise over the selected k */
   int32_t dtype;        /* moe_dtype */
+  int32_t input_norm;   /* 1: input RMSNorm before routing and experts */
+  int32_t residual;     /* 1: y = x + the MoE output */
+  double norm_eps;      /* RMSNorm epsilon, finite and >= 0 */
 } moe_shape;
 
 /* Weights for moe_layer_forward (device pointers, layouts as above). */
@@ -103,6 +113,7 @@ typedef struct {
   const void *shared_gate_proj; /* [I_sh, H] or NULL when shared_inter == 0 */
   const void *shared_up;        /* [I_sh, H] */
   const void *shared_down;      /* [H, I_sh] */
+  const void *norm_weight;      /* [H] input RMSNorm weight; needed iff input_norm */
 } moe_weights;
 
 /* Device pointers into a moe_layer_forward workspace where the routing of the
@@ -233,18 +244,30 @@ moe_status moe_grouped_down(const moe_shape *shape, const void *h, const void *w
                             int32_t num_groups, int64_t rows_bound, int32_t inter,
                             void *y_perm, void *ws, size_t ws_bytes, void *stream);
 
+/* Input preparation (compiler page, Group E: residual_setup):
+ *   x_norm[t, h] = x[t, h] / sqrt((1/H) sum_h x[t, h]^2 + norm_eps) * norm_weight[h]
+ * x, x_norm [T, H] and norm_weight [H] in the activation type; x_norm is
+ * computed to about 2^-44 relative accuracy and rounded once (nearest even).
+ * Uses shape->norm_eps whatever shape->input_norm says.  No workspace. */
+moe_status moe_residual_setup(const moe_shape *shape, const void *x, const void *norm_weight,
+                              void *x_norm, void *stream);
+
 /* Route-weighted gather-combine (gather of "Fused MoE Kernel Notes"; the
- * per-token K-axis sum of the Spyre adapter's decode path):
- *   y[t] = g_t * shared_out[t] + sum_s topk_w[t, s] * y_perm[scatter_index[t, s]]
+ * per-token K-axis sum of the Spyre adapter's decode path) with the residual:
+ *   y[t] = sum_s topk_w[t, s] * y_perm[scatter_index[t, s]] + g_t * shared_out[t]
+ *          + residual[t]
  * g_t = gate[t] when gate != NULL, else 1; the shared term is skipped when
- * shared_out == NULL.  Each y row is written once, no read-modify-write, so
- * duplicate routes are safe.  fp32 sums, y rounded once.  No workspace. */
+ * shared_out == NULL, the residual when residual == NULL.  Each y row is
+ * written once, no read-modify-write, so duplicate routes are safe.  fp32
+ * sums in that order, y rounded once.  No workspace. */
 moe_status moe_combine(const moe_shape *shape, const void *y_perm,
                        const int32_t *scatter_index, const float *topk_w,
-                       const void *shared_out, const float *gate, void *y, void *stream);
+                       const void *shared_out, const float *gate, const void *residual,
+                       void *y, void *stream);
 
-/* Whole layer: route (or direct routes) -> permute -> grouped gate/up+SwiGLU
- * -> grouped down -> shared MLP -> combine, all on `stream`, no host sync.
+/* Whole layer: [residual_setup] -> route (or direct routes) -> permute ->
+ * grouped gate/up+SwiGLU -> grouped down -> shared MLP -> combine (+ residual),
+ * all on `stream`, no host sync.
  * routes_idx/routes_w [T, k] (device) replace the router when non-NULL
  * (duplicates allowed); weights->router may then be NULL, and shared_gate
  * must be 0.  ws_bytes >= moe_workspace_bytes(shape). */

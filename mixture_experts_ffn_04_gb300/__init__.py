@@ -26,7 +26,7 @@ MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_DEVICE_ROUTE, MOE_ERR_TIMEOUT, MOE_ERR_ROWS = 4, 5, 6, 7
 MOE_ERR_GATHER = 8
 MOE_F32, MOE_BF16 = 0, 1
-STAGES = ("route", "permute", "gate_up", "down", "shared", "combine")
+STAGES = ("residual_setup", "route", "permute", "gate_up", "down", "shared", "combine")
 
 
 class MoEError(RuntimeError):
@@ -40,14 +40,17 @@ class MoEShape(ctypes.Structure):
     _fields_ = [("tokens", ctypes.c_int64), ("hidden", ctypes.c_int32),
                 ("moe_inter", ctypes.c_int32), ("shared_inter", ctypes.c_int32),
                 ("topk_shape", ctypes.c_uint32), ("shared_gate", ctypes.c_int32),
-                ("norm_topk", ctypes.c_int32), ("dtype", ctypes.c_int32)]
+                ("norm_topk", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("input_norm", ctypes.c_int32), ("residual", ctypes.c_int32),
+                ("norm_eps", ctypes.c_double)]
 
 
 class MoEWeights(ctypes.Structure):
     _fields_ = [("router", ctypes.c_void_p), ("gate", ctypes.c_void_p), ("up", ctypes.c_void_p),
                 ("gate_up_stride", ctypes.c_int64), ("down", ctypes.c_void_p),
                 ("down_stride", ctypes.c_int64), ("shared_gate_proj", ctypes.c_void_p),
-                ("shared_up", ctypes.c_void_p), ("shared_down", ctypes.c_void_p)]
+                ("shared_up", ctypes.c_void_p), ("shared_down", ctypes.c_void_p),
+                ("norm_weight", ctypes.c_void_p)]
 
 
 class MoERouteInfo(ctypes.Structure):
@@ -83,7 +86,8 @@ def lib():
         "moe_grouped_swiglu": (i32, [S, P, P, P, i64, P, i32, i64, i32, P, P, sz, P]),
         "moe_grouped_swiglu_gather": (i32, [S, P, P, P, P, i64, P, i32, i64, i32, P, P, sz, P]),
         "moe_grouped_down": (i32, [S, P, P, i64, P, i32, i64, i32, P, P, sz, P]),
-        "moe_combine": (i32, [S, P, P, P, P, P, P, P]),
+        "moe_combine": (i32, [S, P, P, P, P, P, P, P, P]),
+        "moe_residual_setup": (i32, [S, P, P, P, P]),
         "moe_layer_forward": (i32, [S, ctypes.POINTER(MoEWeights), P, P, P, P, P, sz, P]),
         "moe_layer_forward_traced": (i32, [S, ctypes.POINTER(MoEWeights), P, P, P, P, P, sz, P,
                                            ctypes.POINTER(ctypes.c_void_p)]),
@@ -238,9 +242,16 @@ def moe_grouped_down(shape, h, w_down, expert_stride, offsets, num_groups, rows_
            "moe_grouped_down")
 
 
-def moe_combine(shape, y_perm, scatter_index, topk_w, shared_out, gate, y, stream=None):
+def moe_combine(shape, y_perm, scatter_index, topk_w, shared_out, gate, y, stream=None,
+                residual=None):
     _check(lib().moe_combine(ctypes.byref(shape), _p(y_perm), _p(scatter_index), _p(topk_w),
-                             _p(shared_out), _p(gate), _p(y), _stream(stream)), "moe_combine")
+                             _p(shared_out), _p(gate), _p(residual), _p(y), _stream(stream)),
+           "moe_combine")
+
+
+def moe_residual_setup(shape, x, norm_weight, x_norm, stream=None):
+    _check(lib().moe_residual_setup(ctypes.byref(shape), _p(x), _p(norm_weight), _p(x_norm),
+                                    _stream(stream)), "moe_residual_setup")
 
 
 def moe_layer_forward(shape, weights: MoEWeights, x, routes_idx, routes_w, y, ws, stream=None):
@@ -312,6 +323,9 @@ def shape_for(wl, T: Optional[int] = None) -> MoEShape:
     s.shared_gate = int(wl.shared_gate)
     s.norm_topk = int(wl.norm_topk)
     s.dtype = MOE_F32 if wl.dtype == "f32" else MOE_BF16
+    s.input_norm = int(getattr(wl, "input_norm", False))
+    s.residual = int(getattr(wl, "residual", False))
+    s.norm_eps = float(getattr(wl, "norm_eps", 1e-6))
     return s
 
 
@@ -338,6 +352,7 @@ def weights_from(inputs: dict) -> MoEWeights:
     w.shared_gate_proj = _p(inputs.get("sh_gate"))
     w.shared_up = _p(inputs.get("sh_up"))
     w.shared_down = _p(inputs.get("sh_down"))
+    w.norm_weight = _p(inputs.get("norm_weight"))
     return w
 
 

@@ -1,6 +1,7 @@
 // combine.cu -- route-weighted gather-combine plus the shared-expert add.
 //
-//   y[t] = g_t * shared_out[t] + sum_s w[t, s] * y_perm[scatter_index[t, s]]
+//   y[t] = sum_s w[t, s] * y_perm[scatter_index[t, s]] + g_t * shared_out[t]
+//          (+ residual[t], the sublayer input x)
 //
 // "Fused MoE Kernel Notes", Scatter/gather layout (moe_gather sums the routed
 // expert outputs back to [tokens, hidden]); the Spyre adapter's decode path
@@ -22,6 +23,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y_pe
                                                       const float* __restrict__ w, int k, int H,
                                                       const T* __restrict__ shared_out,
                                                       const float* __restrict__ gate,
+                                                      const T* __restrict__ residual,
                                                       T* __restrict__ y,
                                                       const float* __restrict__ shared_part,
                                                       int nsplit_sh, int64_t part_stride) {
@@ -88,6 +90,13 @@ __global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y_pe
 #pragma unroll
       for (int i = 0; i < V; ++i) acc[i] = fmaf(g, f[i], acc[i]);
     }
+    if (residual) {
+      float f[V];
+      unpack16(__ldg(reinterpret_cast<const uint4*>(residual + t * H) + v), f,
+               (const T*)nullptr);
+#pragma unroll
+      for (int i = 0; i < V; ++i) acc[i] += f[i];
+    }
     reinterpret_cast<uint4*>(y + t * H)[v] = pack16(acc, (const T*)nullptr);
   }
 }
@@ -96,7 +105,8 @@ __global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y_pe
 
 cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* scatter_index,
                            const float* topk_w, const void* shared_out, const float* gate,
-                           void* y, cudaStream_t st, const float* shared_part, int nsplit_sh) {
+                           const void* residual, void* y, cudaStream_t st,
+                           const float* shared_part, int nsplit_sh) {
   const int64_t part_stride = s.T * (int64_t)s.H;
   if (s.T == 0) return cudaSuccess;
   const size_t smem = (size_t)s.k * 8;
@@ -109,17 +119,19 @@ cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* sc
   if (s.dtype == MOE_F32) {
     const float* yp = reinterpret_cast<const float*>(y_perm);
     const float* so = reinterpret_cast<const float*>(shared_out);
+    const float* rs = reinterpret_cast<const float*>(residual);
     float* yo = reinterpret_cast<float*>(y);
-    if (sh == 0) combine_kernel<float, 0><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, yo, shared_part, nsplit_sh, part_stride);
-    else if (sh == 1) combine_kernel<float, 1><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, yo, shared_part, nsplit_sh, part_stride);
-    else combine_kernel<float, 2><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, yo, shared_part, nsplit_sh, part_stride);
+    if (sh == 0) combine_kernel<float, 0><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, rs, yo, shared_part, nsplit_sh, part_stride);
+    else if (sh == 1) combine_kernel<float, 1><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, rs, yo, shared_part, nsplit_sh, part_stride);
+    else combine_kernel<float, 2><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, rs, yo, shared_part, nsplit_sh, part_stride);
   } else {
     const bf16* yp = reinterpret_cast<const bf16*>(y_perm);
     const bf16* so = reinterpret_cast<const bf16*>(shared_out);
+    const bf16* rs = reinterpret_cast<const bf16*>(residual);
     bf16* yo = reinterpret_cast<bf16*>(y);
-    if (sh == 0) combine_kernel<bf16, 0><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, yo, shared_part, nsplit_sh, part_stride);
-    else if (sh == 1) combine_kernel<bf16, 1><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, yo, shared_part, nsplit_sh, part_stride);
-    else combine_kernel<bf16, 2><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, yo, shared_part, nsplit_sh, part_stride);
+    if (sh == 0) combine_kernel<bf16, 0><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, rs, yo, shared_part, nsplit_sh, part_stride);
+    else if (sh == 1) combine_kernel<bf16, 1><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, rs, yo, shared_part, nsplit_sh, part_stride);
+    else combine_kernel<bf16, 2><<<grid, 128, smem, st>>>(yp, scatter_index, topk_w, s.k, s.H, so, gate, rs, yo, shared_part, nsplit_sh, part_stride);
   }
   count_launch();
   return cudaGetLastError();

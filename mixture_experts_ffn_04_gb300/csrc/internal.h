@@ -19,6 +19,8 @@ struct Shape {
   int esize;   // bytes per activation / weight element
   int ncols;   // router rows: E + gate
   int ldl;     // leading dimension of the fp32 logits buffer
+  int input_norm, residual;
+  double norm_eps;
 };
 
 // Decode and validate; on failure returns the status and sets *why.
@@ -30,8 +32,8 @@ struct Layout {
   size_t flags, logits, hist, base, sched_routed, sched_shared, sched_router, scratch_end;
   int nchunks, tokens_per_chunk;
   // layer-forward intermediates
-  size_t topk_idx, topk_w, gate, counts, offsets, sidx, row_token, x_perm, h, y_perm, sh_h,
-      sh_out, total;
+  size_t x_norm, topk_idx, topk_w, gate, counts, offsets, sidx, row_token, x_perm, h, y_perm,
+      sh_h, sh_out, total;
 };
 Layout layout_for(const Shape& s);
 
@@ -108,8 +110,11 @@ void set_error_message(const char* why);
 // of the shared MLP output ([T, H] each, T*H apart), added in order.
 cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* scatter_index,
                            const float* topk_w, const void* shared_out, const float* gate,
-                           void* y, cudaStream_t st, const float* shared_part = nullptr,
-                           int nsplit_sh = 0);
+                           const void* residual, void* y, cudaStream_t st,
+                           const float* shared_part = nullptr, int nsplit_sh = 0);
+// Input RMSNorm [T, H] -> [T, H] (norm.cu).
+cudaError_t launch_rmsnorm(const Shape& s, const void* x, const void* w, double eps, void* out,
+                           cudaStream_t st);
 
 // Shared-MLP down projection split over K for at most this many tokens.
 constexpr int64_t kSharedSplitMaxT = 4096;

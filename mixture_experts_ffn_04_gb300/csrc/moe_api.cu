@@ -70,7 +70,18 @@ moe_status decode_shape(const moe_shape* s, Shape* o, const char** why) {
     *why = "norm_topk must be 0 or 1";
     return MOE_ERR_INVALID_ARG;
   }
+  if ((s->input_norm != 0 && s->input_norm != 1) || (s->residual != 0 && s->residual != 1)) {
+    *why = "input_norm and residual must be 0 or 1";
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (!(s->norm_eps >= 0.0) || s->norm_eps > 1e30) {   // also rejects NaN
+    *why = "norm_eps must be finite and >= 0";
+    return MOE_ERR_INVALID_ARG;
+  }
   o->T = s->tokens;
+  o->input_norm = s->input_norm;
+  o->residual = s->residual;
+  o->norm_eps = s->norm_eps;
   o->H = s->hidden;
   o->I = s->moe_inter;
   o->I_sh = s->shared_inter;
@@ -105,6 +116,7 @@ Layout layout_for(const Shape& s) {
   L.sched_shared = off; off += 256;
   L.sched_router = off; off += 256;
   L.scratch_end = off;
+  L.x_norm = off; off += align256(s.input_norm ? T * (size_t)s.H * s.esize : 0);
   L.topk_idx = off; off += align256(T * k * 4);
   L.topk_w = off; off += align256(T * k * 4);
   L.gate = off; off += align256(T * 4);
@@ -418,16 +430,28 @@ moe_status moe_grouped_down(const moe_shape* shape, const void* h, const void* w
                  rows_bound, inter, y_perm, ws, ws_bytes, stream);
 }
 
+moe_status moe_residual_setup(const moe_shape* shape, const void* x, const void* norm_weight,
+                              void* x_norm, void* stream) {
+  reset_launch_count();
+  DECODE(shape, s);
+  if (s.T > 0 && (!x || !norm_weight || !x_norm))
+    return fail(MOE_ERR_INVALID_ARG, "x, norm_weight and x_norm must be non-NULL");
+  if (!aligned16(x) || !aligned16(norm_weight) || !aligned16(x_norm))
+    return fail(MOE_ERR_INVALID_ARG, "x, norm_weight and x_norm must be 16-byte aligned");
+  CHECK_CUDA(launch_rmsnorm(s, x, norm_weight, s.norm_eps, x_norm, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
 moe_status moe_combine(const moe_shape* shape, const void* y_perm, const int32_t* scatter_index,
-                       const float* topk_w, const void* shared_out, const float* gate, void* y,
-                       void* stream) {
+                       const float* topk_w, const void* shared_out, const float* gate,
+                       const void* residual, void* y, void* stream) {
   reset_launch_count();
   DECODE(shape, s);
   if (s.T > 0 && (!y_perm || !scatter_index || !topk_w || !y))
     return fail(MOE_ERR_INVALID_ARG, "y_perm, scatter_index, topk_w and y must be non-NULL");
-  if (!aligned16(y_perm) || !aligned16(shared_out) || !aligned16(y))
-    return fail(MOE_ERR_INVALID_ARG, "y_perm, shared_out and y must be 16-byte aligned");
-  CHECK_CUDA(launch_combine(s, y_perm, scatter_index, topk_w, shared_out, gate, y,
+  if (!aligned16(y_perm) || !aligned16(shared_out) || !aligned16(residual) || !aligned16(y))
+    return fail(MOE_ERR_INVALID_ARG, "y_perm, shared_out, residual and y must be 16-byte aligned");
+  CHECK_CUDA(launch_combine(s, y_perm, scatter_index, topk_w, shared_out, gate, residual, y,
                             (cudaStream_t)stream));
   return MOE_OK;
 }
@@ -471,6 +495,12 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
     return fail(MOE_ERR_INVALID_ARG, "shared weights given but shared_inter is 0");
   if (W->gate_up_stride < (int64_t)s.I * s.H || W->down_stride < (int64_t)s.H * s.I)
     return fail(MOE_ERR_INVALID_ARG, "expert strides smaller than one expert matrix");
+  if (s.input_norm && s.T > 0 && !W->norm_weight)
+    return fail(MOE_ERR_INVALID_ARG, "input_norm needs weights->norm_weight");
+  if (!s.input_norm && W->norm_weight)
+    return fail(MOE_ERR_INVALID_ARG, "norm_weight given but input_norm is 0");
+  if (!aligned16(W->norm_weight))
+    return fail(MOE_ERR_INVALID_ARG, "norm_weight must be 16-byte aligned");
   if (!aligned16(x) || !aligned16(y) || !aligned16(W->router) || !aligned16(W->gate) ||
       !aligned16(W->up) || !aligned16(W->down) || !aligned16(W->shared_gate_proj) ||
       !aligned16(W->shared_up) || !aligned16(W->shared_down) ||
@@ -490,12 +520,19 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
   const float* use_w = tw;
 #define STAGE_EVENT(i) \
   if (ev) CHECK_CUDA(record_stage_event(ev[i], st))
+  // the activations the FFN sees: x, or its input RMSNorm
+  STAGE_EVENT(MOE_STAGE_RESIDUAL_SETUP);
+  const void* xin = x;
+  if (s.input_norm) {
+    CHECK_CUDA(launch_rmsnorm(s, x, W->norm_weight, s.norm_eps, w + L.x_norm, st));
+    xin = w + L.x_norm;
+  }
   STAGE_EVENT(MOE_STAGE_ROUTE);
   if (direct) {
     use_idx = routes_idx;
     use_w = routes_w;
   } else {
-    moe_status r = do_route(s, L, w, x, W->router, idx, tw, gate, st);
+    moe_status r = do_route(s, L, w, xin, W->router, idx, tw, gate, st);
     if (r != MOE_OK) return r;
   }
   int32_t* counts = reinterpret_cast<int32_t*>(w + L.counts);
@@ -510,7 +547,7 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
   // through a TMA tensor map: at prefill sizes that is faster than gathering
   // the rows inside the GEMM (moe_grouped_swiglu_gather), whose cp.async
   // producers cannot keep the tensor cores fed.
-  CHECK_CUDA(launch_permute(s, L, w, x, use_idx, counts, offsets, sidx, row_token, x_perm, st));
+  CHECK_CUDA(launch_permute(s, L, w, xin, use_idx, counts, offsets, sidx, row_token, x_perm, st));
   STAGE_EVENT(MOE_STAGE_GATE_UP);
 
   GemmArgs a;
@@ -558,7 +595,7 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
     b.sched = reinterpret_cast<int32_t*>(w + L.sched_shared);
     b.flags = flags;
     b.mode = kSwiGLU;
-    b.A = x;
+    b.A = xin;
     b.B0 = W->shared_gate_proj;
     b.B1 = W->shared_up;
     b.bstride = 0;
@@ -584,11 +621,12 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
     CHECK_CUDA(launch_grouped_gemm(b, st));
   }
   STAGE_EVENT(MOE_STAGE_COMBINE);
+  const void* resid = s.residual ? x : nullptr;
   if (sh_split > 1) {
-    CHECK_CUDA(launch_combine(s, y_perm, sidx, use_w, nullptr, gate, y, st,
+    CHECK_CUDA(launch_combine(s, y_perm, sidx, use_w, nullptr, gate, resid, y, st,
                               static_cast<const float*>(sh_out), sh_split));
   } else {
-    CHECK_CUDA(launch_combine(s, y_perm, sidx, use_w, sh_out, gate, y, st));
+    CHECK_CUDA(launch_combine(s, y_perm, sidx, use_w, sh_out, gate, resid, y, st));
   }
   STAGE_EVENT(MOE_NUM_STAGES);
 #undef STAGE_EVENT
@@ -655,8 +693,8 @@ const char* moe_status_string(moe_status st) {
 const char* moe_last_error(void) { return tl_error; }
 
 const char* moe_stage_name(int32_t stage) {
-  static const char* names[MOE_NUM_STAGES] = {"route",  "permute", "gate_up",
-                                              "down",   "shared",  "combine"};
+  static const char* names[MOE_NUM_STAGES] = {"residual_setup", "route", "permute", "gate_up",
+                                              "down", "shared", "combine"};
   if (stage < 0 || stage >= MOE_NUM_STAGES) return "";
   return names[stage];
 }

@@ -68,7 +68,7 @@ def oracle_ffn(wl, host_x, dev_or_host, tokens, idx, w, gate):
 
 def host_routing_inputs(dev):
     d = {"x": dev["x"].cpu()}
-    for k in ("w_router", "routes_idx", "routes_w"):
+    for k in ("w_router", "routes_idx", "routes_w", "norm_weight"):
         d[k] = None if dev.get(k) is None else dev[k].cpu()
     return d
 
@@ -82,7 +82,8 @@ def check_layer(wl, dev, res, sample=None, report=None):
     y = res["y"]
     assert bool(torch.isfinite(y).all()), "non-finite output"
     hin = host_routing_inputs(dev)
-    r_all = O.route(wl, hin)                       # every token
+    xin = O.layer_input(wl, hin)                   # x, or its input RMSNorm
+    r_all = O.route(wl, hin, xin=xin)              # every token
     gidx = res["topk_idx"].numpy() if res["topk_idx"] is not None else None
     if wl.routing == "router":
         mism = (gidx != r_all["idx"]).any(axis=1)
@@ -110,8 +111,10 @@ def check_layer(wl, dev, res, sample=None, report=None):
     # layer output
     tokens = np.arange(T) if sample is None else np.asarray(sample)
     tokens = tokens[ok[tokens]]
-    ref = oracle_ffn(wl, hin["x"], dev, tokens, r_all["idx"][tokens], r_all["weights"][tokens],
+    ref = oracle_ffn(wl, xin, dev, tokens, r_all["idx"][tokens], r_all["weights"][tokens],
                      None if r_all["gate"] is None else r_all["gate"][tokens])
+    if wl.residual:
+        ref = ref + hin["x"].double().numpy()[tokens]
     yg = y.index_select(0, torch.as_tensor(tokens, device=y.device)).double().cpu().numpy()
     err = rel_l2(yg, ref)
     tol = TOL[wl.dtype]

@@ -48,9 +48,9 @@ def test_pack_unpack_matches_pages_rule(m):
 
 def test_stage_names(m):
     """The stage vocabulary of the header and the binding agree both ways."""
-    names = [m.moe_stage_name(i) for i in range(6)]
+    names = [m.moe_stage_name(i) for i in range(7)]
     assert tuple(names) == m.STAGES
-    assert m.moe_stage_name(6) == "" and m.moe_stage_name(-1) == ""
+    assert m.moe_stage_name(7) == "" and m.moe_stage_name(-1) == ""
 
 
 def _shape(m, **kw):
@@ -73,6 +73,9 @@ def test_validation_rejects_bad_shapes(m):
         (dict(dtype=7), m.MOE_ERR_UNSUPPORTED, "dtype"),
         (dict(hidden=100), m.MOE_ERR_INVALID_ARG, "multiples of 8"),
         (dict(tokens=-1), m.MOE_ERR_INVALID_ARG, "tokens"),
+        (dict(input_norm=2), m.MOE_ERR_INVALID_ARG, "input_norm"),
+        (dict(norm_eps=-1e-6), m.MOE_ERR_INVALID_ARG, "norm_eps"),
+        (dict(norm_eps=float("nan")), m.MOE_ERR_INVALID_ARG, "norm_eps"),
     ]
     for kw, status, frag in cases:
         s = _shape(m, **kw)
@@ -107,6 +110,16 @@ def test_validation_rejects_bad_calls(m):
     st = lib.moe_route(ctypes.byref(s2), P(4096), P(4096), P(4096), P(4096), None, P(4096),
                        1 << 30, None)
     assert st == m.MOE_ERR_INVALID_ARG and "top_k" in m.moe_last_error()
+    # input RMSNorm without its weight, and a weight without input_norm
+    sn = _shape(m, input_norm=1)
+    st = lib.moe_layer_forward(ctypes.byref(sn), ctypes.byref(w), P(4096), None, None,
+                               P(4096), P(4096), m.moe_workspace_bytes(sn), None)
+    assert st == m.MOE_ERR_INVALID_ARG and "norm_weight" in m.moe_last_error()
+    w.norm_weight = 4096
+    st = lib.moe_layer_forward(ctypes.byref(s), ctypes.byref(w), P(4096), None, None,
+                               P(4096), P(4096), need, None)
+    assert st == m.MOE_ERR_INVALID_ARG and "input_norm" in m.moe_last_error()
+    w.norm_weight = None
     # shared weights without shared_inter
     w.shared_up = 4096
     st = lib.moe_layer_forward(ctypes.byref(s), ctypes.byref(w), P(4096), None, None, P(4096),

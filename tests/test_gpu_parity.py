@@ -8,6 +8,8 @@ on routing (every token, bit-exact), grouping (bit-exact) and a seeded token
 sample of the output.  Intermediates are poisoned with NaN before each run, so
 a row the kernels failed to write shows up as a non-finite output.
 """
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -31,6 +33,9 @@ REDUCED = [
     W.small(W.QWEN3_30B_A3B, T=100, H=256, I=128, E=64, k=40),    # k+1 > 32: warp top-k
     W.small(W.QWEN3_30B_A3B, T=200, H=256, I=128, E=300, k=4),    # E > 256
     W.small(W.QWEN3_30B_A3B, T=600, H=256, I=128, E=2048, k=4),   # > 1024 groups, > 512 columns
+    W.small(W.GEMMA4_26B_A4B, T=300, H=704, I=176, E=16, k=4),    # input RMSNorm + residual
+    dataclasses.replace(W.small(W.TINY_F32, T=200), input_norm=True, residual=True,
+                        name="tiny-f32-norm-residual-T200"),
 ]
 ENGINES = {0: "auto", 1: "cuda-core", 2: "tensor-core", 3: "skinny", 4: "tensor-core-pairs"}
 
@@ -65,6 +70,8 @@ FULL = [
     (W.get("adversarial-all-e0-T16384"), 8),
     (W.get("adversarial-zipf-T128"), 24),
     (W.get("adversarial-zipf-T16384"), 8),
+    (W.get("gemma4-26b-a4b-shape-T512"), 24),
+    (W.get("gemma4-26b-a4b-shape-T4096"), 12),
 ]
 
 
@@ -114,7 +121,7 @@ def test_step_api_matches_layer_and_merged_fc1():
     sh = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
     m.moe_grouped_down(s, hs, dev["sh_down"], 0, one, 1, T, Ish, sh, ws)
     y = torch.empty_like(dev["x"])
-    m.moe_combine(s, y_perm, sidx, tw, sh, gate, y)
+    m.moe_combine(s, y_perm, sidx, tw, sh, gate, y)   # no residual: this workload has none
     torch.cuda.synchronize()
     assert m.moe_get_device_status(ws)[0] == m.MOE_OK
     assert torch.equal(y, y_ref)
@@ -342,3 +349,58 @@ def test_router_logit_error_within_tie_bound(wl):
     print("%s: max |fp32 logit - exact| = %.3e (%.3f of the smallest tie bound), "
           "re-decided %d of %d tokens" % (wl.name, err, err / bound, redecided, T))
     assert err < 0.5 * bound
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+def test_residual_setup_matches_oracle(dtype):
+    """moe_residual_setup against the oracle's RMSNorm (fp64, rounded once):
+    bf16 bit for bit; fp32 within one ulp (the kernel's double-float value
+    can sit on the other side of an fp32 rounding boundary about once in 2^22
+    elements)."""
+    from oracle import oracle as O
+    wl = W.small(W.GEMMA4_26B_A4B, T=300, H=704, I=176, E=16, k=4)
+    wl = dataclasses.replace(wl, dtype=dtype)
+    inp = W.make_inputs(wl, seed=9, with_experts=False)
+    x = inp["x"] * 3.0 + 0.5          # an offset and a scale: rms far from 1
+    ref = O.rmsnorm(x, inp["norm_weight"], wl.norm_eps)
+    s = m.shape_for(wl)
+    xd, wd = x.cuda(), inp["norm_weight"].cuda()
+    out = torch.empty_like(xd)
+    m.moe_residual_setup(s, xd, wd, out)
+    got = out.cpu()
+    if dtype == "bf16":
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))
+    else:
+        diff = (got.view(torch.int32).long() - ref.view(torch.int32).long()).abs()
+        assert int(diff.max()) <= 1
+
+
+def test_step_api_with_input_norm_and_residual():
+    """residual_setup -> route -> permute -> gate/up -> down -> combine with
+    the residual, through the individual entry points, equals the layer bit
+    for bit."""
+    wl = W.small(W.GEMMA4_26B_A4B, T=300, H=704, I=176, E=16, k=4)
+    dev = to_dev(W.make_inputs(wl, seed=3, device="cpu"))
+    layer = m.MoELayer(wl, dev)
+    y_ref = layer.forward(dev["x"])
+    s = layer.shape
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    ws = m.alloc_workspace(s, full=False)
+    i32 = dict(dtype=torch.int32, device="cuda")
+    xn = torch.empty_like(dev["x"])
+    m.moe_residual_setup(s, dev["x"], dev["norm_weight"], xn)
+    idx, tw = torch.empty(T, k, **i32), torch.empty(T, k, dtype=torch.float32, device="cuda")
+    m.moe_route(s, xn, dev["w_router"], idx, tw, None, ws)
+    counts, offsets = torch.empty(E, **i32), torch.empty(E + 1, **i32)
+    sidx, row_token = torch.empty(T, k, **i32), torch.empty(T * k, **i32)
+    x_perm = torch.empty(T * k, H, dtype=torch.bfloat16, device="cuda")
+    m.moe_permute(s, xn, idx, counts, offsets, sidx, row_token, x_perm, ws)
+    h = torch.empty(T * k, I, dtype=torch.bfloat16, device="cuda")
+    m.moe_grouped_swiglu(s, x_perm, dev["w_gate"], dev["w_up"], I * H, offsets, E, T * k, I, h, ws)
+    y_perm = torch.empty(T * k, H, dtype=torch.bfloat16, device="cuda")
+    m.moe_grouped_down(s, h, dev["w_down"], H * I, offsets, E, T * k, I, y_perm, ws)
+    y = torch.empty_like(dev["x"])
+    m.moe_combine(s, y_perm, sidx, tw, None, None, y, residual=dev["x"])
+    torch.cuda.synchronize()
+    assert m.moe_get_device_status(ws)[0] == m.MOE_OK
+    assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
