@@ -41,6 +41,14 @@ __device__ __forceinline__ df two_prod(float a, float b) {
   const float p = __fmul_rn(a, b);
   return {p, __fmaf_rn(a, b, -p)};
 }
+// Product of two activation-type values as a double-float.  Two bf16 values
+// have 8 significant bits each, so their fp32 product is exact.
+__device__ __forceinline__ df exact_prod(float a, float b, const bf16*) {
+  return {__fmul_rn(a, b), 0.f};
+}
+__device__ __forceinline__ df exact_prod(float a, float b, const float*) {
+  return two_prod(a, b);
+}
 __device__ __forceinline__ df df_add(df a, df b) {
   df s = two_sum(a.hi, b.hi);
   s.lo = __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo));
@@ -113,7 +121,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const T* __restrict__ x,
         unpack16(u[b], f, (const T*)nullptr);
 #pragma unroll
         for (int i = 0; i < V; ++i) {
-          const df p = two_prod(f[i], f[i]);
+          const df p = exact_prod(f[i], f[i], (const T*)nullptr);
           const df s = two_sum(ss.hi, p.hi);
           ss = {s.hi, __fadd_rn(ss.lo, __fadd_rn(s.lo, p.lo))};
         }
@@ -145,8 +153,9 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const T* __restrict__ x,
         unpack16(uw[b], g, (const T*)nullptr);
         T o[V];
 #pragma unroll
-        for (int i = 0; i < V; ++i) o[i] = round_out(df_mul(two_prod(f[i], g[i]), inv),
-                                                     (const T*)nullptr);
+        for (int i = 0; i < V; ++i)
+          o[i] = round_out(df_mul(exact_prod(f[i], g[i], (const T*)nullptr), inv),
+                           (const T*)nullptr);
         orow[c0 + 32 * b] = *reinterpret_cast<const uint4*>(o);
       }
     }
