@@ -87,7 +87,11 @@ typedef enum {
  * stage does (Group E): x_norm = x / sqrt(mean_h x^2 + norm_eps) * norm_weight
  * (stored in the activation type, computed to about 2^-44 relative accuracy
  * and rounded once), and the router, experts and shared MLP see x_norm;
- * residual = 1 adds x to the output (y = x + MoE), inside the combine. */
+ * residual = 1 adds x to the output (y = x + MoE), inside the combine.
+ * train = 1: moe_layer_forward also keeps, in its workspace, what
+ * moe_layer_backward (moe_backward.h) needs -- the gate/up pre-activations
+ * of every grouped row and a copy of direct routes -- and the workspace
+ * grows by the backward's grouped buffers. */
 typedef struct {
   int64_t tokens;       /* T >= 0 */
   int32_t hidden;       /* H, multiple of 8 */
@@ -100,6 +104,7 @@ typedef struct {
   int32_t input_norm;   /* 1: input RMSNorm before routing and experts */
   int32_t residual;     /* 1: y = x + the MoE output */
   double norm_eps;      /* RMSNorm epsilon, finite and >= 0 */
+  int32_t train;        /* 1: keep what the backward needs (see above) */
 } moe_shape;
 
 /* Weights for moe_layer_forward (device pointers, layouts as above). */

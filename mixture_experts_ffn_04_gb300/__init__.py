@@ -42,7 +42,7 @@ class MoEShape(ctypes.Structure):
                 ("topk_shape", ctypes.c_uint32), ("shared_gate", ctypes.c_int32),
                 ("norm_topk", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("input_norm", ctypes.c_int32), ("residual", ctypes.c_int32),
-                ("norm_eps", ctypes.c_double)]
+                ("norm_eps", ctypes.c_double), ("train", ctypes.c_int32)]
 
 
 class MoEWeights(ctypes.Structure):
@@ -51,6 +51,16 @@ class MoEWeights(ctypes.Structure):
                 ("down_stride", ctypes.c_int64), ("shared_gate_proj", ctypes.c_void_p),
                 ("shared_up", ctypes.c_void_p), ("shared_down", ctypes.c_void_p),
                 ("norm_weight", ctypes.c_void_p)]
+
+
+class MoEExpertGrads(ctypes.Structure):
+    _fields_ = [("gate", ctypes.c_void_p), ("up", ctypes.c_void_p),
+                ("gate_up_stride", ctypes.c_int64), ("down", ctypes.c_void_p),
+                ("down_stride", ctypes.c_int64)]
+
+
+class MoEBackwardInfo(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("fc1", "grad_fc2", "d_fc1", "dx_perm")]
 
 
 class MoERouteInfo(ctypes.Structure):
@@ -99,6 +109,16 @@ def lib():
         "moe_testing_set_gemm_engine": (i32, [i32]),
         "moe_get_route_stats": (i32, [P, P, ctypes.POINTER(u32)]),
         "moe_testing_router_logits": (i32, [S, P, P, P, P, sz, P]),
+        # backward (moe_backward.h)
+        "moe_backward_views": (i32, [S, P, ctypes.POINTER(MoEBackwardInfo)]),
+        "moe_grouped_swiglu_save": (i32, [S, P, P, P, i64, P, i32, i64, i32, P, P, P, sz, P]),
+        "moe_scatter_grad": (i32, [S, P, P, P, P, P, P, P]),
+        "moe_grouped_down_dgrad": (i32, [S, P, P, i64, P, P, i32, i64, i32, P, P, sz, P]),
+        "moe_grouped_gate_up_dgrad": (i32, [S, P, P, P, i64, P, i32, i64, i32, P, P, sz, P]),
+        "moe_grouped_wgrad": (i32, [S, P, i64, P, i64, P, i32, i64, i32, i32, P, i64, P, sz, P]),
+        "moe_gather_grad": (i32, [S, P, P, P, P, P]),
+        "moe_layer_backward": (i32, [S, ctypes.POINTER(MoEWeights), P, P, P,
+                                     ctypes.POINTER(MoEExpertGrads), P, sz, P]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -313,6 +333,92 @@ def moe_testing_set_gemm_engine(engine: int) -> int:
 
 
 # ---------------------------------------------------------------------------
+# backward (moe_backward.h), name for name
+# ---------------------------------------------------------------------------
+def _nbytes(ws):
+    return ws.numel() * ws.element_size()
+
+
+def moe_backward_views(shape, ws) -> dict:
+    """Tensor views of the backward's grouped buffers in a train-mode workspace."""
+    info = MoEBackwardInfo()
+    _check(lib().moe_backward_views(ctypes.byref(shape), _p(ws), ctypes.byref(info)),
+           "moe_backward_views")
+    _, k = moe_topk_unpack(shape.topk_shape)
+    R, H, I = shape.tokens * k, shape.hidden, shape.moe_inter
+    act = torch.float32 if shape.dtype == MOE_F32 else torch.bfloat16
+    esz = 4 if shape.dtype == MOE_F32 else 2
+    base = ws.data_ptr()
+
+    def view(ptr, cols):
+        off = ptr - base
+        return ws[off: off + R * cols * esz].view(act).view(R, cols)
+
+    return dict(fc1=view(info.fc1, 2 * I), grad_fc2=view(info.grad_fc2, H),
+                d_fc1=view(info.d_fc1, 2 * I), dx_perm=view(info.dx_perm, H))
+
+
+def moe_grouped_swiglu_save(shape, x_perm, w_gate, w_up, expert_stride, offsets, num_groups,
+                            rows_bound, inter, h, fc1, ws, stream=None):
+    _check(lib().moe_grouped_swiglu_save(ctypes.byref(shape), _p(x_perm), _p(w_gate), _p(w_up),
+                                         expert_stride, _p(offsets), num_groups, rows_bound,
+                                         inter, _p(h), _p(fc1), _p(ws), _nbytes(ws),
+                                         _stream(stream)), "moe_grouped_swiglu_save")
+
+
+def moe_scatter_grad(shape, dy, scatter_index, topk_w, y_perm, grad_fc2, d_topk_w, stream=None):
+    _check(lib().moe_scatter_grad(ctypes.byref(shape), _p(dy), _p(scatter_index), _p(topk_w),
+                                  _p(y_perm), _p(grad_fc2), _p(d_topk_w), _stream(stream)),
+           "moe_scatter_grad")
+
+
+def moe_grouped_down_dgrad(shape, grad_fc2, w_down, expert_stride, fc1, offsets, num_groups,
+                           rows_bound, inter, d_fc1, ws, stream=None):
+    _check(lib().moe_grouped_down_dgrad(ctypes.byref(shape), _p(grad_fc2), _p(w_down),
+                                        expert_stride, _p(fc1), _p(offsets), num_groups,
+                                        rows_bound, inter, _p(d_fc1), _p(ws), _nbytes(ws),
+                                        _stream(stream)), "moe_grouped_down_dgrad")
+
+
+def moe_grouped_gate_up_dgrad(shape, d_fc1, w_gate, w_up, expert_stride, offsets, num_groups,
+                              rows_bound, inter, dx_perm, ws, stream=None):
+    _check(lib().moe_grouped_gate_up_dgrad(ctypes.byref(shape), _p(d_fc1), _p(w_gate), _p(w_up),
+                                           expert_stride, _p(offsets), num_groups, rows_bound,
+                                           inter, _p(dx_perm), _p(ws), _nbytes(ws),
+                                           _stream(stream)), "moe_grouped_gate_up_dgrad")
+
+
+def moe_grouped_wgrad(shape, a, lda, b, ldb, offsets, num_groups, rows_bound, M, N, dw,
+                      dw_stride, ws, stream=None, a_ptr=None):
+    """a_ptr: a raw device address for a (a column offset into a wider matrix)."""
+    ap = a_ptr if a_ptr is not None else _p(a)
+    _check(lib().moe_grouped_wgrad(ctypes.byref(shape), ap, lda, _p(b), ldb, _p(offsets),
+                                   num_groups, rows_bound, M, N, _p(dw), dw_stride, _p(ws),
+                                   _nbytes(ws), _stream(stream)), "moe_grouped_wgrad")
+
+
+def moe_gather_grad(shape, dx_perm, scatter_index, residual_grad, dx, stream=None):
+    _check(lib().moe_gather_grad(ctypes.byref(shape), _p(dx_perm), _p(scatter_index),
+                                 _p(residual_grad), _p(dx), _stream(stream)), "moe_gather_grad")
+
+
+def moe_layer_backward(shape, weights: MoEWeights, dy, dx, d_topk_w, grads: MoEExpertGrads, ws,
+                       stream=None):
+    _check(lib().moe_layer_backward(ctypes.byref(shape), ctypes.byref(weights), _p(dy), _p(dx),
+                                    _p(d_topk_w), ctypes.byref(grads), _p(ws), _nbytes(ws),
+                                    _stream(stream)), "moe_layer_backward")
+
+
+def grads_for(dw_gate, dw_up, dw_down) -> MoEExpertGrads:
+    """MoEExpertGrads over [E, I, H], [E, I, H], [E, H, I] tensors."""
+    g = MoEExpertGrads()
+    g.gate, g.up, g.down = _p(dw_gate), _p(dw_up), _p(dw_down)
+    g.gate_up_stride = dw_gate.shape[1] * dw_gate.shape[2]
+    g.down_stride = dw_down.shape[1] * dw_down.shape[2]
+    return g
+
+
+# ---------------------------------------------------------------------------
 # conveniences over the ABI (allocation through torch, nothing else)
 # ---------------------------------------------------------------------------
 def shape_for(wl, T: Optional[int] = None) -> MoEShape:
@@ -326,6 +432,7 @@ def shape_for(wl, T: Optional[int] = None) -> MoEShape:
     s.input_norm = int(getattr(wl, "input_norm", False))
     s.residual = int(getattr(wl, "residual", False))
     s.norm_eps = float(getattr(wl, "norm_eps", 1e-6))
+    s.train = int(getattr(wl, "train", False))
     return s
 
 
@@ -359,10 +466,12 @@ def weights_from(inputs: dict) -> MoEWeights:
 class MoELayer:
     """One layer: shape, weight table and a workspace, over caller tensors."""
 
-    def __init__(self, wl, inputs: dict, T: Optional[int] = None, device="cuda"):
+    def __init__(self, wl, inputs: dict, T: Optional[int] = None, device="cuda",
+                 train: bool = False):
         self.wl = wl
         self.inputs = inputs
         self.shape = shape_for(wl, T if T is not None else inputs["x"].shape[0])
+        self.shape.train = int(train)
         self.weights = weights_from(inputs)
         self.ws = alloc_workspace(self.shape, device)
 
@@ -371,6 +480,10 @@ class MoELayer:
             y = torch.empty_like(x)
         moe_layer_forward(self.shape, self.weights, x, routes_idx, routes_w, y, self.ws, stream)
         return y
+
+    def backward(self, dy, dx, d_topk_w, grads: MoEExpertGrads, stream=None):
+        """Gradients after a train-mode forward on this layer's workspace."""
+        moe_layer_backward(self.shape, self.weights, dy, dx, d_topk_w, grads, self.ws, stream)
 
     def views(self):
         return moe_workspace_views(self.shape, self.ws)

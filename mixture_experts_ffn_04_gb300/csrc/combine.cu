@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const T* __restrict__ y_pe
   const int64_t t = blockIdx.x;
   for (int s = threadIdx.x; s < k; s += blockDim.x) {
     rows[s] = sidx[t * k + s];
-    wt[s] = w[t * k + s];
+    wt[s] = w ? w[t * k + s] : 1.0f;
   }
   __syncthreads();
   const float g = gate ? gate[t] : 1.0f;

@@ -219,6 +219,11 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(GemmArgs a) {
         reinterpret_cast<T*>(a.out)[row * a.ldo + n] = from_f<T>(acc[i][q]);
       } else {
         reinterpret_cast<T*>(a.out)[row * a.ldo + n] = from_f<T>(silu_f(acc[i][q]) * accu[i][q]);
+        if (a.pre) {   // the pre-activations, for the backward
+          T* pre = reinterpret_cast<T*>(a.pre) + row * a.ldp;
+          pre[n] = from_f<T>(acc[i][q]);
+          pre[N + n] = from_f<T>(accu[i][q]);
+        }
       }
     }
   }

@@ -83,6 +83,8 @@ struct TcArgs {
   const bf16* gA;         // gathered A: row r of the operand is gA[gather[r]]
   const int32_t* gather;  // or NULL: A through the tensor map
   int64_t a_rows;         // rows of gA (bound on gather values)
+  bf16* pre;              // SwiGLU: also the pre-activations [rows, ldp] = [gate | up]
+  int64_t ldp;
 };
 
 // Tile -> (K split, group, m-tile, n-tile).  Within a split, tiles of one
@@ -367,7 +369,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll 1
         for (int c = 0; c < ncols && n0 + c < a.N; c += 32) {
           uint32_t gr[32];
-          uint4 packed[4];
+          uint4 packed[4], pg[4], pu[4];
           tmem_ld32(taddr + c, gr);
           if (swiglu) {
             uint32_t ur[32];
@@ -380,6 +382,19 @@ __global__ void __launch_bounds__(THREADS, 1)
               for (int e = 0; e < 8; ++e)
                 f[e] = silu_fast(__uint_as_float(gr[v * 8 + e])) * __uint_as_float(ur[v * 8 + e]);
               packed[v] = pack16(f, (const bf16*)nullptr);
+            }
+            if (a.pre) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                float fg[8], fu[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                  fg[e] = __uint_as_float(gr[v * 8 + e]);
+                  fu[e] = __uint_as_float(ur[v * 8 + e]);
+                }
+                pg[v] = pack16(fg, (const bf16*)nullptr);
+                pu[v] = pack16(fu, (const bf16*)nullptr);
+              }
             }
           } else {
             tmem_wait_ld();
@@ -404,6 +419,26 @@ __global__ void __launch_bounds__(THREADS, 1)
                   *reinterpret_cast<const uint4*>(stage + rr * OUT_ROW_BYTES + pc * 16);
           }
           __syncwarp();
+          if (swiglu && a.pre) {
+            // the gate and up pre-activations, rounded once, for the backward
+#pragma unroll 1
+            for (int part = 0; part < 2; ++part) {
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                reinterpret_cast<uint4*>(my_row)[v] = part ? pu[v] : pg[v];
+              __syncwarp();
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int p = lane + 32 * i;
+                const int rr = p >> 2, pc = p & 3;
+                const int n = n0 + c + pc * 8;
+                if (rr < nvalid && n < a.N)
+                  *reinterpret_cast<uint4*>(a.pre + (row0 + rr) * a.ldp + part * a.N + n) =
+                      *reinterpret_cast<const uint4*>(stage + rr * OUT_ROW_BYTES + pc * 16);
+              }
+              __syncwarp();
+            }
+          }
         }
       } else {
         // fp32 rows (router logits): ldo and split_stride are multiples of 4
@@ -569,6 +604,9 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   t.gA = reinterpret_cast<const bf16*>(a.A);
   t.gather = a.gather;
   t.a_rows = a.a_rows;
+  t.pre = reinterpret_cast<bf16*>(a.pre);
+  t.ldp = a.ldp;
+  if (t.pre && (a.mode != kSwiGLU || (a.ldp % 8) != 0)) return cudaErrorInvalidValue;
   int64_t mt_bound = a.offsets ? (a.rows_bound + BM - 1) / BM + a.G : (a.single_rows + BM - 1) / BM;
   if (a.offsets && mt_bound > a.rows_bound) mt_bound = a.rows_bound;  // >= 1 row per tile
   const int64_t tiles_bound = mt_bound * t.NT * t.ksplit;

@@ -21,6 +21,7 @@ struct Shape {
   int ldl;     // leading dimension of the fp32 logits buffer
   int input_norm, residual;
   double norm_eps;
+  int train;   // the forward keeps what the backward needs (fc1 rows)
 };
 
 // Decode and validate; on failure returns the status and sets *why.
@@ -33,7 +34,10 @@ struct Layout {
   int nchunks, tokens_per_chunk;
   // layer-forward intermediates
   size_t x_norm, topk_idx, topk_w, gate, counts, offsets, sidx, row_token, x_perm, h, y_perm,
-      sh_h, sh_out, total;
+      sh_h, sh_out,
+      // training (shape.train): the gate/up pre-activations the forward keeps,
+      // and the backward's grouped intermediates
+      fc1, g_fc2, d_fc1, dx_perm, total;
 };
 Layout layout_for(const Shape& s);
 
@@ -70,6 +74,8 @@ struct GemmArgs {
   int64_t split_stride = 0;  // written split_stride floats apart
   const int32_t* gather = nullptr;  // non-NULL: row r of the operand is A[gather[r]]
   int64_t a_rows = 0;               // rows of A when gathered (bound on gather values)
+  void* pre = nullptr;              // SwiGLU: also store the pre-activations,
+  int64_t ldp = 0;                  // gate at pre[r, n], up at pre[r, N + n]
 };
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t st);
@@ -78,6 +84,43 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_tc2(const GemmArgs& a, cudaStream_t st);   // SM pairs
 cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_schedule(const GemmArgs& a, int bm, cudaStream_t st);
+
+// Backward grouped GEMMs (gemm_bwd.cu on the tensor cores, gemm_bwd_simt.cu
+// on the CUDA cores).
+enum BwdKind { kBwdDgrad = 0, kBwdDgradSwiGLU = 1, kBwdWgrad = 2 };
+struct BwdGemmArgs {
+  int kind;
+  int dtype;
+  // dgrad: A [rows, lda] with K0 + K1 columns used; group g's weights
+  //        B0 + g * bstride ([K0, N]) and B1 + g * bstride ([K1, N]).
+  // wgrad: A [rows, lda] (M columns used), B0 [rows, ldb] (N columns used);
+  //        group g's output [M, N] at out + g * ostride.
+  const void* A;
+  int64_t lda;
+  const void* B0;
+  const void* B1;
+  int64_t bstride, ldb;
+  int M, N, K0, K1;
+  const int32_t* offsets;  // [G + 1]
+  int G;
+  int64_t rows_bound;
+  void* out;
+  int64_t ldo, ostride;
+  const void* pre;         // kBwdDgradSwiGLU: [rows, ldp] = [a | b], N each
+  int64_t ldp;
+  int32_t* sched;          // [G + 1] scratch (dgrad)
+  uint32_t* flags;
+};
+bool bwd_gemm_tc_ok(const BwdGemmArgs& a);
+cudaError_t launch_bwd_gemm(const BwdGemmArgs& a, cudaStream_t st);
+cudaError_t launch_bwd_gemm_tc(const BwdGemmArgs& a, cudaStream_t st);
+cudaError_t launch_bwd_gemm_simt(const BwdGemmArgs& a, cudaStream_t st);
+
+// grad_fc2[scatter_index[t, s]] = topk_w[t, s] * dy[t];
+// d_topk_w[t, s] = <dy[t], y_perm[scatter_index[t, s]]> (backward.cu).
+cudaError_t launch_scatter_grad(const Shape& s, const void* dy, const int32_t* scatter_index,
+                                const float* topk_w, const void* y_perm, void* grad_fc2,
+                                float* d_topk_w, cudaStream_t st);
 
 // logits: nsplit partial sums of [T, ldl] floats, T * ldl apart.
 // redecided: count of tokens whose near tie was re-decided exactly.
@@ -106,6 +149,7 @@ cudaError_t launch_permute_scratch(const Shape& s, int nchunks, int tpc, int32_t
 // Record why the current host call failed (read back by moe_last_error).
 void set_error_message(const char* why);
 
+// topk_w == NULL: every slot weighs 1 (the backward's gather).
 // shared_part/nsplit_sh: instead of shared_out, nsplit_sh fp32 partial sums
 // of the shared MLP output ([T, H] each, T*H apart), added in order.
 cudaError_t launch_combine(const Shape& s, const void* y_perm, const int32_t* scatter_index,

@@ -78,10 +78,15 @@ moe_status decode_shape(const moe_shape* s, Shape* o, const char** why) {
     *why = "norm_eps must be finite and >= 0";
     return MOE_ERR_INVALID_ARG;
   }
+  if (s->train != 0 && s->train != 1) {
+    *why = "train must be 0 or 1";
+    return MOE_ERR_INVALID_ARG;
+  }
   o->T = s->tokens;
   o->input_norm = s->input_norm;
   o->residual = s->residual;
   o->norm_eps = s->norm_eps;
+  o->train = s->train;
   o->H = s->hidden;
   o->I = s->moe_inter;
   o->I_sh = s->shared_inter;
@@ -134,6 +139,11 @@ Layout layout_for(const Shape& s) {
   if (s.I_sh && s.T <= kSharedSplitMaxT)
     sh_bytes = std::max(sh_bytes, (size_t)kMaxSplit * T * (size_t)s.H * 4);
   L.sh_out = off; off += align256(sh_bytes);
+  const size_t rows = s.train ? T * k : 0;
+  L.fc1 = off; off += align256(rows * 2 * (size_t)s.I * s.esize);
+  L.g_fc2 = off; off += align256(rows * (size_t)s.H * s.esize);
+  L.d_fc1 = off; off += align256(rows * 2 * (size_t)s.I * s.esize);
+  L.dx_perm = off; off += align256(rows * (size_t)s.H * s.esize);
   L.total = off;
   return L;
 }
@@ -143,7 +153,9 @@ Layout layout_for(const Shape& s) {
 static int engine_for(const GemmArgs& a) {
   const int ov = gemm_path_override();
   const int64_t rows = a.offsets ? a.rows_bound : a.single_rows;
-  if (a.dtype == MOE_F32) return ov == 3 ? 3 : 1;
+  if (a.dtype == MOE_F32) return ov == 3 && a.pre == nullptr ? 3 : 1;
+  // the pre-activation store exists on the one-SM tensor-core and CUDA-core engines
+  if (a.pre) return ov == 1 ? 1 : 2;
   const bool pair_ok = a.mode != kStoreF32 && a.ksplit == 1 && a.gather == nullptr;
   if (ov == 4) return pair_ok ? 4 : 2;
   if (ov >= 1 && ov <= 3) return ov;
@@ -531,6 +543,10 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
   if (direct) {
     use_idx = routes_idx;
     use_w = routes_w;
+    if (s.train) {   // the backward reads the routes from the workspace
+      CHECK_CUDA(cudaMemcpyAsync(idx, routes_idx, (size_t)s.T * s.k * 4, cudaMemcpyDeviceToDevice, st));
+      CHECK_CUDA(cudaMemcpyAsync(tw, routes_w, (size_t)s.T * s.k * 4, cudaMemcpyDeviceToDevice, st));
+    }
   } else {
     moe_status r = do_route(s, L, w, xin, W->router, idx, tw, gate, st);
     if (r != MOE_OK) return r;
@@ -567,7 +583,12 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
   a.K = s.H;
   a.out = h;
   a.ldo = s.I;
+  if (s.train) {   // the backward's SwiGLU derivative needs a and b
+    a.pre = w + L.fc1;
+    a.ldp = 2 * (int64_t)s.I;
+  }
   CHECK_CUDA(launch_grouped_gemm(a, st));
+  a.pre = nullptr;
   STAGE_EVENT(MOE_STAGE_DOWN);
   a.mode = kStoreAct;
   a.A = h;

@@ -180,6 +180,11 @@ def _routes(w: Workload, seed: int):
     return torch.from_numpy(idx), torch.from_numpy(wt)
 
 
+def make_output_grad(w: Workload, seed: int = 0, device="cpu") -> torch.Tensor:
+    """dy = dL/dy [T, H] for the backward: standard normal in the activation type."""
+    return _normal(seed, "dy", (w.T, w.H), 1.0, w.torch_dtype, device)
+
+
 def make_inputs(w: Workload, seed: int = 0, device="cpu", with_experts: bool = True):
     """All input tensors of one workload, drawn on ``device``.
 

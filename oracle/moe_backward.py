@@ -114,3 +114,17 @@ def backward(x, idx, w, w_gate, w_up, w_down, dy):
         dXe = dA @ Wg[e] + dB @ Wu[e]                  # dgrad through gate/up
         np.add.at(dx, tok, dXe)                        # gather to the tokens
     return dict(dx=dx, dw=dw, dw_gate=dWg, dw_up=dWu, dw_down=dWd)
+
+
+def group_weight_grads(a, b, offsets) -> np.ndarray:
+    """The weight-gradient grouped GEMM on its own ("Fused MoE Kernel Notes",
+    group_gemm_same_mn): dW_g = sum over rows r of group g of a[r]^T b[r],
+    i.e. a_g^T b_g, for a [rows, M], b [rows, N]; [G, M, N] float64."""
+    A, B = _f64(a), _f64(b)
+    off = np.asarray(offsets, dtype=np.int64)
+    G = off.size - 1
+    out = np.zeros((G, A.shape[1], B.shape[1]))
+    for g in range(G):
+        r0, r1 = off[g], off[g + 1]
+        out[g] = A[r0:r1].T @ B[r0:r1]
+    return out

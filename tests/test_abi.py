@@ -21,7 +21,7 @@ def m():
 
 def _declared_functions():
     names = []
-    for h in ("moe.h", "moe_testing.h"):
+    for h in ("moe.h", "moe_testing.h", "moe_backward.h"):
         src = open(os.path.join(ROOT, "include", h)).read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
         names += re.findall(r"^[A-Za-z_][\w \*]*?\b(moe_\w+)\s*\(", src, flags=re.M)
@@ -142,3 +142,58 @@ def test_workspace_layout_scales(m):
     inter = 2 * T * k * H * 2 + T * k * I * 2     # x_perm, y_perm and h
     assert inter <= m.moe_workspace_bytes(s) <= inter * 1.2
     assert m.moe_scratch_bytes(s) < 128 << 20   # split-K router partials dominate
+
+
+def test_backward_validation(m):
+    """The backward's host checks (include/moe_backward.h), no GPU needed."""
+    lib = m.lib()
+    P = ctypes.c_void_p
+    w = m.MoEWeights()
+    w.gate = w.up = w.down = 4096
+    w.gate_up_stride = w.down_stride = 128 * 256
+    g = m.MoEExpertGrads()
+    g.gate = g.up = g.down = 8192
+    g.gate_up_stride = g.down_stride = 128 * 256
+    s = _shape(m)
+    need = m.moe_workspace_bytes(s)
+    # the backward needs a train-mode workspace
+    st = lib.moe_layer_backward(ctypes.byref(s), ctypes.byref(w), P(4096), P(4096), P(4096),
+                                ctypes.byref(g), P(4096), need, None)
+    assert st == m.MOE_ERR_INVALID_ARG and "train" in m.moe_last_error()
+    info = m.MoEBackwardInfo()
+    assert lib.moe_backward_views(ctypes.byref(s), P(4096), ctypes.byref(info)) == m.MOE_ERR_INVALID_ARG
+    st_ = _shape(m, train=1)
+    need_t = m.moe_workspace_bytes(st_)
+    R, H, I = 64 * 2, 256, 128
+    assert need_t - need >= 2 * (R * 2 * I * 2) + 2 * (R * H * 2)   # fc1, d_fc1, grad_fc2, dx_perm
+    assert lib.moe_backward_views(ctypes.byref(st_), P(4096), ctypes.byref(info)) == m.MOE_OK
+    assert info.fc1 >= 4096 + m.moe_scratch_bytes(st_)
+    # shapes whose dense parts the op does not differentiate
+    for kw, frag in ((dict(shared_inter=256), "shared"), (dict(input_norm=1), "RMSNorm")):
+        sx = _shape(m, train=1, **kw)
+        st = lib.moe_layer_backward(ctypes.byref(sx), ctypes.byref(w), P(4096), P(4096), P(4096),
+                                    ctypes.byref(g), P(4096), m.moe_workspace_bytes(sx), None)
+        assert st == m.MOE_ERR_UNSUPPORTED and frag in m.moe_last_error(), m.moe_last_error()
+    # workspace too small; gradient stride smaller than one expert
+    st = lib.moe_layer_backward(ctypes.byref(st_), ctypes.byref(w), P(4096), P(4096), P(4096),
+                                ctypes.byref(g), P(4096), need_t - 1, None)
+    assert st == m.MOE_ERR_WORKSPACE
+    g.down_stride = 100
+    st = lib.moe_layer_backward(ctypes.byref(st_), ctypes.byref(w), P(4096), P(4096), P(4096),
+                                ctypes.byref(g), P(4096), need_t, None)
+    assert st == m.MOE_ERR_INVALID_ARG and "stride" in m.moe_last_error()
+    # grouped calls: bad sizes and misaligned operands
+    st = lib.moe_grouped_wgrad(ctypes.byref(s), P(4096), 100, P(4096), 128, P(4096), 8, 128,
+                               128, 128, P(4096), 128 * 128, P(4096), 1 << 30, None)
+    assert st == m.MOE_ERR_INVALID_ARG and "lda" in m.moe_last_error()
+    st = lib.moe_grouped_down_dgrad(ctypes.byref(s), P(4098), P(4096), 32768, P(4096), P(4096),
+                                    8, 128, 128, P(4096), P(4096), 1 << 30, None)
+    assert st == m.MOE_ERR_INVALID_ARG
+    st = lib.moe_grouped_gate_up_dgrad(ctypes.byref(s), P(4096), P(4096), P(4096), 0, P(4096),
+                                       8, 128, 128, P(4096), P(4096), 1 << 30, None)
+    assert st == m.MOE_ERR_INVALID_ARG and "expert_stride" in m.moe_last_error()
+    st = lib.moe_scatter_grad(ctypes.byref(s), P(4096), None, P(4096), P(4096), P(4096),
+                              P(4096), None)
+    assert st == m.MOE_ERR_INVALID_ARG
+    s_bad = _shape(m, train=2)
+    assert m.moe_workspace_bytes(s_bad) == 0

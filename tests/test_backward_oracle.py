@@ -147,8 +147,28 @@ def check_unused_expert_has_zero_grads(B=MB):
         assert np.any(gr[key][1] != 0.0)
 
 
+def check_group_weight_grads_bruteforce(B=MB):
+    """The grouped weight-gradient GEMM by explicit triple loops on tiny
+    inputs, with an empty group and a group of one row."""
+    rng = np.random.default_rng(4)
+    a = rng.standard_normal((7, 3))
+    b = rng.standard_normal((7, 2))
+    offsets = [0, 3, 3, 4, 7]
+    got = B.group_weight_grads(a, b, offsets)
+    assert got.shape == (4, 3, 2)
+    for g in range(4):
+        for i in range(3):
+            for j in range(2):
+                ref = 0.0
+                for r in range(offsets[g], offsets[g + 1]):
+                    ref += a[r, i] * b[r, j]
+                assert abs(got[g, i, j] - ref) <= 1e-14 * max(1.0, abs(ref)), (g, i, j)
+    assert np.all(got[1] == 0.0)
+
+
 CHECKS = [check_central_differences, check_forward_matches_c_oracle, check_homogeneity,
-          check_symbolic, check_duplicate_routes, check_unused_expert_has_zero_grads]
+          check_symbolic, check_duplicate_routes, check_unused_expert_has_zero_grads,
+          check_group_weight_grads_bruteforce]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=[c.__name__ for c in CHECKS])
@@ -171,6 +191,8 @@ MUTANTS = [
      "dw[tok, slot] = np.sum(dY[tok][:, :Hh.shape[1]] * Hh, axis=1)"),
     ("gather keeps only the last slot", "np.add.at(dx, tok, dXe)", "dx[tok] = dXe"),
     ("gate weight gradient uses the up input", "dWg[e] = dA.T @ Xe", "dWg[e] = dB.T @ Xe"),
+    ("weight-gradient groups off by one row", "r0, r1 = off[g], off[g + 1]",
+     "r0, r1 = off[g], off[g + 1] + (1 if g + 1 < G else 0)"),
 ]
 
 
