@@ -169,6 +169,7 @@ BwdGemmArgs bwd_args(const Shape& s, const Layout& L, char* w, int kind, int32_t
   b.ldp = 0;
   b.sched = reinterpret_cast<int32_t*>(w + (G > 1 ? L.sched_routed : L.sched_shared));
   b.flags = reinterpret_cast<uint32_t*>(w + L.flags);
+  b.tmaps = w + L.tmaps;
   return b;
 }
 

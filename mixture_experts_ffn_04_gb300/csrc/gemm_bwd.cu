@@ -17,16 +17,24 @@
 //    its own K = the group's row count:
 //      dW_g[m, n] = sum over rows r of group g of A[r, m] * B[r, n]
 //    Both operands are read in their stored [rows, M] / [rows, N] layouts
-//    (MN-major).  A group's last k-block reaches into the next group's rows:
-//    those rows are zeroed in shared memory before the MMA reads them.  A
-//    group with no rows gets a zero gradient.
+//    (MN-major), through tensor maps of the group's own rows: a small kernel
+//    writes, per group, copies of the two maps whose base is the group's
+//    first row and whose row extent is the group's size (tensormap.replace),
+//    so the TMA zero-fills what a group's last k-block reaches past its end
+//    and no row of the next group enters the sum.  A group with no rows gets
+//    a zero gradient.
 //
 // Pipeline (one CTA per SM, persistent over the tile list): warp 0 lane 0
 // issues the TMA loads of a stage (A and B on one "full" barrier), warp 1
-// owns TMEM, zeroes tail rows (wgrad) and issues tcgen05.mma (M = 128, N =
-// 256, K = 16) into one of two 256-column fp32 accumulators; warps 2-5 drain
-// the other accumulator (tcgen05.ld), finish the values and store them
-// through a shared-memory staging slice as whole-row 16-byte pieces.
+// owns TMEM and issues tcgen05.mma (M = 128, N =
+// 256, K = 16) into one of two 256-column fp32 accumulators; warps 2-9 drain
+// the other accumulator (tcgen05.ld; two warps per 32-lane quarter, one per
+// half of the columns), finish the values and store them through a
+// shared-memory staging slice as whole-row 16-byte pieces.  The weight
+// gradient's tiles carry few k-blocks (a group's rows), so its epilogue has
+// to keep pace with about one tile of MMAs: hence eight epilogue warps, the
+// group offsets staged in shared memory, and a last block that issues only
+// the K = 16 steps holding rows of the group.
 // MN-major operands sit in shared memory as 64-element-wide boxes, each box
 // 64 k-rows of 128 bytes with the 128-byte swizzle; an MMA's K = 16 slice is
 // two 8-row core groups of every box.
@@ -57,14 +65,15 @@ constexpr int B_BYTES = BN * BK * 2;              // 32 KB
 constexpr int BOX_BYTES = 64 * BK * 2;            // one 64-wide MN box: 8 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int RING_BYTES = S * STAGE_BYTES;
-constexpr int THREADS = 192;                      // warps 0-5
+constexpr int THREADS = 320;                      // warps 0-9
+constexpr int EPI_WARPS = 8;                      // warps 2-9: two per TMEM lane quarter
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
 constexpr int MAX_SMEM_G = 1024;
 constexpr int SCHED_BYTES = (MAX_SMEM_G + 1) * 4;
 constexpr int OUT_ROW_BYTES = 80;
 constexpr int OUT_WARP_BYTES = 32 * OUT_ROW_BYTES;
-constexpr int OUT_BYTES = 4 * OUT_WARP_BYTES;
+constexpr int OUT_BYTES = EPI_WARPS * OUT_WARP_BYTES;
 constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES + OUT_BYTES + SCHED_BYTES;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
 static_assert((2 * S + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
@@ -102,13 +111,20 @@ struct Args {
   const bf16* pre;        // dgrad + SwiGLU: [rows, ldp] = [a | b]
   int64_t ldp;
   uint32_t* flags;
+  const CUtensorMap* tmaps;   // wgrad: per group g, A's map at 2g, B's at 2g + 1
+  // MN-major operands whose width is a multiple of 64 are mapped with the
+  // 64-wide blocks as an outer dimension, so one TMA box brings every block
+  // of a stage (wgrad: A and B; dgrad: B); otherwise one box per block
+  int a_wide, b_wide;
 };
 
 // Rows of group g, 0 when the offsets are inconsistent (same answer in every
-// role, so all of them skip the same tiles).
-__device__ __forceinline__ int64_t group_rows(const Args& a, int g, int64_t& beg) {
-  beg = a.offsets[g];
-  const int64_t end = a.offsets[g + 1];
+// role, so all of them skip the same tiles).  off: the offsets, staged in
+// shared memory when they fit.
+__device__ __forceinline__ int64_t group_rows(const Args& a, const int32_t* off, int g,
+                                              int64_t& beg) {
+  beg = off[g];
+  const int64_t end = off[g + 1];
   if (beg < 0 || end < beg || end > a.rows_bound) return 0;
   return end - beg;
 }
@@ -218,7 +234,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull(b), 1);
-      mbar_init(tempty(b), 128);
+      mbar_init(tempty(b), 32 * EPI_WARPS);
     }
     mbar_init(final_bar, 1);
     *abort_flag = 0;
@@ -230,6 +246,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     tmem_relinquish();
   }
   if (warp == 2 && !wgrad && a.sched == nullptr) build_schedule(a, s_sched, lane);
+  if (warp == 3 && wgrad && a.G <= MAX_SMEM_G)
+    for (int g = lane; g <= a.G; g += 32) s_sched[g] = a.offsets[g];
   if (warp == 2 && wgrad && blockIdx.x == 0) {
     // offsets must rise from 0 to at most the row bound; a group whose own
     // range is invalid is skipped (group_rows), and the flag says so
@@ -242,6 +260,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int32_t* sched = a.sched ? a.sched : s_sched;
+  const int32_t* off = wgrad && a.G <= MAX_SMEM_G ? s_sched : a.offsets;
   const int64_t total =
       wgrad ? (int64_t)a.G * a.MT * a.NT : (int64_t)sched[a.G] * a.NT;
 
@@ -249,7 +268,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto tile_kblocks = [&](int64_t tile, int& g, int& mt, int& nt, int64_t& r0) -> int {
     if (wgrad) {
       decode_wgrad(a, tile, g, mt, nt);
-      const int64_t rows = group_rows(a, g, r0);
+      const int64_t rows = group_rows(a, off, g, r0);
       return (int)((rows + BK - 1) / BK);
     }
     decode_dgrad(a, sched, tile, g, mt, nt);
@@ -263,32 +282,52 @@ __global__ void __launch_bounds__(THREADS, 1)
       int s = 0;
       uint32_t ph = 0, issued = 0, par = 0;
       bool ok = true;
+      int gmap = -1;   // wgrad: the group whose maps were last acquired
       for (int64_t tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         int g, mt, nt;
         int64_t r0;
         const int nkb = tile_kblocks(tile, g, mt, nt, r0);
+        const CUtensorMap* gA = &tmA;
+        const CUtensorMap* gB = &tmB0;
+        if (wgrad && nkb > 0) {
+          gA = a.tmaps + 2 * g;
+          gB = gA + 1;
+          if (g != gmap) {   // maps written by the preceding kernel
+            asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(
+                             reinterpret_cast<uint64_t>(gA))
+                         : "memory");
+            asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(
+                             reinterpret_cast<uint64_t>(gB))
+                         : "memory");
+            gmap = g;
+          }
+        }
         const int m0 = mt * BM, n0 = nt * BN;
         // boxes wholly past M or N are not loaded: they only feed outputs
         // the epilogue drops
         const int na = wgrad ? (m0 + 64 < a.M ? 2 : 1) : 1;
         int nb = (a.N - n0 + 63) / 64;
         if (nb > 4) nb = 4;
-        const uint32_t bytes = (uint32_t)(wgrad ? na * BOX_BYTES : A_BYTES) + nb * BOX_BYTES;
+        const uint32_t bytes = (uint32_t)(wgrad && !a.a_wide ? na * BOX_BYTES : A_BYTES) +
+                               (uint32_t)(a.b_wide ? B_BYTES : nb * BOX_BYTES);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(empty(s), ph ^ 1u, abort_flag)) { ok = false; break; }
           const uint32_t sa = ring + s * STAGE_BYTES, sb = sa + A_BYTES;
           mbar_expect_tx(full(s), bytes);
           if (wgrad) {
-            const int r = (int)(r0 + (int64_t)kb * BK);
-            for (int j = 0; j < na; ++j) tma_load_2d(sa + j * BOX_BYTES, &tmA, m0 + 64 * j, r, full(s));
-            for (int j = 0; j < nb; ++j) tma_load_2d(sb + j * BOX_BYTES, &tmB0, n0 + 64 * j, r, full(s));
+            const int r = kb * BK;   // row within the group's maps
+            if (a.a_wide) tma_load_3d(sa, gA, 0, r, m0 / 64, full(s));
+            else for (int j = 0; j < na; ++j) tma_load_2d(sa + j * BOX_BYTES, gA, m0 + 64 * j, r, full(s));
+            if (a.b_wide) tma_load_3d(sb, gB, 0, r, n0 / 64, full(s));
+            else for (int j = 0; j < nb; ++j) tma_load_2d(sb + j * BOX_BYTES, gB, n0 + 64 * j, r, full(s));
           } else {
             const bool seg1 = kb >= a.KB0;
             const int kk = seg1 ? kb - a.KB0 : kb;
             const int acol = seg1 ? a.K0 + kk * BK : kb * BK;
             tma_load_2d(sa, &tmA, acol, (int)r0, full(s));
             const CUtensorMap* mb = seg1 ? &tmB1 : &tmB0;
-            for (int j = 0; j < nb; ++j) tma_load_3d(sb + j * BOX_BYTES, mb, n0 + 64 * j, kk * BK, g, full(s));
+            if (a.b_wide) tma_load_4d(sb, mb, 0, kk * BK, n0 / 64, g, full(s));
+            else for (int j = 0; j < nb; ++j) tma_load_3d(sb + j * BOX_BYTES, mb, n0 + 64 * j, kk * BK, g, full(s));
           }
           issued |= 1u << s;
           par = (par & ~(1u << s)) | (ph << s);
@@ -301,7 +340,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer (lane 0); the warp zeroes tail rows ----------
+    // ---------------- MMA issuer (lane 0) ----------------
     int s = 0, acc = 0;
     uint32_t ph = 0, aph = 0;
     bool ok = true;
@@ -312,7 +351,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int nkb = tile_kblocks(tile, g, mt, nt, r0);
       if (nkb == 0) continue;   // empty group: the epilogue writes zeros
       int64_t rows = 0;
-      if (wgrad) rows = group_rows(a, g, r0);
+      if (wgrad) rows = group_rows(a, off, g, r0);
       int w = 1;
       if (lane == 0) w = mbar_wait(tempty(acc), aph ^ 1u, abort_flag) ? 1 : 0;
       if (!__shfl_sync(0xffffffffu, w, 0)) break;
@@ -324,25 +363,14 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t sa = ring + s * STAGE_BYTES, sb = sa + A_BYTES;
         const int64_t left = rows - (int64_t)kb * BK;
         const int valid = wgrad && left < BK ? (int)left : BK;
-        if (valid < BK) {
-          // rows valid..63 of every box belong to the next group: zero them
-          // (a k-row is one whole 128-byte line; the swizzle only permutes
-          // the 16-byte pieces inside it)
-          unsigned char* base = smem + (sa - ring);
-          const int lines = BK - valid;
-          for (int i = lane; i < lines * 6 * 8; i += 32) {
-            const int box = i / (lines * 8), rem = i % (lines * 8);
-            const int line = valid + rem / 8, piece = rem % 8;
-            unsigned char* boxp = box < 2 ? base + box * BOX_BYTES : base + A_BYTES + (box - 2) * BOX_BYTES;
-            *reinterpret_cast<uint4*>(boxp + line * 128 + piece * 16) = make_uint4(0u, 0u, 0u, 0u);
-          }
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-        }
+        // K = 16 steps of this block that hold rows of the group (rows past
+        // the group's end arrive as zeros; later steps are not issued)
+        const int ksteps = (valid + 15) / 16;
         if (lane == 0) {
           tc_fence_after();
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
+            if (k >= ksteps) break;
             const uint64_t ad = wgrad ? sw128_mn_desc(sa + k * 2048, BOX_BYTES) : sw128_desc(sa + k * 32);
             const uint64_t bd = sw128_mn_desc(sb + k * 2048, BOX_BYTES);
             tc_mma(d, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
@@ -362,8 +390,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait_quiet(final_bar, 0);
     }
   } else {
-    // ---------------- epilogue (warps 2..5) ----------------
-    const int q = warp & 3;   // TMEM lanes 32q .. 32q+31
+    // ---------------- epilogue (warps 2..9) ----------------
+    // warps w and w + 4 read the same TMEM lanes (32q .. 32q+31, q = w & 3)
+    // and split the 256 accumulator columns into halves
+    const int q = warp & 3;
+    const int c_lo = ((warp - 2) / 4) * (BN / 2), c_hi = c_lo + BN / 2;
     unsigned char* stage = s_out + (warp - 2) * OUT_WARP_BYTES;
     int acc = 0;
     uint32_t aph = 0;
@@ -392,18 +423,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         // a group without rows has a zero weight gradient
         const uint4 z[4] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0),
                             make_uint4(0, 0, 0, 0)};
-        for (int c = 0; c < BN && n0 + c < a.N; c += 32)
+        for (int c = c_lo; c < c_hi && n0 + c < a.N; c += 32)
           store_chunk(stage, lane, z, nvalid, n0 + c, a.N, row_ptr);
         continue;
       }
       if (!__all_sync(0xffffffffu, mbar_wait(tfull(acc), aph, abort_flag))) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * BN;
-#pragma unroll 1
-      for (int c = 0; c < BN && n0 + c < a.N; c += 32) {
-        uint32_t v[32];
-        tmem_ld32(taddr + c, v);
-        tmem_wait_ld();
+      // finish 32 accumulator columns (c .. c+31 of the tile) and store them
+      auto finish = [&](const uint32_t (&v)[32], int c) {
         const int n = n0 + c;
         if (a.kind == kBwdDgradSwiGLU) {
           // dh -> da = dh * b * silu'(a), db = dh * silu(a) with the saved
@@ -447,6 +475,17 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           store_chunk(stage, lane, pk, nvalid, n, a.N, row_ptr);
         }
+      };
+      // two 32-column TMEM loads in flight per wait
+#pragma unroll 1
+      for (int c = c_lo; c < c_hi && n0 + c < a.N; c += 64) {
+        uint32_t v0[32], v1[32];
+        const bool two = c + 32 < c_hi && n0 + c + 32 < a.N;
+        tmem_ld32(taddr + c, v0);
+        if (two) tmem_ld32(taddr + c + 32, v1);
+        tmem_wait_ld();
+        finish(v0, c);
+        if (two) finish(v1, c + 32);
       }
       tc_fence_before();
       mbar_arrive(tempty(acc));
@@ -464,6 +503,61 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0 && *abort_flag) set_flag(a.flags, kFlagTimeout);
 }
 
+// Per-group copies of the weight gradient's two operand maps: group g's maps
+// start at its first row and span its rows (at least one, so the map stays
+// valid for a group without rows, whose tiles load nothing).  One warp per
+// group: copy the base map to shared memory, replace the base address and the
+// row extent (dimension 1), and copy it out with the proxy fence that makes
+// it visible to the TMA unit.
+__global__ void __launch_bounds__(32) wgrad_maps_kernel(const __grid_constant__ CUtensorMap baseA,
+                                                        const __grid_constant__ CUtensorMap baseB,
+                                                        CUtensorMap* maps, const int32_t* offsets,
+                                                        int G, int64_t rows_bound,
+                                                        const char* A, int64_t lda_bytes,
+                                                        const char* B, int64_t ldb_bytes) {
+  __shared__ __align__(128) CUtensorMap sm[2];
+  const int lane = threadIdx.x;
+  for (int g = blockIdx.x; g < G; g += gridDim.x) {
+    int64_t beg = offsets[g], end = offsets[g + 1];
+    if (beg < 0 || end < beg || end > rows_bound) beg = end = 0;
+    const uint32_t rows = end > beg ? (uint32_t)(end - beg) : 1u;
+    if (lane < 8) {
+      reinterpret_cast<uint4*>(&sm[0])[lane] = reinterpret_cast<const uint4*>(&baseA)[lane];
+      reinterpret_cast<uint4*>(&sm[1])[lane] = reinterpret_cast<const uint4*>(&baseB)[lane];
+    }
+    __syncwarp();
+    if (lane == 0) {
+      const uint32_t s0 = smem_u32(&sm[0]), s1 = smem_u32(&sm[1]);
+      const uint64_t pa = reinterpret_cast<uint64_t>(A + beg * lda_bytes);
+      const uint64_t pb = reinterpret_cast<uint64_t>(B + beg * ldb_bytes);
+      asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(s0),
+                   "l"(pa)
+                   : "memory");
+      asm volatile("tensormap.replace.tile.global_dim.shared::cta.b1024.b32 [%0], 1, %1;" ::"r"(s0),
+                   "r"(rows)
+                   : "memory");
+      asm volatile("tensormap.replace.tile.global_address.shared::cta.b1024.b64 [%0], %1;" ::"r"(s1),
+                   "l"(pb)
+                   : "memory");
+      asm volatile("tensormap.replace.tile.global_dim.shared::cta.b1024.b32 [%0], 1, %1;" ::"r"(s1),
+                   "r"(rows)
+                   : "memory");
+    }
+    __syncwarp();
+    asm volatile(
+        "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned"
+        " [%0], [%1], 128;" ::"l"(reinterpret_cast<uint64_t>(maps + 2 * g)),
+        "r"(smem_u32(&sm[0]))
+        : "memory");
+    asm volatile(
+        "tensormap.cp_fenceproxy.global.shared::cta.tensormap::generic.release.gpu.sync.aligned"
+        " [%0], [%1], 128;" ::"l"(reinterpret_cast<uint64_t>(maps + 2 * g + 1)),
+        "r"(smem_u32(&sm[1]))
+        : "memory");
+    __syncwarp();
+  }
+}
+
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
@@ -477,6 +571,36 @@ static bool map_rows(CUtensorMap* m, const void* ptr, int64_t rows, int64_t widt
   cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
   cuuint32_t es[2] = {1, 1};
   return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map {64, rows, width / 64} over the same rows: the 64-wide column blocks
+// as the outer dimension, box 64 x 64 rows x `blocks`, so one box lands as
+// `blocks` consecutive [64 rows][64] tiles (width a multiple of 64).
+static bool map_rows_wide(CUtensorMap* m, const void* ptr, int64_t rows, int64_t width, int64_t ld,
+                          int blocks) {
+  cuuint64_t dims[3] = {64, (cuuint64_t)rows, (cuuint64_t)(width / 64)};
+  cuuint64_t strides[2] = {(cuuint64_t)ld * 2, 128};
+  cuuint32_t box[3] = {64, 64, (cuuint32_t)blocks};
+  cuuint32_t es[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                     box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 4-D map {64, K, N / 64, G} over G weight matrices stored [K, N], box
+// 64 x 64 x 4 x 1: a stage's four 64-wide blocks in one box (N a multiple of 64).
+static bool map_weights_kn_wide(CUtensorMap* m, const void* ptr, int N, int K, int G,
+                                int64_t gstride) {
+  if (G == 1 && gstride == 0) gstride = (int64_t)N * K;
+  cuuint64_t dims[4] = {64, (cuuint64_t)K, (cuuint64_t)(N / 64), (cuuint64_t)G};
+  cuuint64_t strides[3] = {(cuuint64_t)N * 2, 128, (cuuint64_t)gstride * 2};
+  cuuint32_t box[4] = {64, 64, 4, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(ptr), dims, strides,
                      box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -528,6 +652,7 @@ cudaError_t launch_bwd_gemm_tc(const BwdGemmArgs& a, cudaStream_t st) {
   t.flags = a.flags;
   t.NT = (a.N + BN - 1) / BN;
   t.sched = nullptr;
+  t.tmaps = nullptr;
   CUtensorMap mA, mB0, mB1;
   int64_t tiles_bound;
   if (a.kind == kBwdWgrad) {
@@ -535,10 +660,23 @@ cudaError_t launch_bwd_gemm_tc(const BwdGemmArgs& a, cudaStream_t st) {
     t.MT = (a.M + BM - 1) / BM;
     t.K0 = t.KB0 = t.KB = 0;
     const int64_t rows = a.rows_bound > 0 ? a.rows_bound : 1;
-    if (!map_rows(&mA, a.A, rows, a.M, a.lda, BK) || !map_rows(&mB0, a.B0, rows, a.N, a.ldb, BK))
+    t.a_wide = a.M % 64 == 0;
+    t.b_wide = a.N % 64 == 0;
+    if (!(t.a_wide ? map_rows_wide(&mA, a.A, rows, a.M, a.lda, BM / 64)
+                   : map_rows(&mA, a.A, rows, a.M, a.lda, BK)) ||
+        !(t.b_wide ? map_rows_wide(&mB0, a.B0, rows, a.N, a.ldb, BN / 64)
+                   : map_rows(&mB0, a.B0, rows, a.N, a.ldb, BK)))
       return cudaErrorInvalidValue;
     mB1 = mB0;
     tiles_bound = (int64_t)a.G * t.MT * t.NT;
+    if (a.tmaps == nullptr) return cudaErrorInvalidValue;
+    t.tmaps = reinterpret_cast<const CUtensorMap*>(a.tmaps);
+    const int mg = a.G < 1024 ? a.G : 1024;
+    wgrad_maps_kernel<<<mg, 32, 0, st>>>(mA, mB0, reinterpret_cast<CUtensorMap*>(a.tmaps),
+                                         a.offsets, a.G, a.rows_bound,
+                                         reinterpret_cast<const char*>(a.A), a.lda * 2,
+                                         reinterpret_cast<const char*>(a.B0), a.ldb * 2);
+    count_launch();
   } else {
     if (a.rows_bound <= 0 || a.N <= 0) return cudaSuccess;
     t.MT = 0;
@@ -558,9 +696,15 @@ cudaError_t launch_bwd_gemm_tc(const BwdGemmArgs& a, cudaStream_t st) {
       t.sched = a.sched;
     }
     if (!map_rows(&mA, a.A, a.rows_bound, a.K0 + a.K1, a.lda, BM)) return cudaErrorInvalidValue;
-    if (!map_weights_kn(&mB0, a.B0, a.N, a.K0, a.G, a.bstride)) return cudaErrorInvalidValue;
+    t.a_wide = 0;
+    t.b_wide = a.N % 64 == 0;
+    auto map_w = [&](CUtensorMap* m, const void* p, int K) {
+      return t.b_wide ? map_weights_kn_wide(m, p, a.N, K, a.G, a.bstride)
+                      : map_weights_kn(m, p, a.N, K, a.G, a.bstride);
+    };
+    if (!map_w(&mB0, a.B0, a.K0)) return cudaErrorInvalidValue;
     if (a.K1 > 0) {
-      if (!map_weights_kn(&mB1, a.B1, a.N, a.K1, a.G, a.bstride)) return cudaErrorInvalidValue;
+      if (!map_w(&mB1, a.B1, a.K1)) return cudaErrorInvalidValue;
     } else {
       mB1 = mB0;
     }

@@ -30,7 +30,7 @@ moe_status decode_shape(const moe_shape* s, Shape* out, const char** why);
 // Byte offsets of every region inside the workspace (all 256-byte aligned).
 struct Layout {
   // scratch
-  size_t flags, logits, hist, base, sched_routed, sched_shared, sched_router, scratch_end;
+  size_t flags, logits, hist, base, sched_routed, sched_shared, sched_router, tmaps, scratch_end;
   int nchunks, tokens_per_chunk;
   // layer-forward intermediates
   size_t x_norm, topk_idx, topk_w, gate, counts, offsets, sidx, row_token, x_perm, h, y_perm,
@@ -110,6 +110,8 @@ struct BwdGemmArgs {
   int64_t ldp;
   int32_t* sched;          // [G + 1] scratch (dgrad)
   uint32_t* flags;
+  void* tmaps = nullptr;   // wgrad on the tensor cores: 2 * G tensor maps
+                           // (128 bytes each, 64-byte aligned) of scratch
 };
 bool bwd_gemm_tc_ok(const BwdGemmArgs& a);
 cudaError_t launch_bwd_gemm(const BwdGemmArgs& a, cudaStream_t st);

@@ -120,6 +120,7 @@ Layout layout_for(const Shape& s) {
   L.sched_routed = off; off += align256((E + 1) * 4);
   L.sched_shared = off; off += 256;
   L.sched_router = off; off += 256;
+  L.tmaps = off; off += align256(256 * E);   // two tensor maps per group
   L.scratch_end = off;
   L.x_norm = off; off += align256(s.input_norm ? T * (size_t)s.H * s.esize : 0);
   L.topk_idx = off; off += align256(T * k * 4);
