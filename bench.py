@@ -245,6 +245,68 @@ def _make_inputs(wl, device):
     return W.make_inputs(wl, seed=0, device=device)
 
 
+def train_step(m, wl, inputs, args, flush, peaks, dist):
+    """Training step of the routed-expert op on the same inputs: the
+    train-mode forward (which also keeps the gate/up pre-activations) and the
+    backward (moe_layer_backward) with a seeded output gradient, timed with
+    CUDA events after an L2 flush; W warm-up steps, K timed.  None for
+    workloads whose backward the library does not cover (a shared expert or
+    an input RMSNorm)."""
+    if wl.I_sh or wl.input_norm:
+        return None
+    from mixture_experts_ffn_04_gb300 import workloads as W
+    layer = m.MoELayer(wl, inputs, train=True)
+    x = inputs["x"]
+    ridx, rw = inputs.get("routes_idx"), inputs.get("routes_w")
+    y = torch.empty_like(x)
+    dy = W.make_output_grad(wl, seed=0, device="cuda")
+    dx = torch.empty_like(x)
+    dtw = torch.empty((wl.T, wl.k), device="cuda")
+    E, I, H = wl.E, wl.I, wl.H
+    dwg = torch.empty((E, I, H), device="cuda", dtype=wl.torch_dtype)
+    dwu = torch.empty_like(dwg)
+    dwd = torch.empty((E, H, I), device="cuda", dtype=wl.torch_dtype)
+    grads = m.grads_for(dwg, dwu, dwd)
+    stream = torch.cuda.current_stream()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    def step():
+        flush.fill_(1)
+        ev[0].record(stream)
+        layer.forward(x, y, ridx, rw)
+        ev[1].record(stream)
+        layer.backward(dy, dx, dtw, grads)
+        ev[2].record(stream)
+        ev[2].synchronize()
+        return ev[0].elapsed_time(ev[1]), ev[1].elapsed_time(ev[2])
+
+    for _ in range(args.warmup):
+        step()
+    launches = m.moe_last_launch_count()
+    if dist is not None:
+        dist.barrier()
+    times = [step() for _ in range(args.steps)]
+    st, bits = layer.device_status()
+    if st != m.MOE_OK:
+        raise RuntimeError("device status %d (bits %#x) in the training steps" % (st, bits))
+    fwd_ms = max_over_ranks(sum(t[0] for t in times), dist) / args.steps
+    bwd_ms = max_over_ranks(sum(t[1] for t in times), dist) / args.steps
+    world = dist.get_world_size() if dist is not None else 1
+    rows = wl.T * wl.k
+    # dgrad through down 2RHI, dgrad through gate/up 4RHI, weight gradients
+    # of down 2RHI and of gate/up 4RHI
+    bwd_flops = 12.0 * rows * H * I
+    bwd_tflops = bwd_flops / (bwd_ms / 1000.0) / 1e12
+    return {
+        "what": "train-mode forward + moe_layer_backward (routed experts: dx, routing-weight "
+                "and expert weight gradients), seeded dy, L2 flushed before each step",
+        "ms_per_step": fwd_ms + bwd_ms, "forward_ms": fwd_ms, "backward_ms": bwd_ms,
+        "tokens_per_s": world * wl.T / ((fwd_ms + bwd_ms) / 1000.0),
+        "backward_tflops": bwd_tflops, "backward_frac_bf16_peak": bwd_tflops / peaks["bf16"],
+        "backward_launches": launches,
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -446,6 +508,8 @@ def main():
     layer_roof_ms = 1000.0 * max(alg["layer_flops"] / (peaks["bf16"] * 1e12),
                                  alg["layer_bytes"] / (peaks["hbm"] * 1e9))
 
+    train = train_step(m, wl, inputs, args, flush, peaks, dist)
+
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -464,6 +528,8 @@ def main():
         "wall_s_timed_region": t_wall,
         "experts_touched": alg["touched"],
     }
+    if train is not None:
+        line["train_step"] = train
     if rank == 0 and not args.no_cpu_baseline:
         from oracle import oracle as O
         O.load()
