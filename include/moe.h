@@ -173,6 +173,22 @@ moe_status moe_route(const moe_shape *shape, const void *x, const void *w_router
                      int32_t *topk_idx, float *topk_w, float *gate, void *ws,
                      size_t ws_bytes, void *stream);
 
+/* Hash-MoE routing ("Fused MoE Kernel Notes", Duplicate top-k routes: a
+ * router whose token-to-expert lookup can send two slots of a token to the
+ * same expert, as DeepSeek-V4's hash MoE does):
+ *   topk_idx[t, s] = table[token_ids[t] * k + s],  topk_w[t, s] = 1/k
+ * token_ids [T] int32, table [vocab, k] int32 (device).  Duplicates are kept:
+ * they are what the grouped GEMMs' launch bound must cover (pass the result
+ * to moe_layer_forward as direct routes).  Every slot weighs 1/k, one
+ * correctly rounded fp32 division (the notes' regression pattern uses one
+ * constant routing weight).  A token id outside [0, vocab) sets
+ * MOE_ERR_DEVICE_ROUTE on the device and routes that token's slots to -1,
+ * which moe_permute drops; a table entry outside [0, E) is dropped and
+ * flagged by moe_permute.  ws: at least moe_scratch_bytes (status word). */
+moe_status moe_hash_route(const moe_shape *shape, const int32_t *token_ids,
+                          const int32_t *table, int64_t vocab, int32_t *topk_idx,
+                          float *topk_w, void *ws, size_t ws_bytes, void *stream);
+
 /* Expert histogram, group offsets and scatter ("Fused MoE Kernel Notes",
  * Scatter/gather layout): counts[e] = pairs routed to e (duplicates count
  * again); offsets[e] = sum of counts before e, offsets[E] = T*k;

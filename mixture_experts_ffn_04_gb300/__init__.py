@@ -91,6 +91,7 @@ def lib():
         "moe_workspace_views": (i32, [S, P, ctypes.POINTER(MoERouteInfo)]),
         "moe_workspace_init": (i32, [P, P]),
         "moe_route": (i32, [S, P, P, P, P, P, P, sz, P]),
+        "moe_hash_route": (i32, [S, P, P, i64, P, P, P, sz, P]),
         "moe_permute": (i32, [S, P, P, P, P, P, P, P, P, sz, P]),
         "moe_permute_static": (i32, [S, P, P, P, P, P, P, P, P]),
         "moe_grouped_swiglu": (i32, [S, P, P, P, i64, P, i32, i64, i32, P, P, sz, P]),
@@ -218,6 +219,12 @@ def moe_route(shape, x, w_router, topk_idx, topk_w, gate, ws, stream=None):
     _check(lib().moe_route(ctypes.byref(shape), _p(x), _p(w_router), _p(topk_idx), _p(topk_w),
                            _p(gate), _p(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "moe_route")
+
+
+def moe_hash_route(shape, token_ids, table, vocab, topk_idx, topk_w, ws, stream=None):
+    _check(lib().moe_hash_route(ctypes.byref(shape), _p(token_ids), _p(table), vocab,
+                                _p(topk_idx), _p(topk_w), _p(ws), ws.numel() * ws.element_size(),
+                                _stream(stream)), "moe_hash_route")
 
 
 def moe_permute(shape, x, topk_idx, counts, offsets, scatter_index, row_token, x_perm, ws,

@@ -131,6 +131,10 @@ cudaError_t launch_topk(const Shape& s, const float* logits, int nsplit, const v
                         uint32_t* redecided, cudaStream_t st);
 cudaError_t launch_sum_partials(const Shape& s, const float* logits, int nsplit, float* out,
                                 cudaStream_t st);
+// Hash-MoE routes: idx[t, s] = table[token_ids[t] * k + s], w = 1/k.
+cudaError_t launch_hash_route(const Shape& s, const int32_t* token_ids, const int32_t* table,
+                              int64_t vocab, int32_t* idx, float* w, uint32_t* flags,
+                              cudaStream_t st);
 
 // Split-K factor for a tensor-core fp32-output GEMM of one group (router):
 // enough CTAs to cover the SMs, at most kMaxSplit, at least 4 k-blocks each.

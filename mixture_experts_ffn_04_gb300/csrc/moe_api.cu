@@ -350,6 +350,23 @@ moe_status moe_route(const moe_shape* shape, const void* x, const void* w_router
                   (cudaStream_t)stream);
 }
 
+moe_status moe_hash_route(const moe_shape* shape, const int32_t* token_ids, const int32_t* table,
+                          int64_t vocab, int32_t* topk_idx, float* topk_w, void* ws,
+                          size_t ws_bytes, void* stream) {
+  reset_launch_count();
+  DECODE(shape, s);
+  if (vocab < 1) return fail(MOE_ERR_INVALID_ARG, "vocab must be >= 1");
+  if (s.T > 0 && (!token_ids || !table || !topk_idx || !topk_w))
+    return fail(MOE_ERR_INVALID_ARG, "token_ids, table, topk_idx and topk_w must be non-NULL");
+  const Layout L = layout_for(s);
+  moe_status c = check_ws(ws, ws_bytes, L.scratch_end);
+  if (c != MOE_OK) return c;
+  char* w = static_cast<char*>(ws);
+  CHECK_CUDA(launch_hash_route(s, token_ids, table, vocab, topk_idx, topk_w,
+                               reinterpret_cast<uint32_t*>(w + L.flags), (cudaStream_t)stream));
+  return MOE_OK;
+}
+
 moe_status moe_permute(const moe_shape* shape, const void* x, const int32_t* topk_idx,
                        int32_t* counts, int32_t* offsets, int32_t* scatter_index,
                        int32_t* row_token, void* x_perm, void* ws, size_t ws_bytes,

@@ -690,6 +690,44 @@ __global__ void sum_partials_kernel(const float* __restrict__ part, int nsplit,
 }
 }  // namespace
 
+namespace {
+// Hash-MoE lookup ("Fused MoE Kernel Notes", Duplicate top-k routes): slot s
+// of token t goes to table[token_ids[t], s]; every slot weighs 1/k (one
+// correctly rounded fp32 division).  A token id outside the table sends its
+// slots to route -1, which the permutation drops, and raises the route flag.
+__global__ void hash_route_kernel(const int32_t* __restrict__ token_ids,
+                                  const int32_t* __restrict__ table, int64_t vocab, int64_t T,
+                                  int k, int32_t* __restrict__ idx, float* __restrict__ w,
+                                  uint32_t* flags) {
+  const float wk = __fdiv_rn(1.0f, (float)k);
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < T * k;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = i / k;
+    const int sl = (int)(i - t * k);
+    const int64_t tok = token_ids[t];
+    int32_t e = -1;
+    if (tok >= 0 && tok < vocab) {
+      e = table[tok * k + sl];
+    } else if (sl == 0) {
+      set_flag(flags, kFlagRoute);
+    }
+    idx[i] = e;
+    w[i] = wk;
+  }
+}
+}  // namespace
+
+cudaError_t launch_hash_route(const Shape& s, const int32_t* token_ids, const int32_t* table,
+                              int64_t vocab, int32_t* idx, float* w, uint32_t* flags,
+                              cudaStream_t st) {
+  if (s.T == 0) return cudaSuccess;
+  const int64_t n = s.T * s.k;
+  const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  hash_route_kernel<<<blocks, 256, 0, st>>>(token_ids, table, vocab, s.T, s.k, idx, w, flags);
+  count_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_sum_partials(const Shape& s, const float* logits, int nsplit, float* out,
                                 cudaStream_t st) {
   if (s.T == 0) return cudaSuccess;

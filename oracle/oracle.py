@@ -218,6 +218,23 @@ def moe_ffn(x, idx, weights, gate, w_gate, w_up, w_down, sh_gate=None, sh_up=Non
     return y
 
 
+def hash_route(token_ids, table, top_k: int):
+    """Hash-MoE routing ("Fused MoE Kernel Notes", Duplicate top-k routes: a
+    token-to-expert lookup can give two slots of a token the same expert):
+    idx[t, s] = table[token_ids[t], s] for a lookup table [vocab, k]; every
+    slot weighs 1/k (the reading taken: the notes' regression pattern uses one
+    constant routing weight for all slots), as float64.  A token id outside
+    [0, vocab) routes all its slots to -1 (dropped by the permutation)."""
+    ids = np.asarray(token_ids, dtype=np.int64)
+    tab = np.asarray(table, dtype=np.int64).reshape(-1, top_k)
+    idx = np.full((ids.size, top_k), -1, dtype=np.int32)
+    for t, tok in enumerate(ids):
+        if 0 <= tok < tab.shape[0]:
+            for s in range(top_k):
+                idx[t, s] = tab[tok, s]
+    return idx, np.full((ids.size, top_k), 1.0 / top_k)
+
+
 def round_act(v: float, dtype: str) -> float:
     """The activation-type value nearest to v (ties to even), as a float."""
     return load().oracle_round_act(float(v), BF16 if dtype == "bf16" else F32)

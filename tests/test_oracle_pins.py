@@ -522,3 +522,24 @@ def check_residual_identity():
 
 def test_residual_identity(orc):
     check_residual_identity()
+
+
+def check_hash_route():
+    """Hash-MoE lookup ("Fused MoE Kernel Notes", Duplicate top-k routes): a
+    hand-worked table, an out-of-range token id, and the notes' example --
+    128 tokens whose lookup sends both slots to expert 0 form one group of
+    256 rows."""
+    table = np.array([[3, 1], [2, 2], [0, 3]], dtype=np.int32)   # vocab 3, k 2
+    idx, w = O.hash_route([2, 1, 0, 7, 1], table, 2)
+    assert idx.tolist() == [[0, 3], [2, 2], [3, 1], [-1, -1], [2, 2]]
+    assert w.shape == (5, 2) and (w == 0.5).all()
+    idx, w = O.hash_route(np.arange(128) % 5, np.zeros((5, 2), np.int32), 2)
+    counts, offsets, sidx, _ = O.permute(idx, 4)
+    assert counts.tolist() == [256, 0, 0, 0] and offsets.tolist() == [0, 256, 256, 256, 256]
+    assert sidx[127].tolist() == [254, 255]
+    _, w3 = O.hash_route([0], np.zeros((1, 3), np.int32), 3)
+    assert w3[0, 0] == 1.0 / 3.0
+
+
+def test_hash_route():
+    check_hash_route()
