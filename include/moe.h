@@ -61,6 +61,21 @@ typedef enum {
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 
+/* Storage of the expert weights (routed gate/up/down and the shared MLP's;
+ * the router always has the activation type).  MOE_WEIGHTS_MXFP8 ("MoE:
+ * shared experts, arbitrary V_TOPK expert shapes, and an enforced
+ * stage-marker contract", the fusion identity: e4m3 values with one e8m0
+ * scale per block of 8 along the reduced axis) stores each [N, K] matrix
+ * packed: its N*K e4m3 bytes row-major, then its N*K/8 e8m0 bytes row-major
+ * ([N, K/8]); value = e4m3(q) * 2^(scale - 127).  With MXFP8 the expert
+ * strides of moe_weights and of the grouped calls count BYTES (at least
+ * N*K*9/8, multiples of 16), the activations are bf16, and the weights are
+ * read by the decode engine (at most 512 grouped rows a call: half the bytes
+ * of bf16 weights) or, for larger calls, the CUDA-core engine; no tensor-core
+ * path and no backward take MXFP8 weights.  moe_quantize_mxfp8 makes the
+ * packed matrices. */
+typedef enum { MOE_WEIGHTS_ACT = 0, MOE_WEIGHTS_MXFP8 = 1 } moe_weight_format;
+
 /* Stages of the forward pass, in execution order.  Their names (see
  * moe_stage_name) label the benchmark's per-stage timings. */
 typedef enum {
@@ -105,6 +120,7 @@ typedef struct {
   int32_t residual;     /* 1: y = x + the MoE output */
   double norm_eps;      /* RMSNorm epsilon, finite and >= 0 */
   int32_t train;        /* 1: keep what the backward needs (see above) */
+  int32_t weight_format; /* moe_weight_format of the expert weights */
 } moe_shape;
 
 /* Weights for moe_layer_forward (device pointers, layouts as above). */
@@ -138,6 +154,17 @@ typedef struct {
                              tensor-core engine it may hold fp32 partial sums
                              over K instead, which the combine adds */
 } moe_route_info;
+
+/* Quantise weights to packed MXFP8 matrices (see moe_weight_format): batch
+ * matrices [rows, K] of `dtype` (MOE_BF16 or MOE_F32), matrix b at
+ * w + b * src_stride elements, into packed matrices at packed + b * dst_stride
+ * bytes (dst_stride >= rows*K*9/8).  K a multiple of 8.  A block's scale is
+ * the smallest power of two X with max|V| / X <= 448 (so MXFP8-representable
+ * weights come back unchanged, as the pages state), values are rounded to
+ * nearest even and saturate at 448.  Asynchronous on `stream`; no workspace. */
+moe_status moe_quantize_mxfp8(const void *w, int32_t dtype, int64_t batch, int64_t rows,
+                              int32_t K, int64_t src_stride, int64_t dst_stride, void *packed,
+                              void *stream);
 
 /* Packed routing-shape word (compiler page, Group A: (num_experts << 8) |
  * top_k; the 8-bit shift keeps every shape with up to 16383 experts in a

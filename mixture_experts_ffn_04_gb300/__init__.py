@@ -42,7 +42,8 @@ class MoEShape(ctypes.Structure):
                 ("topk_shape", ctypes.c_uint32), ("shared_gate", ctypes.c_int32),
                 ("norm_topk", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("input_norm", ctypes.c_int32), ("residual", ctypes.c_int32),
-                ("norm_eps", ctypes.c_double), ("train", ctypes.c_int32)]
+                ("norm_eps", ctypes.c_double), ("train", ctypes.c_int32),
+                ("weight_format", ctypes.c_int32)]
 
 
 class MoEWeights(ctypes.Structure):
@@ -90,6 +91,7 @@ def lib():
         "moe_workspace_bytes": (sz, [S]),
         "moe_workspace_views": (i32, [S, P, ctypes.POINTER(MoERouteInfo)]),
         "moe_workspace_init": (i32, [P, P]),
+        "moe_quantize_mxfp8": (i32, [P, i32, i64, i64, i32, i64, i64, P, P]),
         "moe_route": (i32, [S, P, P, P, P, P, P, sz, P]),
         "moe_hash_route": (i32, [S, P, P, i64, P, P, P, sz, P]),
         "moe_permute": (i32, [S, P, P, P, P, P, P, P, P, sz, P]),
@@ -177,6 +179,26 @@ def moe_scratch_bytes(shape: MoEShape) -> int:
 
 def moe_workspace_bytes(shape: MoEShape) -> int:
     return int(lib().moe_workspace_bytes(ctypes.byref(shape)))
+
+
+def moe_quantize_mxfp8(w, batch, rows, K, src_stride, dst_stride, packed, stream=None):
+    """Packed MXFP8 matrices from bf16 / fp32 ones (see include/moe.h)."""
+    _check(lib().moe_quantize_mxfp8(_p(w), _dtype_code(w.dtype), batch, rows, K, src_stride,
+                                    dst_stride, _p(packed), _stream(stream)),
+           "moe_quantize_mxfp8")
+
+
+def mxfp8_pack(w: torch.Tensor, stream=None) -> torch.Tensor:
+    """[..., N, K] weights -> [..., N*K*9/8] uint8 packed MXFP8 matrices (the
+    leading dimensions are the batch), on w's device."""
+    N, K = w.shape[-2], w.shape[-1]
+    batch = w.numel() // (N * K)
+    out = torch.empty(tuple(w.shape[:-2]) + (N * K // 8 * 9,), dtype=torch.uint8, device=w.device)
+    moe_quantize_mxfp8(w, batch, N, K, N * K, N * K // 8 * 9, out, stream)
+    return out
+
+
+MOE_WEIGHTS_ACT, MOE_WEIGHTS_MXFP8 = 0, 1
 
 
 def moe_workspace_init(ws: torch.Tensor, stream=None):
@@ -440,6 +462,7 @@ def shape_for(wl, T: Optional[int] = None) -> MoEShape:
     s.residual = int(getattr(wl, "residual", False))
     s.norm_eps = float(getattr(wl, "norm_eps", 1e-6))
     s.train = int(getattr(wl, "train", False))
+    s.weight_format = MOE_WEIGHTS_MXFP8 if getattr(wl, "weights", "act") == "mxfp8" else MOE_WEIGHTS_ACT
     return s
 
 
@@ -460,9 +483,12 @@ def weights_from(inputs: dict) -> MoEWeights:
     g, d = inputs["w_gate"], inputs["w_down"]
     w.router = _p(inputs.get("w_router"))
     w.gate, w.up = _p(g), _p(inputs["w_up"])
-    w.gate_up_stride = g.shape[1] * g.shape[2]
     w.down = _p(d)
-    w.down_stride = d.shape[1] * d.shape[2]
+    if g.dtype == torch.uint8:   # packed MXFP8 [E, N*K*9/8]: strides in bytes
+        w.gate_up_stride, w.down_stride = g.shape[1], d.shape[1]
+    else:
+        w.gate_up_stride = g.shape[1] * g.shape[2]
+        w.down_stride = d.shape[1] * d.shape[2]
     w.shared_gate_proj = _p(inputs.get("sh_gate"))
     w.shared_up = _p(inputs.get("sh_up"))
     w.shared_down = _p(inputs.get("sh_down"))

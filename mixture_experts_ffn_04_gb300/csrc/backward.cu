@@ -366,6 +366,7 @@ moe_status moe_layer_backward(const moe_shape* shape, const moe_weights* W, cons
   if (!s.train) return fail(MOE_ERR_INVALID_ARG, "moe_layer_backward needs a train-mode forward (shape->train = 1)");
   if (s.I_sh) return fail(MOE_ERR_UNSUPPORTED, "the shared expert's backward is not part of the routed-expert op");
   if (s.input_norm) return fail(MOE_ERR_UNSUPPORTED, "the input RMSNorm's backward is not part of the routed-expert op");
+  if (s.wfmt) return fail(MOE_ERR_UNSUPPORTED, "the backward takes expert weights in the activation type, not MXFP8");
   if (!W || !grads) return fail(MOE_ERR_INVALID_ARG, "weights and grads must be non-NULL");
   if (s.T > 0 && (!dy || !dx || !d_topk_w || !W->gate || !W->up || !W->down || !grads->gate ||
                   !grads->up || !grads->down))

@@ -96,7 +96,9 @@ __device__ __forceinline__ int find_group(const int32_t* sched, int G, int j) {
 namespace {
 constexpr int kBN = 64, kBK = 16, kThreads = 256;
 
-template <typename T, int MODE, int BM>
+// MX: B0/B1 hold packed MXFP8 matrices (bstride in bytes), dequantised as
+// they are loaded.
+template <typename T, int MODE, int BM, bool MX = false>
 __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(GemmArgs a) {
   constexpr int TM = BM / 16;  // rows per thread
   __shared__ __align__(16) float As[kBK][BM + 4];
@@ -115,8 +117,10 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(GemmArgs a) {
   const int K = a.K, N = a.N;
 
   const T* A = reinterpret_cast<const T*>(a.A);
-  const T* B0 = reinterpret_cast<const T*>(a.B0) + (int64_t)g * a.bstride;
-  const T* B1 = MODE == kSwiGLU ? reinterpret_cast<const T*>(a.B1) + (int64_t)g * a.bstride : nullptr;
+  const T* B0 = reinterpret_cast<const T*>(a.B0) + (MX ? 0 : (int64_t)g * a.bstride);
+  const T* B1 = MODE == kSwiGLU ? reinterpret_cast<const T*>(a.B1) + (MX ? 0 : (int64_t)g * a.bstride) : nullptr;
+  const uint8_t* M0 = MX ? reinterpret_cast<const uint8_t*>(a.B0) + (int64_t)g * a.bstride : nullptr;
+  const uint8_t* M1 = MX && MODE == kSwiGLU ? reinterpret_cast<const uint8_t*>(a.B1) + (int64_t)g * a.bstride : nullptr;
 
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   for (int r = tid; r < BM; r += kThreads) {
@@ -156,8 +160,13 @@ __global__ void __launch_bounds__(kThreads) simt_gemm_kernel(GemmArgs a) {
     for (int q = 0; q < EB; ++q) {
       const int e = tid + q * kThreads, n = e / kBK, kk = e % kBK;
       const bool in = n0 + n < N && k0 + kk < K;
-      rb[q] = in ? to_f(B0[(int64_t)(n0 + n) * K + k0 + kk]) : 0.f;
-      if (MODE == kSwiGLU) ru[q] = in ? to_f(B1[(int64_t)(n0 + n) * K + k0 + kk]) : 0.f;
+      if (MX) {
+        rb[q] = in ? mx_weight(M0, N, K, n0 + n, k0 + kk) : 0.f;
+        if (MODE == kSwiGLU) ru[q] = in ? mx_weight(M1, N, K, n0 + n, k0 + kk) : 0.f;
+      } else {
+        rb[q] = in ? to_f(B0[(int64_t)(n0 + n) * K + k0 + kk]) : 0.f;
+        if (MODE == kSwiGLU) ru[q] = in ? to_f(B1[(int64_t)(n0 + n) * K + k0 + kk]) : 0.f;
+      }
     }
   };
   auto stash = [&]() {
@@ -237,10 +246,16 @@ cudaError_t launch_t(const GemmArgs& a, cudaStream_t st) {
   if (mt_bound <= 0 || a.N <= 0) return cudaSuccess;
   if (mt_bound > 0x7fffffff) return cudaErrorInvalidValue;
   dim3 grid((unsigned)mt_bound, (unsigned)((a.N + kBN - 1) / kBN));
-  switch (a.mode) {
-    case kSwiGLU: simt_gemm_kernel<T, kSwiGLU, BM><<<grid, kThreads, 0, st>>>(a); break;
-    case kStoreAct: simt_gemm_kernel<T, kStoreAct, BM><<<grid, kThreads, 0, st>>>(a); break;
-    default: simt_gemm_kernel<T, kStoreF32, BM><<<grid, kThreads, 0, st>>>(a); break;
+  if (a.wfmt) {
+    if (a.mode == kSwiGLU) simt_gemm_kernel<T, kSwiGLU, BM, true><<<grid, kThreads, 0, st>>>(a);
+    else if (a.mode == kStoreAct) simt_gemm_kernel<T, kStoreAct, BM, true><<<grid, kThreads, 0, st>>>(a);
+    else return cudaErrorInvalidValue;
+  } else {
+    switch (a.mode) {
+      case kSwiGLU: simt_gemm_kernel<T, kSwiGLU, BM><<<grid, kThreads, 0, st>>>(a); break;
+      case kStoreAct: simt_gemm_kernel<T, kStoreAct, BM><<<grid, kThreads, 0, st>>>(a); break;
+      default: simt_gemm_kernel<T, kStoreF32, BM><<<grid, kThreads, 0, st>>>(a); break;
+    }
   }
   count_launch();
   return cudaGetLastError();
@@ -293,7 +308,11 @@ __device__ void block_schedule(const GemmArgs& a, int bm, int32_t* sched, int la
   }
 }
 
-template <typename T, int MODE>
+// MX: the weights are packed MXFP8 matrices (bstride in bytes): per 8-value
+// chunk of A a lane loads the block's 8 e4m3 bytes and its scale byte, half
+// the bytes of bf16 weights, and the dequantised values are exact, so the
+// sums equal those over the same weights stored in bf16.
+template <typename T, int MODE, bool MX = false>
 __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched, int ks) {
   constexpr int NU = MODE == kSwiGLU ? 2 : 1;
   __shared__ int32_t s_sched[kSkMaxG + 1];
@@ -340,11 +359,26 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched,
                                 : nullptr;
   const uint4* Bc[kSkC];
   const uint4* Uc[kSkC];
+  const uint2* Bq[kSkC];
+  const uint2* Uq[kSkC];
+  const uint8_t* Bs[kSkC];
+  const uint8_t* Us[kSkC];
 #pragma unroll
   for (int q = 0; q < kSkC; ++q) {
     const int n = min(n0 + q, a.N - 1);   // clamped columns are computed, not stored
-    Bc[q] = reinterpret_cast<const uint4*>(B0 + (int64_t)n * K);
-    Uc[q] = MODE == kSwiGLU ? reinterpret_cast<const uint4*>(B1 + (int64_t)n * K) : nullptr;
+    if (MX) {
+      const uint8_t* m0 = reinterpret_cast<const uint8_t*>(a.B0) + (int64_t)g * a.bstride;
+      Bq[q] = reinterpret_cast<const uint2*>(m0 + (int64_t)n * K);
+      Bs[q] = m0 + (int64_t)a.N * K + (int64_t)n * (K / 8);
+      if (MODE == kSwiGLU) {
+        const uint8_t* m1 = reinterpret_cast<const uint8_t*>(a.B1) + (int64_t)g * a.bstride;
+        Uq[q] = reinterpret_cast<const uint2*>(m1 + (int64_t)n * K);
+        Us[q] = m1 + (int64_t)a.N * K + (int64_t)n * (K / 8);
+      }
+    } else {
+      Bc[q] = reinterpret_cast<const uint4*>(B0 + (int64_t)n * K);
+      Uc[q] = MODE == kSwiGLU ? reinterpret_cast<const uint4*>(B1 + (int64_t)n * K) : nullptr;
+    }
   }
   float acc[kSkR][kSkC], accu[MODE == kSwiGLU ? kSkR : 1][kSkC];
 #pragma unroll
@@ -360,8 +394,13 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched,
       float w[kSkC][V], u[MODE == kSwiGLU ? kSkC : 1][V];
 #pragma unroll
       for (int q = 0; q < kSkC; ++q) {
-        unpack16(__ldg(Bc[q] + c), w[q], (const T*)nullptr);
-        if (MODE == kSwiGLU) unpack16(__ldg(Uc[q] + c), u[q], (const T*)nullptr);
+        if (MX) {
+          unpack_mx8(__ldg(Bq[q] + c), __ldg(Bs[q] + c), w[q]);
+          if (MODE == kSwiGLU) unpack_mx8(__ldg(Uq[q] + c), __ldg(Us[q] + c), u[q]);
+        } else {
+          unpack16(__ldg(Bc[q] + c), w[q], (const T*)nullptr);
+          if (MODE == kSwiGLU) unpack16(__ldg(Uc[q] + c), u[q], (const T*)nullptr);
+        }
       }
 #pragma unroll
       for (int r = 0; r < kSkR; ++r) {
@@ -449,10 +488,17 @@ cudaError_t launch_skinny_t(const GemmArgs& a, int smem_sched, cudaStream_t st) 
   while (ks < kSkW && base_warps * ks < 2432) ks *= 2;
   const int cols_per_block = (kSkW / ks) * kSkC;
   dim3 grid((unsigned)mt_bound, (unsigned)((a.N + cols_per_block - 1) / cols_per_block));
-  switch (a.mode) {
-    case kSwiGLU: skinny_kernel<T, kSwiGLU><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
-    case kStoreAct: skinny_kernel<T, kStoreAct><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
-    default: skinny_kernel<T, kStoreF32><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
+  if (a.wfmt) {
+    if (sizeof(T) != 2) return cudaErrorInvalidValue;   // MXFP8 blocks are one bf16 chunk
+    if (a.mode == kSwiGLU) skinny_kernel<T, kSwiGLU, true><<<grid, 256, 0, st>>>(a, smem_sched, ks);
+    else if (a.mode == kStoreAct) skinny_kernel<T, kStoreAct, true><<<grid, 256, 0, st>>>(a, smem_sched, ks);
+    else return cudaErrorInvalidValue;
+  } else {
+    switch (a.mode) {
+      case kSwiGLU: skinny_kernel<T, kSwiGLU><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
+      case kStoreAct: skinny_kernel<T, kStoreAct><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
+      default: skinny_kernel<T, kStoreF32><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
+    }
   }
   count_launch();
   return cudaGetLastError();

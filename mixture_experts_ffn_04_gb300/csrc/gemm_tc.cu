@@ -559,6 +559,7 @@ int router_split(int64_t rows, int ncols, int K) {
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   using namespace tc;
   if (a.dtype != MOE_BF16 || encode_fn() == nullptr) return cudaErrorNotSupported;
+  if (a.wfmt) return cudaErrorNotSupported;   // MXFP8 weights: decode or CUDA-core engine
   // bf16 outputs are stored as 8-element vectors; fp32 outputs column by column
   if ((a.K % 8) != 0 || (a.mode != kStoreF32 && (a.N % 8) != 0) || a.K <= 0 || a.N <= 0)
     return cudaErrorInvalidValue;

@@ -429,7 +429,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 cudaError_t launch_gemm_tc2(const GemmArgs& a, cudaStream_t st) {
   using namespace tc2;
-  if (a.dtype != MOE_BF16 || a.mode == kStoreF32 || a.ksplit != 1 || a.gather)
+  if (a.dtype != MOE_BF16 || a.mode == kStoreF32 || a.ksplit != 1 || a.gather || a.wfmt)
     return cudaErrorNotSupported;
   if ((a.K % 8) != 0 || (a.N % 8) != 0 || a.K <= 0 || a.N <= 0) return cudaErrorInvalidValue;
   cudaError_t e;

@@ -22,6 +22,7 @@ struct Shape {
   int input_norm, residual;
   double norm_eps;
   int train;   // the forward keeps what the backward needs (fc1 rows)
+  int wfmt;    // expert weights: 0 the activation type, 1 packed MXFP8
 };
 
 // Decode and validate; on failure returns the status and sets *why.
@@ -76,6 +77,8 @@ struct GemmArgs {
   int64_t a_rows = 0;               // rows of A when gathered (bound on gather values)
   void* pre = nullptr;              // SwiGLU: also store the pre-activations,
   int64_t ldp = 0;                  // gate at pre[r, n], up at pre[r, N + n]
+  int wfmt = 0;                     // 1: B0/B1 are packed MXFP8 [N, K] matrices,
+                                    // bstride in bytes
 };
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t st);
@@ -131,6 +134,11 @@ cudaError_t launch_topk(const Shape& s, const float* logits, int nsplit, const v
                         uint32_t* redecided, cudaStream_t st);
 cudaError_t launch_sum_partials(const Shape& s, const float* logits, int nsplit, float* out,
                                 cudaStream_t st);
+// Packed MXFP8 matrices from activation-type ones: batch matrices [rows, K]
+// src_stride elements apart -> packed matrices dst_stride bytes apart.
+cudaError_t launch_quantize_mxfp8(int dtype, const void* w, int64_t batch, int64_t rows, int K,
+                                  int64_t src_stride, int64_t dst_stride, void* out,
+                                  cudaStream_t st);
 // Hash-MoE routes: idx[t, s] = table[token_ids[t] * k + s], w = 1/k.
 cudaError_t launch_hash_route(const Shape& s, const int32_t* token_ids, const int32_t* table,
                               int64_t vocab, int32_t* idx, float* w, uint32_t* flags,

@@ -82,11 +82,20 @@ moe_status decode_shape(const moe_shape* s, Shape* o, const char** why) {
     *why = "train must be 0 or 1";
     return MOE_ERR_INVALID_ARG;
   }
+  if (s->weight_format != MOE_WEIGHTS_ACT && s->weight_format != MOE_WEIGHTS_MXFP8) {
+    *why = "weight_format must be MOE_WEIGHTS_ACT or MOE_WEIGHTS_MXFP8";
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (s->weight_format == MOE_WEIGHTS_MXFP8 && s->dtype != MOE_BF16) {
+    *why = "MXFP8 expert weights need bf16 activations";
+    return MOE_ERR_UNSUPPORTED;
+  }
   o->T = s->tokens;
   o->input_norm = s->input_norm;
   o->residual = s->residual;
   o->norm_eps = s->norm_eps;
   o->train = s->train;
+  o->wfmt = s->weight_format;
   o->H = s->hidden;
   o->I = s->moe_inter;
   o->I_sh = s->shared_inter;
@@ -154,6 +163,13 @@ Layout layout_for(const Shape& s) {
 static int engine_for(const GemmArgs& a) {
   const int ov = gemm_path_override();
   const int64_t rows = a.offsets ? a.rows_bound : a.single_rows;
+  if (a.wfmt) {
+    // MXFP8 weights: the decode engine (half the weight bytes), or the
+    // CUDA-core engine for large calls and for the pre-activation store
+    if (ov == 1 || a.pre) return 1;
+    if (ov == 3) return 3;
+    return rows <= 512 ? 3 : 1;
+  }
   if (a.dtype == MOE_F32) return ov == 3 && a.pre == nullptr ? 3 : 1;
   // the pre-activation store exists on the one-SM tensor-core and CUDA-core engines
   if (a.pre) return ov == 1 ? 1 : 2;
@@ -281,6 +297,21 @@ moe_status moe_workspace_views(const moe_shape* shape, void* ws, moe_route_info*
   return MOE_OK;
 }
 
+moe_status moe_quantize_mxfp8(const void* w, int32_t dtype, int64_t batch, int64_t rows, int32_t K,
+                              int64_t src_stride, int64_t dst_stride, void* packed, void* stream) {
+  reset_launch_count();
+  if (dtype != MOE_BF16 && dtype != MOE_F32) return fail(MOE_ERR_UNSUPPORTED, "dtype must be MOE_BF16 or MOE_F32");
+  if (batch < 0 || rows < 0 || K <= 0 || K % 8) return fail(MOE_ERR_INVALID_ARG, "batch, rows >= 0 and K a positive multiple of 8");
+  if (batch > 0 && rows > 0 && (!w || !packed)) return fail(MOE_ERR_INVALID_ARG, "w and packed must be non-NULL");
+  if (batch > 1 && (src_stride < rows * K || dst_stride < rows * K / 8 * 9))
+    return fail(MOE_ERR_INVALID_ARG, "strides smaller than one matrix");
+  if (!aligned16(w) || !aligned16(packed) || (batch > 1 && (dst_stride % 16 || (src_stride * (dtype == MOE_F32 ? 4 : 2)) % 16)))
+    return fail(MOE_ERR_INVALID_ARG, "w, packed and the strides must be 16-byte aligned");
+  CHECK_CUDA(launch_quantize_mxfp8(dtype, w, batch, rows, K, src_stride, dst_stride, packed,
+                                   (cudaStream_t)stream));
+  return MOE_OK;
+}
+
 moe_status moe_workspace_init(void* ws, void* stream) {
   if (!ws) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
   CHECK_CUDA(cudaMemsetAsync(ws, 0, 256, (cudaStream_t)stream));
@@ -401,8 +432,14 @@ static moe_status grouped(int mode, const moe_shape* shape, const void* A, const
   if (G > 1 && stride == 0) return fail(MOE_ERR_INVALID_ARG, "expert_stride is 0 with several groups");
   if (rows_bound > 0 && (!A || !B0 || !out || (mode == kSwiGLU && !B1)))
     return fail(MOE_ERR_INVALID_ARG, "operand pointers must be non-NULL");
-  if (!aligned16(A) || !aligned16(B0) || !aligned16(B1) || !aligned16(out) || (stride * s.esize) % 16)
+  const int wsize = s.wfmt ? 1 : s.esize;   // MXFP8: strides in bytes
+  if (!aligned16(A) || !aligned16(B0) || !aligned16(B1) || !aligned16(out) || (stride * wsize) % 16)
     return fail(MOE_ERR_INVALID_ARG, "operands and expert_stride must be 16-byte aligned");
+  if (s.wfmt && G > 1) {
+    const int64_t n = mode == kSwiGLU ? inter : s.H, kk = mode == kSwiGLU ? s.H : inter;
+    if (stride < n * kk / 8 * 9)
+      return fail(MOE_ERR_INVALID_ARG, "MXFP8 expert_stride smaller than one packed matrix");
+  }
   const Layout L = layout_for(s);
   moe_status c = check_ws(ws, ws_bytes, L.scratch_end);
   if (c != MOE_OK) return c;
@@ -426,6 +463,7 @@ static moe_status grouped(int mode, const moe_shape* shape, const void* A, const
   a.flags = reinterpret_cast<uint32_t*>(w + L.flags);
   a.gather = gather;
   a.a_rows = s.T;
+  a.wfmt = s.wfmt;
   CHECK_CUDA(launch_grouped_gemm(a, (cudaStream_t)stream));
   return MOE_OK;
 }
@@ -523,7 +561,9 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
     return fail(MOE_ERR_INVALID_ARG, "shared_inter > 0 needs the three shared weights");
   if (!s.I_sh && (W->shared_gate_proj || W->shared_up || W->shared_down))
     return fail(MOE_ERR_INVALID_ARG, "shared weights given but shared_inter is 0");
-  if (W->gate_up_stride < (int64_t)s.I * s.H || W->down_stride < (int64_t)s.H * s.I)
+  // MXFP8: packed matrices, strides in bytes
+  const int64_t mat = (int64_t)s.I * s.H, wsz = s.wfmt ? 1 : s.esize;
+  if (W->gate_up_stride < (s.wfmt ? mat / 8 * 9 : mat) || W->down_stride < (s.wfmt ? mat / 8 * 9 : mat))
     return fail(MOE_ERR_INVALID_ARG, "expert strides smaller than one expert matrix");
   if (s.input_norm && s.T > 0 && !W->norm_weight)
     return fail(MOE_ERR_INVALID_ARG, "input_norm needs weights->norm_weight");
@@ -534,7 +574,7 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
   if (!aligned16(x) || !aligned16(y) || !aligned16(W->router) || !aligned16(W->gate) ||
       !aligned16(W->up) || !aligned16(W->down) || !aligned16(W->shared_gate_proj) ||
       !aligned16(W->shared_up) || !aligned16(W->shared_down) ||
-      (W->gate_up_stride * s.esize) % 16 || (W->down_stride * s.esize) % 16)
+      (W->gate_up_stride * wsz) % 16 || (W->down_stride * wsz) % 16)
     return fail(MOE_ERR_INVALID_ARG, "tensors and strides must be 16-byte aligned");
   const Layout L = layout_for(s);
   moe_status c = check_ws(ws, ws_bytes, L.total);
@@ -592,6 +632,7 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
   a.rows_bound = s.T * s.k;
   a.sched = reinterpret_cast<int32_t*>(w + L.sched_routed);
   a.flags = flags;
+  a.wfmt = s.wfmt;
   a.mode = kSwiGLU;
   a.A = x_perm;
   a.B0 = W->gate;
@@ -633,6 +674,7 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
     b.rows_bound = s.T;
     b.sched = reinterpret_cast<int32_t*>(w + L.sched_shared);
     b.flags = flags;
+    b.wfmt = s.wfmt;
     b.mode = kSwiGLU;
     b.A = xin;
     b.B0 = W->shared_gate_proj;

@@ -48,6 +48,7 @@ class Workload:
     input_norm: bool = False     # input RMSNorm before the router and experts
     residual: bool = False       # y = x + MoE(x_norm)
     norm_eps: float = 1e-6
+    weights: str = "act"         # expert weights: "act" (activation type) or "mxfp8" (packed)
     description: str = ""
 
     @property
@@ -180,6 +181,28 @@ def _routes(w: Workload, seed: int):
     return torch.from_numpy(idx), torch.from_numpy(wt)
 
 
+def _mxfp8_packed(seed: int, name: str, batch: int, N: int, K: int, std: float,
+                  device) -> torch.Tensor:
+    """Seeded packed MXFP8 matrices [batch, N*K*9/8] drawn directly as codes and
+    scales (no quantisation): e4m3 codes with a random sign, exponent field
+    4..9 and mantissa 0..7 (magnitudes 0.125 .. 7.5), and per-block scale
+    bytes within one of 127 + round(log2(std / 4)), so the values have about
+    the standard deviation `std`."""
+    g = torch.Generator(device=device)
+    g.manual_seed(_key(seed, name))
+    nk = N * K
+    out = torch.empty((batch, nk // 8 * 9), dtype=torch.uint8, device=device)
+    for b in range(batch):
+        sign = torch.randint(0, 2, (nk,), generator=g, device=device, dtype=torch.int32)
+        ex = torch.randint(4, 10, (nk,), generator=g, device=device, dtype=torch.int32)
+        man = torch.randint(0, 8, (nk,), generator=g, device=device, dtype=torch.int32)
+        out[b, :nk] = ((sign << 7) | (ex << 3) | man).to(torch.uint8)
+        base = 127 + int(round(math.log2(std / 4.0)))
+        sc = torch.randint(-1, 2, (nk // 8,), generator=g, device=device, dtype=torch.int32) + base
+        out[b, nk:] = sc.to(torch.uint8)
+    return out
+
+
 def make_output_grad(w: Workload, seed: int = 0, device="cpu") -> torch.Tensor:
     """dy = dL/dy [T, H] for the backward: standard normal in the activation type."""
     return _normal(seed, "dy", (w.T, w.H), 1.0, w.torch_dtype, device)
@@ -214,11 +237,21 @@ def make_inputs(w: Workload, seed: int = 0, device="cpu", with_experts: bool = T
         d["w_router"] = None
         ri, rw = _routes(w, seed)
         d["routes_idx"], d["routes_w"] = ri.to(device), rw.to(device)
-    if with_experts:
+    mx = w.weights == "mxfp8"
+    if with_experts and mx:
+        # packed MXFP8 [E, N*K*9/8] (include/moe.h, moe_weight_format)
+        d["w_gate"] = _mxfp8_packed(seed, "w_gate", E, I, H, 1.0 / math.sqrt(H), device)
+        d["w_up"] = _mxfp8_packed(seed, "w_up", E, I, H, 1.0 / math.sqrt(H), device)
+        d["w_down"] = _mxfp8_packed(seed, "w_down", E, H, I, 1.0 / math.sqrt(I), device)
+    elif with_experts:
         d["w_gate"] = _normal(seed, "w_gate", (E, I, H), 1.0 / math.sqrt(H), dt, device)
         d["w_up"] = _normal(seed, "w_up", (E, I, H), 1.0 / math.sqrt(H), dt, device)
         d["w_down"] = _normal(seed, "w_down", (E, H, I), 1.0 / math.sqrt(I), dt, device)
-    if I_sh > 0:
+    if I_sh > 0 and mx:
+        d["sh_gate"] = _mxfp8_packed(seed, "sh_gate", 1, I_sh, H, 1.0 / math.sqrt(H), device)[0]
+        d["sh_up"] = _mxfp8_packed(seed, "sh_up", 1, I_sh, H, 1.0 / math.sqrt(H), device)[0]
+        d["sh_down"] = _mxfp8_packed(seed, "sh_down", 1, H, I_sh, 1.0 / math.sqrt(I_sh), device)[0]
+    elif I_sh > 0:
         d["sh_gate"] = _normal(seed, "sh_gate", (I_sh, H), 1.0 / math.sqrt(H), dt, device)
         d["sh_up"] = _normal(seed, "sh_up", (I_sh, H), 1.0 / math.sqrt(H), dt, device)
         d["sh_down"] = _normal(seed, "sh_down", (H, I_sh), 1.0 / math.sqrt(I_sh), dt, device)

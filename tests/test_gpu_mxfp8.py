@@ -1,0 +1,121 @@
+"""MXFP8 expert weights on the GPU (include/moe.h, moe_weight_format): e4m3
+values with one e8m0 scale per block of 8 along the reduced axis ("MoE:
+shared experts, arbitrary V_TOPK expert shapes, and an enforced stage-marker
+contract").
+
+* moe_quantize_mxfp8 is bit-exact against the oracle's quantiser (bf16 and
+  fp32 inputs; zero blocks, tiny and large blocks);
+* the decode engine and the CUDA-core engine on packed MXFP8 weights give
+  bit-identical results to the same engines on the dequantised weights
+  stored in bf16 (the dequantisation is exact);
+* the whole layer with MXFP8 routed and shared weights (Qwen2-MoE shape with
+  its gated shared expert: decode T = 1, 8 on the decode engine, T = 200 on
+  the CUDA-core engine) against the oracle on the dequantised weights.
+Weights are drawn as packed codes and scales (workloads.py), so the oracle
+only decodes them (oracle/mxfp8.py)."""
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import mixture_experts_ffn_04_gb300 as m
+from mixture_experts_ffn_04_gb300 import workloads as W
+from oracle import mxfp8 as MX
+from oracle import oracle as O
+
+from gpu_util import TOL, TIE_GAP, rel_l2
+
+pytestmark = pytest.mark.gpu
+
+
+def dequant(packed: torch.Tensor, N: int, K: int) -> torch.Tensor:
+    """fp32 [..., N, K] values of packed matrices [..., N*K*9/8] (oracle decode)."""
+    p = packed.cpu().numpy().reshape(-1, N * K // 8 * 9)
+    out = np.stack([MX.dequantize(*MX.unpack(b, N, K)) for b in p]).astype(np.float32)
+    return torch.from_numpy(out.reshape(tuple(packed.shape[:-1]) + (N, K)))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_quantizer_matches_oracle(dtype):
+    g = torch.Generator().manual_seed(3)
+    w = torch.randn(3, 40, 64, generator=g) * torch.exp2(torch.randint(-20, 12, (3, 40, 1), generator=g).float())
+    w[0, :, :8] = 0.0                      # zero blocks
+    w[1, 5, 8:16] = 448.0 * 2.0 ** 3      # exactly at the boundary of a scale
+    w[2, 7, :8] = 1.875 * 2.0 ** -4       # the mantissa the floor rule would saturate
+    w = w.to(dtype)
+    got = m.mxfp8_pack(w.cuda()).cpu().numpy()
+    for b in range(3):
+        c, s = MX.quantize(w[b].double().numpy(), 64)
+        assert np.array_equal(got[b], MX.pack(c, s)), b
+
+
+def _grouped_pair(engine, mode):
+    E, H, I, T, k = 6, 256, 128, 7, 4
+    wl = dataclasses.replace(W.small(W.QWEN2_MOE, T=T, H=H, I=I, I_sh=0, E=E, k=k), weights="mxfp8",
+                             shared_gate=False)
+    d = W.make_inputs(wl, seed=2, device="cuda")
+    idx = torch.randint(0, E, (T, k), generator=torch.Generator().manual_seed(0)).int()
+    counts, offsets, sidx, row_token = O.permute(idx.numpy(), E)
+    R = T * k
+    x_perm = d["x"][torch.from_numpy(row_token).long().cuda()].contiguous()
+    off = torch.from_numpy(offsets).cuda()
+    out = {}
+    for fmt in ("mxfp8", "bf16"):
+        s = m.shape_for(dataclasses.replace(wl, weights="mxfp8" if fmt == "mxfp8" else "act"))
+        ws = m.alloc_workspace(s, full=False)
+        if fmt == "mxfp8":
+            wg, wu, wd = d["w_gate"], d["w_up"], d["w_down"]
+            gstride, dstride = wg.shape[1], wd.shape[1]
+        else:
+            wg = dequant(d["w_gate"], I, H).bfloat16().cuda()
+            wu = dequant(d["w_up"], I, H).bfloat16().cuda()
+            wd = dequant(d["w_down"], H, I).bfloat16().cuda()
+            gstride, dstride = I * H, H * I
+        prev = m.moe_testing_set_gemm_engine(engine)
+        try:
+            if mode == "swiglu":
+                o = torch.empty(R, I, device="cuda", dtype=torch.bfloat16)
+                m.moe_grouped_swiglu(s, x_perm, wg, wu, gstride, off, E, R, I, o, ws)
+            else:
+                hh = (torch.randn(R, I, generator=torch.Generator().manual_seed(1)) * 0.5).bfloat16().cuda()
+                o = torch.empty(R, H, device="cuda", dtype=torch.bfloat16)
+                m.moe_grouped_down(s, hh, wd, dstride, off, E, R, I, o, ws)
+            assert m.moe_get_device_status(ws)[0] == m.MOE_OK
+        finally:
+            m.moe_testing_set_gemm_engine(prev)
+        out[fmt] = o.cpu()
+    return out
+
+
+@pytest.mark.parametrize("engine", [3, 1], ids=["decode-engine", "cuda-core-engine"])
+@pytest.mark.parametrize("mode", ["swiglu", "down"])
+def test_mxfp8_bitwise_equals_dequantised_bf16(engine, mode):
+    out = _grouped_pair(engine, mode)
+    assert torch.isfinite(out["mxfp8"].float()).all()
+    assert torch.equal(out["mxfp8"].view(torch.int16), out["bf16"].view(torch.int16))
+
+
+@pytest.mark.parametrize("T", [1, 8, 200])
+def test_layer_forward_with_mxfp8_weights(T):
+    wl = dataclasses.replace(W.small(W.QWEN2_MOE, T=T, H=512, I=256, I_sh=512, E=16, k=4),
+                             weights="mxfp8")
+    dev = W.make_inputs(wl, seed=7, device="cuda")
+    layer = m.MoELayer(wl, dev)
+    y = layer.forward(dev["x"])
+    st, bits = layer.device_status()
+    assert st == m.MOE_OK, (st, bits)
+    E, I, H, I_sh = wl.E, wl.I, wl.H, wl.I_sh
+    host = {"x": dev["x"].cpu(), "w_router": dev["w_router"].cpu(), "routes_idx": None,
+            "routes_w": None, "norm_weight": None,
+            "w_gate": dequant(dev["w_gate"], I, H), "w_up": dequant(dev["w_up"], I, H),
+            "w_down": dequant(dev["w_down"], H, I),
+            "sh_gate": dequant(dev["sh_gate"], I_sh, H), "sh_up": dequant(dev["sh_up"], I_sh, H),
+            "sh_down": dequant(dev["sh_down"], H, I_sh)}
+    ref = O.forward(dataclasses.replace(wl, weights="act"), host)
+    ok = ref["gap"] >= TIE_GAP
+    gi = layer.views()["topk_idx"].cpu().numpy()
+    assert (gi[ok] == ref["idx"][ok]).all()
+    yg = y.double().cpu().numpy()
+    assert np.isfinite(yg).all()
+    assert rel_l2(yg[ok], ref["y"][ok]) <= TOL["bf16"], rel_l2(yg[ok], ref["y"][ok])
