@@ -140,14 +140,16 @@ def algorithmic(wl, counts: np.ndarray):
     """Algorithmic FLOPs and bytes of the gate/up GEMM and of the whole layer
     (touched experts only, each weight byte once, activations once)."""
     b = wl.esize
+    # expert weights: the activation type, or packed MXFP8 (1 + 1/8 bytes a weight)
+    wb = 1.125 if getattr(wl, "weights", "act") == "mxfp8" else b
     T, H, I, k, Ish = wl.T, wl.H, wl.I, wl.k, wl.I_sh
     touched = int((counts > 0).sum())
     rows = T * k
     gu_flops = 4.0 * rows * H * I
-    gu_bytes = touched * 2.0 * I * H * b + rows * H * b + rows * I * b
+    gu_bytes = touched * 2.0 * I * H * wb + rows * H * b + rows * I * b
     dn_flops = 2.0 * rows * H * I
     layer_flops = wl.flops()
-    layer_bytes = (touched * 3.0 * I * H * b + 3.0 * Ish * H * b + T * H * b * 2
+    layer_bytes = (touched * 3.0 * I * H * wb + 3.0 * Ish * H * wb + T * H * b * 2
                    + (wl.E + (1 if wl.shared_gate else 0)) * H * b)
     if getattr(wl, "input_norm", False):   # x_norm written once (x itself read already)
         layer_bytes += T * H * b + H * b
@@ -232,7 +234,8 @@ def run_reference(args, wl, rank, world):
 
 
 def _config(wl, graph=None):
-    return {"workload": wl.name, "cuda_graph": graph, "tokens": wl.T, "hidden": wl.H, "experts": wl.E,
+    return {"workload": wl.name, "cuda_graph": graph, "expert_weights": getattr(wl, "weights", "act"),
+            "tokens": wl.T, "hidden": wl.H, "experts": wl.E,
             "top_k": wl.k, "moe_inter": wl.I, "shared_inter": wl.I_sh,
             "shared_gate": wl.shared_gate, "norm_topk": wl.norm_topk, "routing": wl.routing,
             "l2": "flushed before every timed step (256 MiB device write); e2e steps "
@@ -252,7 +255,7 @@ def train_step(m, wl, inputs, args, flush, peaks, dist):
     CUDA events after an L2 flush; W warm-up steps, K timed.  None for
     workloads whose backward the library does not cover (a shared expert or
     an input RMSNorm)."""
-    if wl.I_sh or wl.input_norm:
+    if wl.I_sh or wl.input_norm or getattr(wl, "weights", "act") == "mxfp8":
         return None
     from mixture_experts_ffn_04_gb300 import workloads as W
     layer = m.MoELayer(wl, inputs, train=True)
@@ -315,6 +318,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--weights", default="act", choices=["act", "mxfp8"],
+                    help="expert weights in the activation type or packed MXFP8 (no CPU "
+                         "baseline or training step with MXFP8)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch every step from the host instead of replaying a CUDA graph")
     args = ap.parse_args()
@@ -322,6 +328,10 @@ def main():
 
     from mixture_experts_ffn_04_gb300 import workloads as W
     wl = W.get(args.workload)
+    if args.weights == "mxfp8":
+        import dataclasses
+        wl = dataclasses.replace(wl, weights="mxfp8")
+        args.no_cpu_baseline = True
     dist, rank, world = _dist()
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if torch.cuda.is_available():

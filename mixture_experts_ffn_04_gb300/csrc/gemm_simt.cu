@@ -312,7 +312,10 @@ __device__ void block_schedule(const GemmArgs& a, int bm, int32_t* sched, int la
 // chunk of A a lane loads the block's 8 e4m3 bytes and its scale byte, half
 // the bytes of bf16 weights, and the dequantised values are exact, so the
 // sums equal those over the same weights stored in bf16.
-template <typename T, int MODE, bool MX = false>
+// PAIR: a lane step covers two consecutive 8-value chunks (K a multiple of
+// 16), so each weight load is 16 bytes for MXFP8 too; the chunk order per
+// lane is the same with and without MX, so both give the same sums.
+template <typename T, int MODE, bool MX = false, bool PAIR = false>
 __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched, int ks) {
   constexpr int NU = MODE == kSwiGLU ? 2 : 1;
   __shared__ int32_t s_sched[kSkMaxG + 1];
@@ -337,8 +340,10 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched,
   const int n0 = (blockIdx.y * ncg + cg) * kSkC;
   const int K = a.K;
   constexpr int V = 16 / sizeof(T);
+  constexpr int CH = PAIR ? 2 : 1;   // chunks per lane step
   const int nv = K / V;
-  const int c0 = (int)((int64_t)nv * sl / ks), c1 = (int)((int64_t)nv * (sl + 1) / ks);
+  const int nvp = nv / CH;
+  const int c0 = (int)((int64_t)nvp * sl / ks), c1 = (int)((int64_t)nvp * (sl + 1) / ks);
   // row r of this tile reads A row arow[r] (gathered or contiguous); -1: zeros
   int64_t arow[kSkR];
 #pragma unroll
@@ -390,30 +395,51 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched,
     }
   if (n0 < a.N) {
 #pragma unroll 2
-    for (int c = c0 + lane; c < c1; c += 32) {
-      float w[kSkC][V], u[MODE == kSwiGLU ? kSkC : 1][V];
+    for (int cp = c0 + lane; cp < c1; cp += 32) {
+      float w[kSkC][CH * V], u[MODE == kSwiGLU ? kSkC : 1][CH * V];
 #pragma unroll
       for (int q = 0; q < kSkC; ++q) {
-        if (MX) {
-          unpack_mx8(__ldg(Bq[q] + c), __ldg(Bs[q] + c), w[q]);
-          if (MODE == kSwiGLU) unpack_mx8(__ldg(Uq[q] + c), __ldg(Us[q] + c), u[q]);
+        if (MX && PAIR) {
+          // two blocks: 16 e4m3 bytes and their two scale bytes
+          const uint4 qq = __ldg(reinterpret_cast<const uint4*>(Bq[q]) + cp);
+          const uint32_t ss = __ldg(reinterpret_cast<const unsigned short*>(Bs[q]) + cp);
+          unpack_mx8(make_uint2(qq.x, qq.y), ss & 0xFFu, w[q]);
+          unpack_mx8(make_uint2(qq.z, qq.w), ss >> 8, w[q] + V);
+          if (MODE == kSwiGLU) {
+            const uint4 uq = __ldg(reinterpret_cast<const uint4*>(Uq[q]) + cp);
+            const uint32_t us = __ldg(reinterpret_cast<const unsigned short*>(Us[q]) + cp);
+            unpack_mx8(make_uint2(uq.x, uq.y), us & 0xFFu, u[q]);
+            unpack_mx8(make_uint2(uq.z, uq.w), us >> 8, u[q] + V);
+          }
         } else {
-          unpack16(__ldg(Bc[q] + c), w[q], (const T*)nullptr);
-          if (MODE == kSwiGLU) unpack16(__ldg(Uc[q] + c), u[q], (const T*)nullptr);
+#pragma unroll
+          for (int h = 0; h < CH; ++h) {
+            const int c = cp * CH + h;
+            if (MX) {
+              unpack_mx8(__ldg(Bq[q] + c), __ldg(Bs[q] + c), w[q] + h * V);
+              if (MODE == kSwiGLU) unpack_mx8(__ldg(Uq[q] + c), __ldg(Us[q] + c), u[q] + h * V);
+            } else {
+              unpack16(__ldg(Bc[q] + c), w[q] + h * V, (const T*)nullptr);
+              if (MODE == kSwiGLU) unpack16(__ldg(Uc[q] + c), u[q] + h * V, (const T*)nullptr);
+            }
+          }
         }
       }
 #pragma unroll
       for (int r = 0; r < kSkR; ++r) {
         if (arow[r] >= 0) {
-          float xa[V];
-          unpack16(__ldg(A + arow[r] * nv + c), xa, (const T*)nullptr);
 #pragma unroll
-          for (int q = 0; q < kSkC; ++q)
+          for (int h = 0; h < CH; ++h) {
+            float xa[V];
+            unpack16(__ldg(A + arow[r] * nv + cp * CH + h), xa, (const T*)nullptr);
 #pragma unroll
-            for (int i = 0; i < V; ++i) {
-              acc[r][q] = fmaf(w[q][i], xa[i], acc[r][q]);
-              if (MODE == kSwiGLU) accu[r][q] = fmaf(u[q][i], xa[i], accu[r][q]);
-            }
+            for (int q = 0; q < kSkC; ++q)
+#pragma unroll
+              for (int i = 0; i < V; ++i) {
+                acc[r][q] = fmaf(w[q][h * V + i], xa[i], acc[r][q]);
+                if (MODE == kSwiGLU) accu[r][q] = fmaf(u[q][h * V + i], xa[i], accu[r][q]);
+              }
+          }
         }
       }
     }
@@ -488,11 +514,23 @@ cudaError_t launch_skinny_t(const GemmArgs& a, int smem_sched, cudaStream_t st) 
   while (ks < kSkW && base_warps * ks < 2432) ks *= 2;
   const int cols_per_block = (kSkW / ks) * kSkC;
   dim3 grid((unsigned)mt_bound, (unsigned)((a.N + cols_per_block - 1) / cols_per_block));
+  const bool pair = a.K % (2 * (16 / (int)sizeof(T))) == 0;
   if (a.wfmt) {
     if (sizeof(T) != 2) return cudaErrorInvalidValue;   // MXFP8 blocks are one bf16 chunk
-    if (a.mode == kSwiGLU) skinny_kernel<T, kSwiGLU, true><<<grid, 256, 0, st>>>(a, smem_sched, ks);
-    else if (a.mode == kStoreAct) skinny_kernel<T, kStoreAct, true><<<grid, 256, 0, st>>>(a, smem_sched, ks);
-    else return cudaErrorInvalidValue;
+    if (a.mode != kSwiGLU && a.mode != kStoreAct) return cudaErrorInvalidValue;
+    if (pair) {
+      if (a.mode == kSwiGLU) skinny_kernel<T, kSwiGLU, true, true><<<grid, 256, 0, st>>>(a, smem_sched, ks);
+      else skinny_kernel<T, kStoreAct, true, true><<<grid, 256, 0, st>>>(a, smem_sched, ks);
+    } else {
+      if (a.mode == kSwiGLU) skinny_kernel<T, kSwiGLU, true><<<grid, 256, 0, st>>>(a, smem_sched, ks);
+      else skinny_kernel<T, kStoreAct, true><<<grid, 256, 0, st>>>(a, smem_sched, ks);
+    }
+  } else if (pair) {
+    switch (a.mode) {
+      case kSwiGLU: skinny_kernel<T, kSwiGLU, false, true><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
+      case kStoreAct: skinny_kernel<T, kStoreAct, false, true><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
+      default: skinny_kernel<T, kStoreF32, false, true><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
+    }
   } else {
     switch (a.mode) {
       case kSwiGLU: skinny_kernel<T, kSwiGLU><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;

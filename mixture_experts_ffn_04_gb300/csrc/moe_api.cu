@@ -168,7 +168,9 @@ static int engine_for(const GemmArgs& a) {
     // CUDA-core engine for large calls and for the pre-activation store
     if (ov == 1 || a.pre) return 1;
     if (ov == 3) return 3;
-    return rows <= 512 ? 3 : 1;
+    // the decode engine re-reads the weights for every 8-row m-tile: fine for
+    // many small groups, not for one big group (the shared MLP)
+    return rows <= (a.G == 1 ? 16 : 512) ? 3 : 1;
   }
   if (a.dtype == MOE_F32) return ov == 3 && a.pre == nullptr ? 3 : 1;
   // the pre-activation store exists on the one-SM tensor-core and CUDA-core engines
