@@ -85,6 +85,9 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_simt(const GemmArgs& a, int bm, cudaStream_t st);
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_tc2(const GemmArgs& a, cudaStream_t st);   // SM pairs
+// MXFP8 weights dequantised in the tensor-core pipeline (K a multiple of 128)
+bool gemm_tc_mx_ok(const GemmArgs& a);
+cudaError_t launch_gemm_tc_mx(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_schedule(const GemmArgs& a, int bm, cudaStream_t st);
 

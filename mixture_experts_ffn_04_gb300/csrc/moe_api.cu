@@ -168,6 +168,10 @@ static int engine_for(const GemmArgs& a) {
     // CUDA-core engine for large calls and for the pre-activation store
     if (ov == 1 || a.pre) return 1;
     if (ov == 3) return 3;
+    // the tensor cores with the weight tiles dequantised in shared memory:
+    // measured faster than the decode engine above 4 rows spread over many
+    // groups, and above 16 rows of one group (the shared MLP)
+    if (gemm_tc_mx_ok(a) && (ov == 2 || rows > (a.G == 1 ? 16 : 4))) return 6;
     // the decode engine re-reads the weights for every 8-row m-tile: fine for
     // many small groups, not for one big group (the shared MLP)
     return rows <= (a.G == 1 ? 16 : 512) ? 3 : 1;
@@ -216,6 +220,7 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t st) {
     case 1: return launch_gemm_simt(a, 64, st);
     case 2: return launch_gemm_tc(a, st);
     case 4: return launch_gemm_tc2(a, st);
+    case 6: return launch_gemm_tc_mx(a, st);
     default: return launch_gemm_skinny(a, st);
   }
 }

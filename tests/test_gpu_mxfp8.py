@@ -5,9 +5,11 @@ contract").
 
 * moe_quantize_mxfp8 is bit-exact against the oracle's quantiser (bf16 and
   fp32 inputs; zero blocks, tiny and large blocks);
-* the decode engine and the CUDA-core engine on packed MXFP8 weights give
+* the decode, CUDA-core and tensor-core engines on packed MXFP8 weights give
   bit-identical results to the same engines on the dequantised weights
-  stored in bf16 (the dequantisation is exact);
+  stored in bf16 (the dequantisation is exact; the tensor-core engine
+  converts the weight tiles into the same shared-memory layout the bf16
+  engine loads);
 * the whole layer with MXFP8 routed and shared weights (Qwen2-MoE shape with
   its gated shared expert: decode T = 1, 8 on the decode engine, T = 200 on
   the CUDA-core engine) against the oracle on the dequantised weights.
@@ -88,7 +90,8 @@ def _grouped_pair(engine, mode):
     return out
 
 
-@pytest.mark.parametrize("engine", [3, 1], ids=["decode-engine", "cuda-core-engine"])
+@pytest.mark.parametrize("engine", [3, 1, 2], ids=["decode-engine", "cuda-core-engine",
+                                                  "tensor-core-engine"])
 @pytest.mark.parametrize("mode", ["swiglu", "down"])
 def test_mxfp8_bitwise_equals_dequantised_bf16(engine, mode):
     out = _grouped_pair(engine, mode)
