@@ -11,7 +11,7 @@
 //               of the 16 scale bytes per row that cover this k-block and its
 //               neighbour (scale rows are 16-byte aligned when K is a
 //               multiple of 128);
-//   warps 7-12  converters: four lanes share a weight row, each taking 16
+//   warps 7-26  converters: four lanes share a weight row, each taking 16
 //               codes (two blocks), so a warp reads 8 consecutive rows of the
 //               staged codes without bank conflicts; each block becomes 8
 //               bf16 values (e4m3 -> fp16 by the hardware conversion, times
@@ -55,8 +55,8 @@ constexpr int RING_A = 0, RING_B = SA * A_BYTES, RING_Q = RING_B + SB * B_BYTES,
 // barriers: fullA emptyA [SA], fullQ emptyQ [SQ], fullB emptyB [SB], then
 // tfull[2] tempty[2] final
 constexpr int NBAR = 2 * (SA + SQ + SB) + 5;
-constexpr int CONV_WARP0 = 7, CONV_WARPS = 6;
-constexpr int THREADS = (CONV_WARP0 + CONV_WARPS) * 32;   // warps 0-12
+constexpr int CONV_WARP0 = 7, CONV_WARPS = 20;
+constexpr int THREADS = (CONV_WARP0 + CONV_WARPS) * 32;   // warps 0-26
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int BAR_BYTES = 256;
 constexpr int MAX_SMEM_G = 512;

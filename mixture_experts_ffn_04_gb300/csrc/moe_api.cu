@@ -168,10 +168,9 @@ static int engine_for(const GemmArgs& a) {
     // CUDA-core engine for large calls and for the pre-activation store
     if (ov == 1 || a.pre) return 1;
     if (ov == 3) return 3;
-    // the tensor cores with the weight tiles dequantised in shared memory:
-    // measured faster than the decode engine above 4 rows spread over many
-    // groups, and above 16 rows of one group (the shared MLP)
-    if (gemm_tc_mx_ok(a) && (ov == 2 || rows > (a.G == 1 ? 16 : 4))) return 6;
+    // the tensor cores with the weight tiles dequantised in shared memory,
+    // above a few rows (as for bf16 weights)
+    if (gemm_tc_mx_ok(a) && (ov == 2 || rows > 4)) return 6;
     // the decode engine re-reads the weights for every 8-row m-tile: fine for
     // many small groups, not for one big group (the shared MLP)
     return rows <= (a.G == 1 ? 16 : 512) ? 3 : 1;

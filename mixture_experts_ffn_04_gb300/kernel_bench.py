@@ -51,6 +51,8 @@ def main(argv=None):
     ap.add_argument("--hidden", type=int, default=7168)
     ap.add_argument("--inter", type=int, default=2048)
     ap.add_argument("--workload", default="qwen3-30b-a3b-shape-T4096")
+    ap.add_argument("--weights", default="act", choices=["act", "mxfp8"],
+                    help="gate_up / down: expert weights packed as MXFP8 (moe_quantize_mxfp8)")
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=2)
     a = ap.parse_args(argv)
@@ -89,6 +91,10 @@ def main(argv=None):
     offsets = torch.cat([torch.zeros(1, dtype=torch.int64), counts.cumsum(0)]).to(torch.int32).cuda()
     R = int(counts.sum())
     wl = W.small(W.DEEPSEEK_V3, T=max(1, R // 8), H=H, I=I, E=E, k=8, I_sh=0)
+    mx = a.weights == "mxfp8" and a.op in ("gate_up", "down")
+    if mx:
+        import dataclasses
+        wl = dataclasses.replace(wl, weights="mxfp8")
     s = m.shape_for(wl)
     ws = m.alloc_workspace(s, full=False)
     rnd = lambda *shape, sc=0.1: (torch.randn(*shape, generator=g, device="cuda") * sc).bfloat16()
@@ -96,13 +102,20 @@ def main(argv=None):
         wg, wu = rnd(E, I, H, sc=0.02), rnd(E, I, H, sc=0.02)
     if a.op in ("down", "dgrad_down"):
         wd = rnd(E, H, I, sc=0.02)
+    gs, ds = I * H, H * I   # expert strides (elements; bytes when packed)
+    if mx and a.op == "gate_up":
+        wg, wu = m.mxfp8_pack(wg), m.mxfp8_pack(wu)
+        gs = wg.shape[1]
+    if mx and a.op == "down":
+        wd = m.mxfp8_pack(wd)
+        ds = wd.shape[1]
     if a.op == "gate_up":
         xp, h = rnd(R, H), torch.empty(R, I, device="cuda", dtype=torch.bfloat16)
-        fn = lambda: m.moe_grouped_swiglu(s, xp, wg, wu, I * H, offsets, E, R, I, h, ws)
+        fn = lambda: m.moe_grouped_swiglu(s, xp, wg, wu, gs, offsets, E, R, I, h, ws)
         flops = 4.0 * R * H * I
     elif a.op == "down":
         h, yp = rnd(R, I), torch.empty(R, H, device="cuda", dtype=torch.bfloat16)
-        fn = lambda: m.moe_grouped_down(s, h, wd, H * I, offsets, E, R, I, yp, ws)
+        fn = lambda: m.moe_grouped_down(s, h, wd, ds, offsets, E, R, I, yp, ws)
         flops = 2.0 * R * H * I
     elif a.op == "dgrad_down":
         gf, fc1 = rnd(R, H), rnd(R, 2 * I, sc=1.0)
@@ -120,7 +133,8 @@ def main(argv=None):
         flops = 2.0 * R * H * I
     us = _time(fn, flush, a.steps, a.warmup)
     st = m.moe_get_device_status(ws)[0]
-    print(json.dumps({"op": a.op, "groups": E, "rows": R, "hidden": H, "inter": I, "us": us,
+    print(json.dumps({"op": a.op, "weights": a.weights, "groups": E, "rows": R, "hidden": H,
+                      "inter": I, "us": us,
                       "tflops": flops / us / 1e6, "status": st}))
     return 0 if st == m.MOE_OK else 1
 
