@@ -69,11 +69,14 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
  * packed: its N*K e4m3 bytes row-major, then its N*K/8 e8m0 bytes row-major
  * ([N, K/8]); value = e4m3(q) * 2^(scale - 127).  With MXFP8 the expert
  * strides of moe_weights and of the grouped calls count BYTES (at least
- * N*K*9/8, multiples of 16), the activations are bf16, and the weights are
- * read by the decode engine (at most 512 grouped rows a call: half the bytes
- * of bf16 weights) or, for larger calls, the CUDA-core engine; no tensor-core
- * path and no backward take MXFP8 weights.  moe_quantize_mxfp8 makes the
- * packed matrices. */
+ * N*K*9/8, multiples of 16) and the activations are bf16.  The weights are
+ * dequantised as they are loaded: on the tensor cores (calls of more than 4
+ * rows with K a multiple of 128: e4m3 tiles by TMA, converted in shared
+ * memory to the bf16 tile the MMA reads), by the decode engine (up to 4
+ * rows) or by the CUDA-core engine (other shapes); results equal those of
+ * the same engine on the dequantised weights stored in bf16.  The backward
+ * does not take MXFP8 weights.  moe_quantize_mxfp8 makes the packed
+ * matrices. */
 typedef enum { MOE_WEIGHTS_ACT = 0, MOE_WEIGHTS_MXFP8 = 1 } moe_weight_format;
 
 /* Stages of the forward pass, in execution order.  Their names (see

@@ -197,3 +197,50 @@ def test_backward_validation(m):
     assert st == m.MOE_ERR_INVALID_ARG
     s_bad = _shape(m, train=2)
     assert m.moe_workspace_bytes(s_bad) == 0
+
+
+def test_mxfp8_validation(m):
+    """MXFP8 expert weights (include/moe.h, moe_weight_format): host checks."""
+    lib = m.lib()
+    P = ctypes.c_void_p
+    assert m.moe_workspace_bytes(_shape(m, weight_format=2)) == 0
+    sf = _shape(m, weight_format=m.MOE_WEIGHTS_MXFP8, dtype=m.MOE_F32)
+    st = lib.moe_route(ctypes.byref(sf), P(4096), P(4096), P(4096), P(4096), None, P(4096),
+                       1 << 30, None)
+    assert st == m.MOE_ERR_UNSUPPORTED and "bf16" in m.moe_last_error()
+    s = _shape(m, weight_format=m.MOE_WEIGHTS_MXFP8)
+    need = m.moe_workspace_bytes(s)
+    w = m.MoEWeights()
+    w.router = w.gate = w.up = w.down = 4096
+    # strides count bytes: one packed [128, 256] matrix is 128*256*9/8 bytes
+    w.gate_up_stride = w.down_stride = 128 * 256
+    st = lib.moe_layer_forward(ctypes.byref(s), ctypes.byref(w), P(4096), None, None, P(4096),
+                               P(4096), need, None)
+    assert st == m.MOE_ERR_INVALID_ARG and "stride" in m.moe_last_error()
+    # grouped call: a stride below one packed matrix
+    st = lib.moe_grouped_swiglu(ctypes.byref(s), P(4096), P(4096), P(4096), 128 * 256, P(4096),
+                                8, 128, 128, P(4096), P(4096), 1 << 30, None)
+    assert st == m.MOE_ERR_INVALID_ARG and "MXFP8" in m.moe_last_error()
+    # the backward refuses MXFP8 weights
+    st_ = _shape(m, weight_format=m.MOE_WEIGHTS_MXFP8, train=1)
+    g = m.MoEExpertGrads()
+    g.gate = g.up = g.down = 8192
+    g.gate_up_stride = g.down_stride = 128 * 256
+    w.gate_up_stride = w.down_stride = 128 * 256 * 9 // 8
+    st = lib.moe_layer_backward(ctypes.byref(st_), ctypes.byref(w), P(4096), P(4096), P(4096),
+                                ctypes.byref(g), P(4096), m.moe_workspace_bytes(st_), None)
+    assert st == m.MOE_ERR_UNSUPPORTED and "MXFP8" in m.moe_last_error()
+    # quantiser: K must be a multiple of 8
+    assert lib.moe_quantize_mxfp8(P(4096), m.MOE_BF16, 1, 4, 12, 48, 54, P(4096), None) == m.MOE_ERR_INVALID_ARG
+
+
+def test_hash_route_validation(m):
+    lib = m.lib()
+    P = ctypes.c_void_p
+    s = _shape(m)
+    st = lib.moe_hash_route(ctypes.byref(s), P(4096), P(4096), 0, P(4096), P(4096), P(4096),
+                            1 << 30, None)
+    assert st == m.MOE_ERR_INVALID_ARG and "vocab" in m.moe_last_error()
+    st = lib.moe_hash_route(ctypes.byref(s), None, P(4096), 10, P(4096), P(4096), P(4096),
+                            1 << 30, None)
+    assert st == m.MOE_ERR_INVALID_ARG
