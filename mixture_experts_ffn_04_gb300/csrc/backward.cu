@@ -111,34 +111,6 @@ using namespace moe;
 
 namespace {
 
-moe_status fail(moe_status st, const char* why) {
-  set_error_message(why);
-  return st;
-}
-
-bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
-
-moe_status check_ws(void* ws, size_t ws_bytes, size_t need) {
-  if (!ws) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
-  if ((uintptr_t)ws & 255u) return fail(MOE_ERR_WORKSPACE, "workspace is not 256-byte aligned");
-  if (ws_bytes < need) return fail(MOE_ERR_WORKSPACE, "workspace smaller than required");
-  return MOE_OK;
-}
-
-#define CHECK_CUDA(expr)                                        \
-  do {                                                          \
-    cudaError_t e_ = (expr);                                    \
-    if (e_ != cudaSuccess) return fail(MOE_ERR_CUDA, cudaGetErrorString(e_)); \
-  } while (0)
-
-#define DECODE(shape, s)                                       \
-  Shape s;                                                     \
-  do {                                                         \
-    const char* why_ = "";                                     \
-    moe_status st_ = decode_shape(shape, &s, &why_);           \
-    if (st_ != MOE_OK) return fail(st_, why_);                 \
-  } while (0)
-
 // Checks shared by the grouped calls: group count, inter, row bound, strides.
 moe_status check_grouped(const Shape& s, int32_t G, int64_t rows_bound, int32_t inter,
                          int64_t stride, const int32_t* offsets) {

@@ -166,6 +166,32 @@ cudaError_t launch_permute_scratch(const Shape& s, int nchunks, int tpc, int32_t
 // Record why the current host call failed (read back by moe_last_error).
 void set_error_message(const char* why);
 
+// Host-side argument checks shared by the C-ABI files (moe_api.cu,
+// backward.cu): every failure names its reason for moe_last_error.
+inline moe_status fail(moe_status st, const char* why) {
+  set_error_message(why);
+  return st;
+}
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+inline moe_status check_ws(void* ws, size_t ws_bytes, size_t need) {
+  if (!ws) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+  if ((uintptr_t)ws & 255u) return fail(MOE_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+  if (ws_bytes < need) return fail(MOE_ERR_WORKSPACE, "workspace smaller than required");
+  return MOE_OK;
+}
+#define CHECK_CUDA(expr)                                                          \
+  do {                                                                            \
+    cudaError_t e_ = (expr);                                                      \
+    if (e_ != cudaSuccess) return ::moe::fail(MOE_ERR_CUDA, cudaGetErrorString(e_)); \
+  } while (0)
+#define DECODE(shape, s)                                         \
+  ::moe::Shape s;                                                \
+  do {                                                           \
+    const char* why_ = "";                                       \
+    moe_status st_ = ::moe::decode_shape(shape, &s, &why_);      \
+    if (st_ != MOE_OK) return ::moe::fail(st_, why_);            \
+  } while (0)
+
 // topk_w == NULL: every slot weighs 1 (the backward's gather).
 // shared_part/nsplit_sh: instead of shared_out, nsplit_sh fp32 partial sums
 // of the shared MLP output ([T, H] each, T*H apart), added in order.

@@ -24,11 +24,6 @@ int gemm_path_override() { return g_engine.load(); }
 
 void set_error_message(const char* why) { tl_error = why; }
 
-static moe_status fail(moe_status st, const char* why) {
-  tl_error = why;
-  return st;
-}
-
 static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
 moe_status decode_shape(const moe_shape* s, Shape* o, const char** why) {
@@ -227,32 +222,6 @@ cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t st) {
 }  // namespace moe
 
 using namespace moe;
-
-#define CHECK_CUDA(expr)                                        \
-  do {                                                          \
-    cudaError_t e_ = (expr);                                    \
-    if (e_ != cudaSuccess) {                                    \
-      tl_error = cudaGetErrorString(e_);                        \
-      return MOE_ERR_CUDA;                                      \
-    }                                                           \
-  } while (0)
-
-static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
-
-static moe_status check_ws(void* ws, size_t ws_bytes, size_t need) {
-  if (!ws) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
-  if ((uintptr_t)ws & 255u) return fail(MOE_ERR_WORKSPACE, "workspace is not 256-byte aligned");
-  if (ws_bytes < need) return fail(MOE_ERR_WORKSPACE, "workspace smaller than required");
-  return MOE_OK;
-}
-
-#define DECODE(shape, s)                                       \
-  Shape s;                                                     \
-  do {                                                         \
-    const char* why_ = "";                                     \
-    moe_status st_ = decode_shape(shape, &s, &why_);           \
-    if (st_ != MOE_OK) return fail(st_, why_);                 \
-  } while (0)
 
 extern "C" {
 
