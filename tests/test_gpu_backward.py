@@ -12,8 +12,9 @@ Cases: reduced Qwen3-30B-A3B / DeepSeek-V3 / Gemma-4 (with the residual)
 shapes; the tiny fp32 layer; "Fused MoE Kernel Notes", Duplicate top-k
 routes (every slot of every token on expert 0, so one group holds T*k rows);
 Zipf routing with duplicates and empty experts; a moe_inter that is not a
-multiple of 64 (the gate/up dgrad then runs on the CUDA cores); each bf16
-case on the tensor-core path and on the CUDA-core path."""
+multiple of 64 (the gate/up dgrad then runs on the CUDA cores); 1100 experts
+(tile schedule and offsets in global memory); a single token with top-1; each
+bf16 case on the tensor-core path and on the CUDA-core path."""
 import dataclasses
 
 import numpy as np
@@ -38,6 +39,11 @@ CASES = [
     W.small(W.ADV_E0, T=96, H=256, I=128, E=8, k=6, I_sh=0),
     W.small(W.ADV_ZIPF, T=128, H=384, I=320, E=16, k=6, I_sh=0),
     W.small(W.QWEN3_30B_A3B, T=70, H=136, I=200, E=5, k=3),
+    # more groups than the kernels keep in shared memory (device-built global
+    # tile schedule, offsets read from global memory), most of them empty
+    W.small(W.QWEN3_30B_A3B, T=40, H=128, I=64, E=1100, k=2),
+    # one token, one slot
+    W.small(W.QWEN3_30B_A3B, T=1, H=64, I=64, E=4, k=1),
 ]
 
 
