@@ -122,3 +122,39 @@ def test_layer_forward_with_mxfp8_weights(T):
     yg = y.double().cpu().numpy()
     assert np.isfinite(yg).all()
     assert rel_l2(yg[ok], ref["y"][ok]) <= TOL["bf16"], rel_l2(yg[ok], ref["y"][ok])
+
+
+@pytest.mark.parametrize("T", [8, 64])
+def test_full_size_mxfp8_layer_sampled(T):
+    """The Qwen2-MoE-shaped layer at full width (H = 3584, 60 experts of
+    2560, gated shared MLP of 20480) with every expert weight in MXFP8, on
+    the engines the benchmark uses: sampled tokens against the oracle on the
+    dequantised weights (each token's own experts and the shared MLP decoded
+    on the host)."""
+    wl = dataclasses.replace(W.QWEN2_MOE.with_tokens(T), weights="mxfp8")
+    dev = W.make_inputs(wl, seed=0, device="cuda")
+    layer = m.MoELayer(wl, dev)
+    y = layer.forward(dev["x"])
+    st, bits = layer.device_status()
+    assert st == m.MOE_OK, (st, bits)
+    assert bool(torch.isfinite(y.float()).all())
+    H, I, I_sh = wl.H, wl.I, wl.I_sh
+    host = {"x": dev["x"].cpu(), "w_router": dev["w_router"].cpu(), "routes_idx": None,
+            "routes_w": None, "norm_weight": None}
+    r = O.route(dataclasses.replace(wl, weights="act"), host)
+    sh = [dequant(dev[k], n, kk) for k, n, kk in (("sh_gate", I_sh, H), ("sh_up", I_sh, H),
+                                                  ("sh_down", H, I_sh))]
+    gi = layer.views()["topk_idx"].cpu().numpy()
+    rng = np.random.default_rng(1)
+    for t in np.sort(rng.choice(T, size=min(T, 4), replace=False)):
+        if r["gap"][t] < TIE_GAP:
+            continue
+        assert (gi[t] == r["idx"][t]).all()
+        used, inv = np.unique(r["idx"][t], return_inverse=True)
+        sel = lambda key, n, kk: torch.stack([dequant(dev[key][e], n, kk) for e in used])
+        ref = O.moe_ffn(host["x"][t:t + 1], inv.reshape(1, -1).astype(np.int32),
+                        r["weights"][t:t + 1], r["gate"][t:t + 1],
+                        sel("w_gate", I, H), sel("w_up", I, H), sel("w_down", H, I),
+                        sh[0], sh[1], sh[2])
+        yg = y[t:t + 1].double().cpu().numpy()
+        assert rel_l2(yg, ref) <= TOL["bf16"], (t, rel_l2(yg, ref))
