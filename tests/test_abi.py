@@ -244,3 +244,30 @@ def test_hash_route_validation(m):
     st = lib.moe_hash_route(ctypes.byref(s), None, P(4096), 10, P(4096), P(4096), P(4096),
                             1 << 30, None)
     assert st == m.MOE_ERR_INVALID_ARG
+
+
+def _declared_arity():
+    """{function name: parameter count} from the headers' prototypes."""
+    out = {}
+    for h in ("moe.h", "moe_testing.h", "moe_backward.h"):
+        src = open(os.path.join(ROOT, "include", h)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        for mm in re.finditer(r"\b(moe_\w+)\s*\(([^;{]*?)\)\s*;", src, flags=re.S):
+            params = mm.group(2).strip()
+            out[mm.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_arity_matches_headers(m):
+    """Every ctypes signature of the binding has as many arguments as the C
+    prototype it marshals (a drifted binding would pass garbage silently)."""
+    arity = _declared_arity()
+    lib = m.lib()
+    checked = 0
+    for name, n in arity.items():
+        f = getattr(lib, name)
+        if f.argtypes is None:
+            continue
+        assert len(f.argtypes) == n, (name, len(f.argtypes), n)
+        checked += 1
+    assert checked >= 30, checked
