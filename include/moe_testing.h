@@ -35,6 +35,16 @@ int32_t moe_testing_set_gemm_engine(int32_t engine);
 moe_status moe_testing_router_logits(const moe_shape *shape, const void *x, const void *w_router,
                                      float *logits, void *ws, size_t ws_bytes, void *stream);
 
+/* The failure path of the pipelines' bounded waits, made to run out on
+ * purpose without faulting: one warp waits on a shared-memory mbarrier that
+ * expects one arrival, with the pipelines' try_wait loop bounded by
+ * max_cycles SM clocks (at most 4e9, about 2 s).  arrive = 0: nothing
+ * arrives, the wait runs out, the kernel sets the timeout bit of the
+ * workspace's status word (moe_get_device_status then returns
+ * MOE_ERR_TIMEOUT) and returns; arrive = 1: the arrival completes the phase
+ * and no bit is set.  Needs the workspace's status word only. */
+moe_status moe_testing_wait_probe(void *ws, int64_t max_cycles, int32_t arrive, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

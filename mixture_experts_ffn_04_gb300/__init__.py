@@ -112,6 +112,7 @@ def lib():
         "moe_testing_set_gemm_engine": (i32, [i32]),
         "moe_get_route_stats": (i32, [P, P, ctypes.POINTER(u32)]),
         "moe_testing_router_logits": (i32, [S, P, P, P, P, sz, P]),
+        "moe_testing_wait_probe": (i32, [P, i64, i32, P]),
         # backward (moe_backward.h)
         "moe_backward_views": (i32, [S, P, ctypes.POINTER(MoEBackwardInfo)]),
         "moe_grouped_swiglu_save": (i32, [S, P, P, P, i64, P, i32, i64, i32, P, P, P, sz, P]),
@@ -339,6 +340,11 @@ def moe_testing_router_logits(shape, x, w_router, logits, ws, stream=None):
     _check(lib().moe_testing_router_logits(ctypes.byref(shape), _p(x), _p(w_router), _p(logits),
                                            _p(ws), ws.numel() * ws.element_size(),
                                            _stream(stream)), "moe_testing_router_logits")
+
+
+def moe_testing_wait_probe(ws, max_cycles: int, arrive: bool, stream=None):
+    _check(lib().moe_testing_wait_probe(_p(ws), max_cycles, int(arrive), _stream(stream)),
+           "moe_testing_wait_probe")
 
 
 def moe_status_string(status: int) -> str:
