@@ -508,7 +508,13 @@ def main():
                 "frac": ach / peaks["hbm"]}
     tr = NCU_TRAFFIC.get(wl.name)
     roof["traffic"] = tr["bytes"] if tr and tr.get("kernel_hash") == _kernel_hash() else None
-    roof["kernel"] = "tc_gemm_kernel (gate/up grouped GEMM + SwiGLU)"
+    # the engine the library picks for the routed gate/up call (T*k rows)
+    if wl.T * wl.k <= 4:
+        roof["kernel"] = "skinny_kernel (decode engine: gate/up + SwiGLU)"
+    elif wl.weights == "mxfp8" and wl.H % 128 == 0:
+        roof["kernel"] = "tc_mx_kernel (gate/up grouped GEMM + SwiGLU, MXFP8 weights)"
+    else:
+        roof["kernel"] = "tc_gemm_kernel (gate/up grouped GEMM + SwiGLU)"
     roof["peak_source"] = peaks["source"] + (" burst" if roof["bound"] == "tensor" else " copy")
     roof["algorithmic_per_launch"] = alg["gu_flops"] if roof["bound"] == "tensor" else alg["gu_bytes"]
     dn_ms = stage_ms[m.STAGES.index("down")]

@@ -265,15 +265,19 @@ cudaError_t launch_t(const GemmArgs& a, cudaStream_t st) {
 // ---------------------------------------------------------------------------
 // Skinny engine for decode-sized calls (a few rows per group): the cost is
 // reading each weight row once, so the engine is built to keep many weight
-// loads in flight.  A block owns kSkC output columns of one m-tile of up to
-// kSkR rows; its 8 warps split K into 8 slices and stream their slice of each
-// column's weight row with 16-byte loads, dotting it with the m-tile's rows of
-// A; the 8 partial sums are added in a fixed order through shared memory.  The
-// m-tile schedule is built in shared memory by each block (no extra launch).
+// loads in flight.  Each warp owns kSkC output columns of one m-tile and a
+// slice of K (the block's 8 warps split K into ks = 1-8 slices per column
+// group) and streams its slice of each column's weight row with 16-byte loads,
+// dotting it with the m-tile's rows of A; the ks partial sums of a column are
+// added in a fixed order through shared memory.  The m-tile schedule is built
+// in shared memory by each block (no extra launch).
+// The m-tile height R (1, 4 or 8 rows) is a template parameter: every row of
+// the tile holds its accumulators in registers, and registers bound how many
+// weight loads a thread keeps in flight.
 // ---------------------------------------------------------------------------
 namespace {
-constexpr int kSkR = 8;      // rows per m-tile
-constexpr int kSkC = 4;      // output columns per block
+constexpr int kSkR = 8;      // largest m-tile (rows)
+constexpr int kSkC = 4;      // output columns per warp
 constexpr int kSkW = 8;      // warps per block (K slices)
 constexpr int kSkMaxG = 1024;
 
@@ -315,15 +319,19 @@ __device__ void block_schedule(const GemmArgs& a, int bm, int32_t* sched, int la
 // PAIR: a lane step covers two consecutive 8-value chunks (K a multiple of
 // 16), so each weight load is 16 bytes for MXFP8 too; the chunk order per
 // lane is the same with and without MX, so both give the same sums.
-template <typename T, int MODE, bool MX = false, bool PAIR = false>
-__global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched, int ks) {
+template <typename T, int MODE, bool MX = false, bool PAIR = false, int R = kSkR>
+// One-row tiles (bf16 weights) ask for two blocks an SM: the register cap
+// that gives (128) still holds two lane steps of weight loads in flight, and
+// the down projection then needs no stack.  MXFP8's unpacking would spill.
+__global__ void __launch_bounds__(256, R == 1 && !MX ? 2 : 1)
+    skinny_kernel(GemmArgs a, int smem_sched, int ks) {
   constexpr int NU = MODE == kSwiGLU ? 2 : 1;
   __shared__ int32_t s_sched[kSkMaxG + 1];
-  __shared__ float red[kSkW][kSkR * kSkC * NU];
+  __shared__ float red[kSkW][R * kSkC * NU];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t* sched = a.sched;
   if (smem_sched) {
-    if (warp == 0) block_schedule(a, kSkR, s_sched, lane);
+    if (warp == 0) block_schedule(a, R, s_sched, lane);
     __syncthreads();
     sched = s_sched;
   }
@@ -333,8 +341,8 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched,
   const int g = find_group(sched, a.G, j);
   const int64_t gbeg = a.offsets ? a.offsets[g] : 0;
   const int64_t gend = a.offsets ? a.offsets[g + 1] : a.single_rows;
-  const int64_t row0 = gbeg + (int64_t)(j - sched[g]) * kSkR;
-  const int nrows = (int)min((int64_t)kSkR, gend - row0);
+  const int64_t row0 = gbeg + (int64_t)(j - sched[g]) * R;
+  const int nrows = (int)min((int64_t)R, gend - row0);
   // warp -> (column group cg, K slice sl); the block owns kSkW/ks column groups
   const int cg = warp / ks, sl = warp % ks, ncg = kSkW / ks;
   const int n0 = (blockIdx.y * ncg + cg) * kSkC;
@@ -345,9 +353,9 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched,
   const int nvp = nv / CH;
   const int c0 = (int)((int64_t)nvp * sl / ks), c1 = (int)((int64_t)nvp * (sl + 1) / ks);
   // row r of this tile reads A row arow[r] (gathered or contiguous); -1: zeros
-  int64_t arow[kSkR];
+  int64_t arow[R];
 #pragma unroll
-  for (int r = 0; r < kSkR; ++r) {
+  for (int r = 0; r < R; ++r) {
     int64_t src = r < nrows ? row0 + r : -1;
     if (src >= 0 && a.gather) {
       src = a.gather[src];
@@ -385,9 +393,9 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched,
       Uc[q] = MODE == kSwiGLU ? reinterpret_cast<const uint4*>(B1 + (int64_t)n * K) : nullptr;
     }
   }
-  float acc[kSkR][kSkC], accu[MODE == kSwiGLU ? kSkR : 1][kSkC];
+  float acc[R][kSkC], accu[MODE == kSwiGLU ? R : 1][kSkC];
 #pragma unroll
-  for (int r = 0; r < kSkR; ++r)
+  for (int r = 0; r < R; ++r)
 #pragma unroll
     for (int q = 0; q < kSkC; ++q) {
       acc[r][q] = 0.f;
@@ -426,7 +434,7 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched,
         }
       }
 #pragma unroll
-      for (int r = 0; r < kSkR; ++r) {
+      for (int r = 0; r < R; ++r) {
         if (arow[r] >= 0) {
 #pragma unroll
           for (int h = 0; h < CH; ++h) {
@@ -453,7 +461,7 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched,
     else reinterpret_cast<T*>(a.out)[o] = from_f<T>(silu_f(sg) * su);
   };
 #pragma unroll
-  for (int r = 0; r < kSkR; ++r) {
+  for (int r = 0; r < R; ++r) {
     if (r >= nrows) break;   // uniform over the block
 #pragma unroll
     for (int q = 0; q < kSkC; ++q) {
@@ -475,8 +483,8 @@ __global__ void __launch_bounds__(256) skinny_kernel(GemmArgs a, int smem_sched,
   if (ks == 1) return;
   __syncthreads();
   const int tid = threadIdx.x;
-  if (tid < ncg * kSkR * kSkC) {
-    const int gi = tid / (kSkR * kSkC), rem = tid % (kSkR * kSkC);
+  if (tid < ncg * R * kSkC) {
+    const int gi = tid / (R * kSkC), rem = tid % (R * kSkC);
     const int r = rem / kSkC, q = rem % kSkC;
     if (r < nrows) {
       float sg = 0.f, su = 0.f;
@@ -503,9 +511,32 @@ int64_t mtile_bound(const GemmArgs& a, int bm) {
   return b < a.rows_bound ? b : a.rows_bound;
 }
 
+// m-tile height of a skinny call.  A grouped call of at most 4 rows (one
+// decode token's routes) puts one row in each group when its routes are
+// distinct, so one-row tiles read each weight row once with the fewest
+// accumulators; a repeated route costs one more read of that expert's weights.
+// One group (the shared MLP) takes all its rows in one tile.  Otherwise (MXFP8
+// weights serve grouped calls of up to 512 rows here) 8 rows a tile.
+int skinny_rows(const GemmArgs& a) {
+  if (a.dtype != MOE_BF16 || a.mode == kStoreF32 || a.K % 16 != 0) return kSkR;
+  const int64_t rows = a.offsets ? a.rows_bound : a.single_rows;
+  if (a.G > 1) return rows <= 4 ? 1 : kSkR;
+  return rows <= 1 ? 1 : (rows <= 4 ? 4 : kSkR);
+}
+
+template <typename T, bool MX, bool PAIR, int R>
+void launch_skinny_mode(const GemmArgs& a, dim3 grid, int smem_sched, int ks, cudaStream_t st) {
+  if (a.mode == kSwiGLU)
+    skinny_kernel<T, kSwiGLU, MX, PAIR, R><<<grid, 256, 0, st>>>(a, smem_sched, ks);
+  else if (a.mode == kStoreAct)
+    skinny_kernel<T, kStoreAct, MX, PAIR, R><<<grid, 256, 0, st>>>(a, smem_sched, ks);
+  else if constexpr (!MX && R == kSkR)
+    skinny_kernel<T, kStoreF32, MX, PAIR, R><<<grid, 256, 0, st>>>(a, smem_sched, ks);
+}
+
 template <typename T>
-cudaError_t launch_skinny_t(const GemmArgs& a, int smem_sched, cudaStream_t st) {
-  const int64_t mt_bound = mtile_bound(a, kSkR);
+cudaError_t launch_skinny_t(const GemmArgs& a, int R, int smem_sched, cudaStream_t st) {
+  const int64_t mt_bound = mtile_bound(a, R);
   if (mt_bound <= 0 || a.N <= 0) return cudaSuccess;
   if (mt_bound > 0x7fffffff) return cudaErrorInvalidValue;
   // K slices per column: enough warps to keep every SM streaming weights
@@ -515,28 +546,26 @@ cudaError_t launch_skinny_t(const GemmArgs& a, int smem_sched, cudaStream_t st) 
   const int cols_per_block = (kSkW / ks) * kSkC;
   dim3 grid((unsigned)mt_bound, (unsigned)((a.N + cols_per_block - 1) / cols_per_block));
   const bool pair = a.K % (2 * (16 / (int)sizeof(T))) == 0;
+  // tiles of 1 or 4 rows exist for paired bf16 chunks in the two store modes
+  if (R != kSkR && (sizeof(T) != 2 || !pair || a.mode == kStoreF32)) return cudaErrorInvalidValue;
   if (a.wfmt) {
-    if (sizeof(T) != 2) return cudaErrorInvalidValue;   // MXFP8 blocks are one bf16 chunk
-    if (a.mode != kSwiGLU && a.mode != kStoreAct) return cudaErrorInvalidValue;
-    if (pair) {
-      if (a.mode == kSwiGLU) skinny_kernel<T, kSwiGLU, true, true><<<grid, 256, 0, st>>>(a, smem_sched, ks);
-      else skinny_kernel<T, kStoreAct, true, true><<<grid, 256, 0, st>>>(a, smem_sched, ks);
+    if constexpr (sizeof(T) != 2) {
+      return cudaErrorInvalidValue;   // MXFP8 blocks are one bf16 chunk
     } else {
-      if (a.mode == kSwiGLU) skinny_kernel<T, kSwiGLU, true><<<grid, 256, 0, st>>>(a, smem_sched, ks);
-      else skinny_kernel<T, kStoreAct, true><<<grid, 256, 0, st>>>(a, smem_sched, ks);
+      if (a.mode != kSwiGLU && a.mode != kStoreAct) return cudaErrorInvalidValue;
+      if (!pair) launch_skinny_mode<T, true, false, kSkR>(a, grid, smem_sched, ks, st);
+      else if (R == 1) launch_skinny_mode<T, true, true, 1>(a, grid, smem_sched, ks, st);
+      else if (R == 4) launch_skinny_mode<T, true, true, 4>(a, grid, smem_sched, ks, st);
+      else launch_skinny_mode<T, true, true, kSkR>(a, grid, smem_sched, ks, st);
     }
-  } else if (pair) {
-    switch (a.mode) {
-      case kSwiGLU: skinny_kernel<T, kSwiGLU, false, true><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
-      case kStoreAct: skinny_kernel<T, kStoreAct, false, true><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
-      default: skinny_kernel<T, kStoreF32, false, true><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
-    }
+  } else if (!pair) {
+    launch_skinny_mode<T, false, false, kSkR>(a, grid, smem_sched, ks, st);
+  } else if constexpr (sizeof(T) == 2) {
+    if (R == 1) launch_skinny_mode<T, false, true, 1>(a, grid, smem_sched, ks, st);
+    else if (R == 4) launch_skinny_mode<T, false, true, 4>(a, grid, smem_sched, ks, st);
+    else launch_skinny_mode<T, false, true, kSkR>(a, grid, smem_sched, ks, st);
   } else {
-    switch (a.mode) {
-      case kSwiGLU: skinny_kernel<T, kSwiGLU><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
-      case kStoreAct: skinny_kernel<T, kStoreAct><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
-      default: skinny_kernel<T, kStoreF32><<<grid, 256, 0, st>>>(a, smem_sched, ks); break;
-    }
+    launch_skinny_mode<T, false, true, kSkR>(a, grid, smem_sched, ks, st);
   }
   count_launch();
   return cudaGetLastError();
@@ -545,13 +574,14 @@ cudaError_t launch_skinny_t(const GemmArgs& a, int smem_sched, cudaStream_t st) 
 
 cudaError_t launch_gemm_skinny(const GemmArgs& a, cudaStream_t st) {
   if (a.K % (a.dtype == MOE_F32 ? 4 : 8) != 0) return cudaErrorInvalidValue;
+  const int R = skinny_rows(a);
   const int smem_sched = a.G <= kSkMaxG;
   if (!smem_sched) {
-    cudaError_t e = launch_schedule(a, kSkR, st);
+    cudaError_t e = launch_schedule(a, R, st);
     if (e != cudaSuccess) return e;
   }
-  return a.dtype == MOE_F32 ? launch_skinny_t<float>(a, smem_sched, st)
-                            : launch_skinny_t<bf16>(a, smem_sched, st);
+  return a.dtype == MOE_F32 ? launch_skinny_t<float>(a, R, smem_sched, st)
+                            : launch_skinny_t<bf16>(a, R, smem_sched, st);
 }
 
 cudaError_t launch_gemm_simt(const GemmArgs& a, int bm, cudaStream_t st) {

@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(256) permute_small_kernel(
   int32_t* cnt = sm;             // [E]
   int32_t* off = sm + E;         // [E + 1]
   int32_t* dst = off + E + 1;    // [T_ * k]
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int np = T_ * k;
   for (int e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
   __syncthreads();
@@ -283,15 +283,27 @@ __global__ void __launch_bounds__(256) permute_small_kernel(
   }
   __syncthreads();
   if (x_perm == nullptr) return;   // routing arrays only
-  constexpr int V = 16 / sizeof(T);
+  // the copy: every thread of the block takes 16-byte vectors of the tokens'
+  // rows, four loads in flight before their stores (one token's row is only
+  // a few vectors a thread)
+  constexpr int V = 16 / sizeof(T), U = 4;
   const int nvec = H / V;
-  for (int t = wid; t < T_; t += nw) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)t * H);
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 val = __ldg(src + v);
+  const int total = T_ * nvec;
+  for (int i0 = threadIdx.x; i0 < total; i0 += U * blockDim.x) {
+    uint4 val[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * (int)blockDim.x;
+      if (i < total) val[u] = __ldg(reinterpret_cast<const uint4*>(x + (int64_t)(i / nvec) * H) + i % nvec);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + u * (int)blockDim.x;
+      if (i >= total) break;
+      const int t = i / nvec, v = i % nvec;
       for (int s2 = 0; s2 < k; ++s2) {
         const int d = dst[t * k + s2];
-        if (d >= 0) reinterpret_cast<uint4*>(x_perm + (int64_t)d * H)[v] = val;
+        if (d >= 0) reinterpret_cast<uint4*>(x_perm + (int64_t)d * H)[v] = val[u];
       }
     }
   }

@@ -99,7 +99,7 @@ def test_mxfp8_bitwise_equals_dequantised_bf16(engine, mode):
     assert torch.equal(out["mxfp8"].view(torch.int16), out["bf16"].view(torch.int16))
 
 
-@pytest.mark.parametrize("T", [1, 8, 200])
+@pytest.mark.parametrize("T", [1, 3, 8, 200])
 def test_layer_forward_with_mxfp8_weights(T):
     wl = dataclasses.replace(W.small(W.QWEN2_MOE, T=T, H=512, I=256, I_sh=512, E=16, k=4),
                              weights="mxfp8")

@@ -28,6 +28,9 @@ REDUCED = [
     W.small(W.DEEPSEEK_V3, T=260, H=512, I=256, I_sh=256),
     W.small(W.QWEN2_MOE, T=300, H=512, I=256, I_sh=512),
     W.small(W.QWEN2_MOE, T=5, H=512, I=256, I_sh=512),            # decode-sized
+    W.small(W.QWEN2_MOE, T=1, H=512, I=256, I_sh=512),            # one token: one-row decode tiles
+    W.small(W.QWEN2_MOE, T=3, H=512, I=256, I_sh=512),            # shared MLP in one decode tile
+    W.small(W.ADV_E0, T=1, H=512, I=256, I_sh=256, k=3),          # one token's 3 routes to one expert
     W.small(W.ADV_E0, T=300, H=512, I=256, I_sh=256),
     W.small(W.ADV_ZIPF, T=300, H=512, I=256, I_sh=256),
     W.small(W.QWEN3_30B_A3B, T=100, H=256, I=128, E=64, k=40),    # k+1 > 32: warp top-k
