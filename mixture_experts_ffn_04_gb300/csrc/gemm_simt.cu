@@ -320,10 +320,11 @@ __device__ void block_schedule(const GemmArgs& a, int bm, int32_t* sched, int la
 // 16), so each weight load is 16 bytes for MXFP8 too; the chunk order per
 // lane is the same with and without MX, so both give the same sums.
 template <typename T, int MODE, bool MX = false, bool PAIR = false, int R = kSkR>
-// One-row tiles (bf16 weights) ask for two blocks an SM: the register cap
-// that gives (128) still holds two lane steps of weight loads in flight, and
-// the down projection then needs no stack.  MXFP8's unpacking would spill.
-__global__ void __launch_bounds__(256, R == 1 && !MX ? 2 : 1)
+// One-row tiles (bf16 weights) ask for two blocks an SM (SwiGLU: the cap of
+// 128 registers still holds two lane steps of weight loads in flight) or
+// three (one weight matrix: a down projection's 448 blocks then fit one
+// wave).  MXFP8's unpacking would spill under either cap.
+__global__ void __launch_bounds__(256, R == 1 && !MX ? (MODE == kSwiGLU ? 2 : 3) : 1)
     skinny_kernel(GemmArgs a, int smem_sched, int ks) {
   constexpr int NU = MODE == kSwiGLU ? 2 : 1;
   __shared__ int32_t s_sched[kSkMaxG + 1];
