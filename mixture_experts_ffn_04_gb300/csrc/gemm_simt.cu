@@ -320,11 +320,13 @@ __device__ void block_schedule(const GemmArgs& a, int bm, int32_t* sched, int la
 // 16), so each weight load is 16 bytes for MXFP8 too; the chunk order per
 // lane is the same with and without MX, so both give the same sums.
 template <typename T, int MODE, bool MX = false, bool PAIR = false, int R = kSkR>
-// One-row tiles (bf16 weights) ask for two blocks an SM (SwiGLU: the cap of
-// 128 registers still holds two lane steps of weight loads in flight) or
-// three (one weight matrix: a down projection's 448 blocks then fit one
-// wave).  MXFP8's unpacking would spill under either cap.
-__global__ void __launch_bounds__(256, R == 1 && !MX ? (MODE == kSwiGLU ? 2 : 3) : 1)
+// One-row tiles ask for two blocks an SM (SwiGLU: the cap of 128 registers
+// still holds two lane steps of weight loads in flight) or three (one weight
+// matrix: a down projection's 448 blocks then fit one wave).  With MXFP8
+// weights the one-row loop unpacks each column right before its use, which
+// fits it under those caps (with 24-32 bytes a thread of spill stores, and
+// still faster than one block an SM).
+__global__ void __launch_bounds__(256, R == 1 ? (MODE == kSwiGLU ? 2 : 3) : 1)
     skinny_kernel(GemmArgs a, int smem_sched, int ks) {
   constexpr int NU = MODE == kSwiGLU ? 2 : 1;
   __shared__ int32_t s_sched[kSkMaxG + 1];
@@ -405,6 +407,43 @@ __global__ void __launch_bounds__(256, R == 1 && !MX ? (MODE == kSwiGLU ? 2 : 3)
   if (n0 < a.N) {
 #pragma unroll 2
     for (int cp = c0 + lane; cp < c1; cp += 32) {
+      if constexpr (MX && PAIR && R == 1) {
+        // one row: the packed weights of every column are loaded first (all
+        // loads in flight), then the row's A values, then each column is
+        // unpacked and used at once, so only one column's 16 values are live
+        // (the same FMA order per accumulator as below)
+        uint4 bq[kSkC], uq[MODE == kSwiGLU ? kSkC : 1];
+        uint32_t bs[kSkC], us[MODE == kSwiGLU ? kSkC : 1];
+#pragma unroll
+        for (int q = 0; q < kSkC; ++q) {
+          bq[q] = __ldg(reinterpret_cast<const uint4*>(Bq[q]) + cp);
+          bs[q] = __ldg(reinterpret_cast<const unsigned short*>(Bs[q]) + cp);
+          if (MODE == kSwiGLU) {
+            uq[q] = __ldg(reinterpret_cast<const uint4*>(Uq[q]) + cp);
+            us[q] = __ldg(reinterpret_cast<const unsigned short*>(Us[q]) + cp);
+          }
+        }
+        if (arow[0] >= 0) {
+          float xa[2 * V];
+          unpack16(__ldg(A + arow[0] * nv + cp * 2), xa, (const T*)nullptr);
+          unpack16(__ldg(A + arow[0] * nv + cp * 2 + 1), xa + V, (const T*)nullptr);
+#pragma unroll
+          for (int q = 0; q < kSkC; ++q) {
+            float wv[2 * V];
+            unpack_mx8(make_uint2(bq[q].x, bq[q].y), bs[q] & 0xFFu, wv);
+            unpack_mx8(make_uint2(bq[q].z, bq[q].w), bs[q] >> 8, wv + V);
+#pragma unroll
+            for (int i = 0; i < 2 * V; ++i) acc[0][q] = fmaf(wv[i], xa[i], acc[0][q]);
+            if (MODE == kSwiGLU) {
+              unpack_mx8(make_uint2(uq[q].x, uq[q].y), us[q] & 0xFFu, wv);
+              unpack_mx8(make_uint2(uq[q].z, uq[q].w), us[q] >> 8, wv + V);
+#pragma unroll
+              for (int i = 0; i < 2 * V; ++i) accu[0][q] = fmaf(wv[i], xa[i], accu[0][q]);
+            }
+          }
+        }
+        continue;
+      }
       float w[kSkC][CH * V], u[MODE == kSwiGLU ? kSkC : 1][CH * V];
 #pragma unroll
       for (int q = 0; q < kSkC; ++q) {
