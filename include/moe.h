@@ -73,7 +73,9 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
  * dequantised as they are loaded: on the tensor cores (calls of more than 4
  * rows with K a multiple of 128: e4m3 tiles by TMA, converted in shared
  * memory to the bf16 tile the MMA reads), by the decode engine (up to 4
- * rows) or by the CUDA-core engine (other shapes); results equal those of
+ * rows; otherwise, where the tensor cores cannot take the call, grouped
+ * calls of up to 512 rows and one group of up to 16) or by the CUDA-core
+ * engine (the rest); results equal those of
  * the same engine on the dequantised weights stored in bf16.  The backward
  * does not take MXFP8 weights.  moe_quantize_mxfp8 makes the packed
  * matrices. */
