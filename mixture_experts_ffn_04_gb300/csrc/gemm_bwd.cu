@@ -41,6 +41,7 @@
 // Every wait is bounded; a wait that runs out aborts the kernel cleanly
 // (loads and MMAs in flight are waited for, TMEM is freed, the device status
 // word gets the timeout bit).
+#include <atomic>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -712,7 +713,7 @@ cudaError_t launch_bwd_gemm_tc(const BwdGemmArgs& a, cudaStream_t st) {
     if (mt_bound > a.rows_bound) mt_bound = a.rows_bound;
     tiles_bound = mt_bound * t.NT;
   }
-  static bool attr_done[64] = {false};
+  static std::atomic<bool> attr_done[64];   // per device; several host threads may launch
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;

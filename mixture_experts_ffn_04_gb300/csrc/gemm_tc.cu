@@ -612,13 +612,17 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   if (a.offsets && mt_bound > a.rows_bound) mt_bound = a.rows_bound;  // >= 1 row per tile
   const int64_t tiles_bound = mt_bound * t.NT * t.ksplit;
   static bool attr_done[64] = {false};   // the attribute is per device
+  static std::mutex attr_mu;               // several host threads may launch
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!attr_done[dev]) {
-    e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    attr_done[dev] = true;
+  {
+    std::lock_guard<std::mutex> lock(attr_mu);
+    if (!attr_done[dev]) {
+      e = cudaFuncSetAttribute(tc_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      attr_done[dev] = true;
+    }
   }
   const int grid = (int)(tiles_bound < sm_count() ? tiles_bound : sm_count());
   tc_gemm_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(mA, mB0, mB1, t);

@@ -28,6 +28,7 @@
 // the one-SM engine; a CTA that gives up raises its abort flag, its partner's
 // waits run out in turn, and both meet at the closing cluster barrier before
 // TMEM is released.
+#include <atomic>
 #include "common.cuh"
 #include "internal.h"
 #include "tcgen05.cuh"
@@ -478,7 +479,7 @@ cudaError_t launch_gemm_tc2(const GemmArgs& a, cudaStream_t st) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   // clusters that fit on the GPU at once (per device, queried once)
-  static int max_clusters[64] = {0};
+  static std::atomic<int> max_clusters[64];
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
@@ -491,8 +492,9 @@ cudaError_t launch_gemm_tc2(const GemmArgs& a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
     max_clusters[dev] = n > 0 ? n : -1;
   }
-  if (max_clusters[dev] < 0) return cudaErrorNotSupported;
-  const int64_t ncl = tiles_bound < max_clusters[dev] ? tiles_bound : max_clusters[dev];
+  const int mc = max_clusters[dev].load();
+  if (mc < 0) return cudaErrorNotSupported;
+  const int64_t ncl = tiles_bound < mc ? tiles_bound : mc;
   cfg.gridDim = dim3((unsigned)(2 * ncl));
   e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel, mA, mB0, mB1, t);
   if (e != cudaSuccess) return e;

@@ -27,6 +27,7 @@
 // (16 KB) + scales (4 KB): the weight stream keeps five stages of loads in
 // flight, released as soon as they are converted, not when the MMA is done.
 // Every wait is bounded; a wait that runs out aborts the kernel cleanly.
+#include <atomic>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -448,7 +449,7 @@ cudaError_t launch_gemm_tc_mx(const GemmArgs& a, cudaStream_t st) {
   int64_t mt_bound = a.offsets ? (a.rows_bound + BM - 1) / BM + a.G : (a.single_rows + BM - 1) / BM;
   if (a.offsets && mt_bound > a.rows_bound) mt_bound = a.rows_bound;
   const int64_t tiles_bound = mt_bound * t.NT;
-  static bool attr_done[64] = {false};
+  static std::atomic<bool> attr_done[64];   // per device; several host threads may launch
   int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;

@@ -9,6 +9,7 @@
 //
 // Three launches, no global atomics (rank, scan, scatter + copy; see each
 // kernel below).
+#include <atomic>
 #include "common.cuh"
 #include "internal.h"
 
@@ -309,14 +310,20 @@ __global__ void __launch_bounds__(256) permute_small_kernel(
   }
 }
 
+// SM count of the current device, cached per device (atomics: several host
+// threads may launch)
 int sm_count_cached() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 1;
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) dev = -1;
+  if (dev >= 0) {
+    const int v = cache[dev].load();
+    if (v > 0) return v;
   }
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev < 0 ? 0 : dev);
+  if (n <= 0) n = 1;
+  if (dev >= 0) cache[dev].store(n);
   return n;
 }
 
