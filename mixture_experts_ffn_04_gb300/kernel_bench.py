@@ -7,8 +7,10 @@ reproduce a profile of one kernel at chosen sizes:
 
 ops: gate_up (forward grouped GEMM + SwiGLU), down (forward), dgrad_down
 (dgrad through down with the SwiGLU derivative), dgrad_gate_up, wgrad
-(the down projection's weight gradient), train_step (train-mode forward and
-backward of a named workload, --workload).  Group sizes alternate between
+(the down projection's weight gradient), layer (moe_layer_forward of a named
+workload, --workload, launched from the host: every kernel of the forward in
+order, for launch lists and per-kernel DRAM counters), train_step (train-mode
+forward and backward of a named workload).  Group sizes alternate between
 rows-per-group +- 13 rows, so every group ends inside a 64-row block.
 Prints one JSON line; exits non-zero if the device status word is set."""
 from __future__ import annotations
@@ -45,7 +47,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--op", required=True,
                     choices=["gate_up", "down", "dgrad_down", "dgrad_gate_up", "wgrad",
-                             "train_step"])
+                             "layer", "train_step"])
     ap.add_argument("--groups", type=int, default=64)
     ap.add_argument("--rows-per-group", type=int, default=256)
     ap.add_argument("--hidden", type=int, default=7168)
@@ -60,6 +62,19 @@ def main(argv=None):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
+
+    if a.op == "layer":
+        wl = W.get(a.workload)
+        dev = W.make_inputs(wl, seed=0, device="cuda")
+        layer = m.MoELayer(wl, dev)
+        x = dev["x"]
+        y = torch.empty_like(x)
+        us = _time(lambda: layer.forward(x, y, dev.get("routes_idx"), dev.get("routes_w")),
+                   flush, a.steps, a.warmup)
+        st = layer.device_status()[0]
+        print(json.dumps({"op": a.op, "workload": wl.name, "us": us,
+                          "launches": m.moe_last_launch_count(), "status": st}))
+        return 0 if st == m.MOE_OK else 1
 
     if a.op == "train_step":
         wl = W.get(a.workload)

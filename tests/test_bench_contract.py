@@ -41,8 +41,12 @@ def _check_line(line, n_gpus):
     e2e = d["e2e"]
     assert e2e["value"] == d["value"] and e2e["unit"] == d["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
-    # ms_per_step is the time of one step of the workload's T tokens
-    assert abs(d["ms_per_step"] - 1000.0 * 64 / d["value"]) <= 1e-6 * d["ms_per_step"]
+    # ms_per_step is the time of one step: one pass over the tokens it ran
+    n = d["tokens_per_step"]
+    assert 1 <= n <= 64
+    assert abs(d["ms_per_step"] - 1000.0 * n / d["value"]) <= 1e-6 * d["ms_per_step"]
+    # the same config dict as the GPU arm's line (no arm-specific keys)
+    assert "cuda_graph" not in d["config"]
 
 
 def _json_lines(text):
