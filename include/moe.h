@@ -249,6 +249,10 @@ moe_status moe_permute(const moe_shape *shape, const void *x, const int32_t *top
  *  - Allocates nothing (no cudaMalloc/cudaFree, no allocating library call).
  *  - The first call on a device looks up the array's device address with
  *    that device current; make that first call before any stream capture.
+ *    The address is kept until exit: do not call it on a device after a
+ *    cudaDeviceReset of that device.
+ *  - x_perm may be NULL (then x may be too): only the routing arrays are
+ *    written, as with moe_permute.
  *  - All calls share the array: calls that overlap on the GPU race.
  *  - No device status word: a route outside [0, E) is dropped
  *    (scatter_index -1, not counted), visible as offsets[E] < T*k. */

@@ -18,7 +18,10 @@
 // In host code the symbol is only a host-side stand-in: its device address is
 // looked up once per device with cudaGetSymbolAddress, with that device
 // current, the first time the entry point runs on it.  That first call should
-// therefore come before any stream capture.  Every call shares the array;
+// therefore come before any stream capture.  The address is kept for the life
+// of the process: after a cudaDeviceReset the module is loaded again and the
+// kept address no longer names the array, so the entry point must not be used
+// on a device after that device has been reset.  Every call shares the array;
 // calls that overlap on the GPU (two streams, or two threads) race on it.
 #include <mutex>
 
@@ -77,8 +80,13 @@ extern "C" moe_status moe_permute_static(const moe_shape* shape, const void* x,
     set_error_message("counts and offsets must be non-NULL");
     return MOE_ERR_INVALID_ARG;
   }
-  if (s.T > 0 && (!x || !topk_idx || !scatter_index || !row_token || !x_perm)) {
-    set_error_message("x, topk_idx, scatter_index, row_token, x_perm must be non-NULL");
+  if (s.T > 0 && (!topk_idx || !scatter_index || !row_token)) {
+    set_error_message("topk_idx, scatter_index and row_token must be non-NULL");
+    return MOE_ERR_INVALID_ARG;
+  }
+  // as moe_permute: without x_perm only the routing arrays are written
+  if (s.T > 0 && x_perm && !x) {
+    set_error_message("x_perm needs x");
     return MOE_ERR_INVALID_ARG;
   }
   if (((uintptr_t)x & 15u) || ((uintptr_t)x_perm & 15u)) {
