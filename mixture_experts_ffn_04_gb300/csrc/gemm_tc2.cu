@@ -3,7 +3,8 @@
 // Same contract as the one-SM engine in gemm_tc.cu ("Fused MoE Kernel Notes",
 // group_gemm_same_nk: groups of rows with shared N and K, the m-tile schedule
 // built from the real group sizes).  The two CTAs of a cluster share one
-// 256 x 256 output tile: CTA r keeps rows 128r .. 128r+127 of the A tile and
+// 256 x 256 output tile (a group's last tile, when at most 128 of its rows
+// are left, is a half tile: M = 128, see IDESC_HALF): CTA r keeps rows 128r .. 128r+127 of the A tile and
 // rows (N) 128r .. 128r+127 of the B tile in its own shared memory, and the
 // even CTA's MMA thread issues tcgen05.mma.cta_group::2 (M = 256, N = 256,
 // K = 16), which reads both CTAs' operands and writes each CTA's 128 rows x
@@ -31,6 +32,7 @@
 #include <atomic>
 #include "common.cuh"
 #include "internal.h"
+#include "tc_pair.cuh"
 #include "tcgen05.cuh"
 
 namespace moe {
@@ -53,13 +55,25 @@ constexpr int SCHED_BYTES = (MAX_SMEM_G + 1) * 4;
 constexpr int OUT_ROW_BYTES = 80;
 constexpr int OUT_WARP_BYTES = 32 * OUT_ROW_BYTES;
 constexpr int OUT_BYTES = 4 * OUT_WARP_BYTES;
-constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES + OUT_BYTES + SCHED_BYTES;
+// half tiles with SwiGLU: the up values of a 32 x 32 chunk handed from the
+// warps holding TMEM lanes 64-127 to those holding lanes 0-63 (fp32, [32][33]
+// for each of the two warp pairs)
+constexpr int XCH_STRIDE = 33;
+constexpr int XCH_BYTES = 2 * 32 * XCH_STRIDE * 4;
+constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES + OUT_BYTES + XCH_BYTES + SCHED_BYTES;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
-static_assert((2 * S + 5) * 8 + 8 <= BAR_BYTES, "barrier area");
+static_assert((2 * S + 5) * 8 + 12 <= BAR_BYTES, "barrier area");
 // kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major,
 // N >> 3 at bits 17-22, M >> 4 at bits 24-28 (M = 256 across the pair).
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
                            ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BMP >> 4) << 24);
+// The last tile of a group with at most 128 rows left is a half tile: M = 128
+// over the pair (64 rows a CTA), full MMA rate per row, so it costs half a
+// tile instead of a whole one.  Its accumulator takes 128 TMEM columns: lane
+// l < 64 holds row l of the CTA's half, columns 0-127 of the tile's N; lane
+// 64 + l the same row, columns 128-255.
+constexpr uint32_t IDESC_HALF = (1u << 4) | (1u << 7) | (1u << 10) |
+                                ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((BMP / 2) >> 4) << 24);
 
 struct Args {
   int mode, N, K, G, NT, KB;
@@ -72,164 +86,31 @@ struct Args {
   uint32_t* flags;
 };
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// The same shared-memory offset in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-               : "memory");
-}
-// Cluster-scope test of a barrier phase (test_wait: never suspends the
-// thread).  Every wait of this kernel polls with it.
-__device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}\n"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-// Bounded wait (about 2 s of SM clocks, then the abort flag).
-__device__ __forceinline__ bool wait2(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-  if (mbar_test_cluster(bar, parity)) return true;
-  const long long t0 = clock64();
-  while (true) {
-    if (mbar_test_cluster(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
-      *abort_flag = 1;
-      return false;
-    }
-  }
-}
-__device__ __forceinline__ void wait2_quiet(uint32_t bar, uint32_t parity) {
-  const long long t0 = clock64();
-  while (!mbar_test_cluster(bar, parity))
-    if (clock64() - t0 > kWaitCycles) return;
-}
-// TMA tile loads into this CTA's shared memory whose completion is counted
-// on a barrier of the even CTA (cta_group::2 form: the barrier may sit in
-// either CTA of the pair; `bar` is its cluster address).
-__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0,
-                                                 int c1, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int c0,
-                                                 int c1, int c2, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
-               "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_alloc2(uint32_t dst_smem, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
-               "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_relinquish2() {
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc2(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-               : "memory");
-}
-__device__ __forceinline__ void mma2(uint32_t d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                     uint32_t accum) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accum)
-      : "memory");
-}
-// Arrive (once) on the barrier at this offset in both CTAs of the pair when
-// every tcgen05 operation issued so far by this thread has completed.
-__device__ __forceinline__ void commit2_both(uint32_t bar) {
-  const uint16_t mask = 0x3;
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
-__device__ __forceinline__ void commit2_self(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-
-// Pair tile -> (group, pair m-tile, n-tile): n-tile major, pair m-tile minor
-// within a group.
+// Pair tile -> (group, pair m-tile, n-tile), pair m-tiles of BMP rows.
 __device__ __forceinline__ void decode_tile(const Args& a, const int32_t* sched, int64_t tile,
                                             int& g, int& mp, int& nt) {
-  int lo = 0, hi = a.G;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if ((int64_t)sched[mid] * a.NT <= tile) lo = mid; else hi = mid;
-  }
-  g = lo;
-  const int mtg = sched[g + 1] - sched[g];
-  const int64_t local = tile - (int64_t)sched[g] * a.NT;
-  nt = (int)(local / mtg);
-  mp = (int)(local % mtg);
+  pair_decode_tile(a, sched, tile, g, mp, nt);
+}
+__device__ void build_schedule(const Args& a, int32_t* sched, int lane) {
+  pair_schedule<BMP>(a, sched, lane);
 }
 
-// Prefix of ceil(rows_g / 256) over the groups (one warp, shared memory);
-// sched[G] = 0 when the offsets are inconsistent or exceed the row bound.
-__device__ void build_schedule(const Args& a, int32_t* sched, int lane) {
-  int carry = 0;
-  bool bad = false;
-  for (int base = 0; base < a.G; base += 32) {
-    const int g = base + lane;
-    int v = 0;
-    if (g < a.G) {
-      int64_t cnt = a.offsets ? (int64_t)a.offsets[g + 1] - a.offsets[g] : a.single_rows;
-      if (cnt < 0) { bad = true; cnt = 0; }
-      v = (int)((cnt + BMP - 1) / BMP);
-    }
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
-    }
-    if (g < a.G) sched[g] = carry + incl - v;
-    carry += __shfl_sync(0xffffffffu, incl, 31);
-  }
-  if (lane == 0) {
-    if (a.offsets) bad |= a.offsets[0] != 0 || (int64_t)a.offsets[a.G] > a.rows_bound;
-    else bad |= a.single_rows > a.rows_bound || a.single_rows < 0;
-  }
-  bad = __any_sync(0xffffffffu, bad);
-  if (lane == 0) {
-    sched[a.G] = bad ? 0 : carry;
-    if (bad && blockIdx.x == 0) set_flag(a.flags, kFlagRows);
-  }
+// Rows of the group left from pair m-tile mp on (> 0 for every scheduled tile).
+__device__ __forceinline__ int64_t tile_rows_left(const Args& a, int g, int mp) {
+  const int64_t gbeg = a.offsets ? a.offsets[g] : 0;
+  const int64_t gend = a.offsets ? a.offsets[g + 1] : a.single_rows;
+  return gend - (gbeg + (int64_t)mp * BMP);
+}
+
+// Named barrier of the four epilogue warps (barrier 0 is __syncthreads).
+__device__ __forceinline__ void epi_bar() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
-    tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                    const __grid_constant__ CUtensorMap tmB1, const Args a) {
+    tc2_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA64,
+                    const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                    const Args a) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -237,8 +118,10 @@ __global__ void __launch_bounds__(THREADS, 1)
   // bars: full[S] empty[S] tfull[2] tempty[2] final
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* s_ok = reinterpret_cast<volatile int*>(tmem_slot + 2);
   unsigned char* s_out = smem + RING_BYTES + BAR_BYTES;
-  int32_t* s_sched = reinterpret_cast<int32_t*>(s_out + OUT_BYTES);
+  float* s_xch = reinterpret_cast<float*>(s_out + OUT_BYTES);
+  int32_t* s_sched = reinterpret_cast<int32_t*>(s_out + OUT_BYTES + XCH_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();
@@ -281,6 +164,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   if ((warp == 0 || warp == 6) && lane == 0) {
     // ---------------- TMA producers ----------------
     const bool is_a = warp == 0;
+    const CUtensorMap* bmap = (a.mode == kSwiGLU && rank == 1) ? &tmB1 : &tmB0;
+    auto b_row = [&](int nt) { return a.mode == kSwiGLU ? nt * BNC : nt * BN + (int)rank * BNC; };
     int s = 0;
     uint32_t ph = 0, issued = 0, par = 0;
     bool ok = true;
@@ -288,17 +173,17 @@ __global__ void __launch_bounds__(THREADS, 1)
       int g, mp, nt;
       decode_tile(a, sched, tile, g, mp, nt);
       const int64_t gbase = a.offsets ? a.offsets[g] : 0;
-      const int arow = (int)(gbase + (int64_t)mp * BMP + (int64_t)rank * BMC);
-      const int brow = a.mode == kSwiGLU ? nt * BNC : nt * BN + (int)rank * BNC;
-      const CUtensorMap* bmap = (a.mode == kSwiGLU && rank == 1) ? &tmB1 : &tmB0;
+      const bool half = tile_rows_left(a, g, mp) <= BMC;
+      const int arow = (int)(gbase + (int64_t)mp * BMP + (int64_t)rank * (half ? BMC / 2 : BMC));
+      const int brow = b_row(nt);
       for (int kb = 0; kb < a.KB; ++kb) {
         if (!wait2(empty(s), ph ^ 1u, abort_flag)) { ok = false; break; }
         const uint32_t st = ring + s * STAGE_BYTES;
         // the even CTA's "full" barrier counts both CTAs' bytes; only the
         // even CTA's producers arrive on it (with the pair's byte count)
         const uint32_t fb = map_to_rank(full(s), 0);
-        if (leader) mbar_expect_tx(full(s), 2 * (is_a ? A_BYTES : B_BYTES));
-        if (is_a) tma_load_2d_pair(st, &tmA, kb * BK, arow, fb);
+        if (leader) mbar_expect_tx(full(s), 2 * (is_a ? (half ? A_BYTES / 2 : A_BYTES) : B_BYTES));
+        if (is_a) tma_load_2d_pair(st, half ? &tmA64 : &tmA, kb * BK, arow, fb);
         else tma_load_3d_pair(st + A_BYTES, bmap, kb * BK, brow, g, fb);
         issued |= 1u << s;
         par = (par & ~(1u << s)) | (ph << s);
@@ -318,6 +203,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t ph = 0, aph = 0;
     bool ok = true;
     for (int64_t tile = cl; tile < total && ok; tile += ncl) {
+      int g, mp, nt;
+      decode_tile(a, sched, tile, g, mp, nt);
+      const uint32_t idesc = tile_rows_left(a, g, mp) <= BMC ? IDESC_HALF : IDESC;
       if (!wait2(tempty(acc), aph ^ 1u, abort_flag)) break;
       tc_fence_after();
       const uint32_t d = tmem_base + (uint32_t)acc * BN;
@@ -330,7 +218,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t st = ring + s * STAGE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-          mma2(d, sw128_desc(st + kk * 32), sw128_desc(st + A_BYTES + kk * 32), IDESC,
+          mma2(d, sw128_desc(st + kk * 32), sw128_desc(st + A_BYTES + kk * 32), idesc,
                (kb | kk) != 0 ? 1u : 0u);
         commit2_both(empty(s));
         if (++s == S) { s = 0; ph ^= 1u; }
@@ -347,67 +235,133 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else if (warp >= 2 && warp <= 5) {
     // ---------------- epilogue (warps 2..5, both CTAs) ----------------
     const int q = warp & 3;   // TMEM lanes 32q .. 32q+31 of this CTA
+    const int et = threadIdx.x - 64;   // 0 .. 127
     unsigned char* stage = s_out + (warp - 2) * OUT_WARP_BYTES;
     unsigned char* my_row = stage + lane * OUT_ROW_BYTES;
+    const bool swiglu = a.mode == kSwiGLU;
+    bf16* out = reinterpret_cast<bf16*>(a.out);
     int acc = 0;
     uint32_t aph = 0;
+    // a 32 x 32 chunk of finished rows (my_row of each lane) to global rows
+    // row0 .. row0+31 (nvalid of them), columns n .. n+31
+    auto store_chunk = [&](const uint4 (&packed)[4], int64_t row0, int nvalid, int n) {
+#pragma unroll
+      for (int v = 0; v < 4; ++v) reinterpret_cast<uint4*>(my_row)[v] = packed[v];
+      __syncwarp();
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int p = lane + 32 * i;   // 128 pieces: 32 rows x 4 x 16 B
+        const int rr = p >> 2, pc = p & 3;
+        const int col = n + pc * 8;
+        if (rr < nvalid && col < a.N)
+          *reinterpret_cast<uint4*>(out + (row0 + rr) * a.ldo + col) =
+              *reinterpret_cast<const uint4*>(stage + rr * OUT_ROW_BYTES + pc * 16);
+      }
+      __syncwarp();
+    };
     for (int64_t tile = cl; tile < total; tile += ncl) {
       int g, mp, nt;
       decode_tile(a, sched, tile, g, mp, nt);
       const int64_t gbeg = a.offsets ? a.offsets[g] : 0;
       const int64_t gend = a.offsets ? a.offsets[g + 1] : a.single_rows;
-      const int64_t row0 = gbeg + (int64_t)mp * BMP + (int64_t)rank * BMC + q * 32;
-      const int64_t nvalid64 = gend - row0;
-      const int nvalid = nvalid64 < 0 ? 0 : (nvalid64 > 32 ? 32 : (int)nvalid64);
-      int okw = 0;   // one lane polls; the warp follows its result
-      if (lane == 0) okw = wait2(tfull(acc), aph, abort_flag) ? 1 : 0;
-      if (!__shfl_sync(0xffffffffu, okw, 0)) break;
+      const bool half = tile_rows_left(a, g, mp) <= BMC;
+      // one thread waits for the accumulator; the four warps follow its
+      // result together (the half tiles' hand-over meets at named barriers)
+      if (et == 0) *s_ok = wait2(tfull(acc), aph, abort_flag) ? 1 : 0;
+      epi_bar();
+      const int okv = *s_ok;
+      epi_bar();
+      if (!okv) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * BN;
-      const bool swiglu = a.mode == kSwiGLU;
-      const int n0 = swiglu ? nt * BNC : nt * BN;
-      const int ncols = swiglu ? BN / 2 : BN;
-      bf16* out = reinterpret_cast<bf16*>(a.out);
+      if (!half) {
+        const int64_t row0 = gbeg + (int64_t)mp * BMP + (int64_t)rank * BMC + q * 32;
+        const int64_t nvalid64 = gend - row0;
+        const int nvalid = nvalid64 < 0 ? 0 : (nvalid64 > 32 ? 32 : (int)nvalid64);
+        const int n0 = swiglu ? nt * BNC : nt * BN;
+        const int ncols = swiglu ? BN / 2 : BN;
 #pragma unroll 1
-      for (int c = 0; c < ncols && n0 + c < a.N; c += 32) {
-        uint32_t gr[32];
-        uint4 packed[4];
-        tmem_ld32(taddr + c, gr);
-        if (swiglu) {
-          uint32_t ur[32];
-          tmem_ld32(taddr + BN / 2 + c, ur);
-          tmem_wait_ld();
+        for (int c = 0; c < ncols && n0 + c < a.N; c += 32) {
+          uint32_t gr[32];
+          uint4 packed[4];
+          tmem_ld32(taddr + c, gr);
+          if (swiglu) {
+            uint32_t ur[32];
+            tmem_ld32(taddr + BN / 2 + c, ur);
+            tmem_wait_ld();
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float f[8];
+            for (int v = 0; v < 4; ++v) {
+              float f[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              f[e] = silu_fast(__uint_as_float(gr[v * 8 + e])) * __uint_as_float(ur[v * 8 + e]);
-            packed[v] = pack16(f, (const bf16*)nullptr);
+              for (int e = 0; e < 8; ++e)
+                f[e] = silu_fast(__uint_as_float(gr[v * 8 + e])) * __uint_as_float(ur[v * 8 + e]);
+              packed[v] = pack16(f, (const bf16*)nullptr);
+            }
+          } else {
+            tmem_wait_ld();
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(gr[v * 8 + e]);
+              packed[v] = pack16(f, (const bf16*)nullptr);
+            }
+          }
+          store_chunk(packed, row0, nvalid, n0 + c);
+        }
+      } else {
+        // half tile: the CTA's 64 rows; warps q and q + 2 hold the same 32
+        // rows, q < 2 columns 0-127 of the tile's N, q >= 2 columns 128-255
+        const int64_t row0 = gbeg + (int64_t)mp * BMP + (int64_t)rank * (BMC / 2) + (q & 1) * 32;
+        const int64_t nvalid64 = gend - row0;
+        const int nvalid = nvalid64 < 0 ? 0 : (nvalid64 > 32 ? 32 : (int)nvalid64);
+        if (!swiglu) {
+          const int n0 = nt * BN + (q >> 1) * (BN / 2);
+#pragma unroll 1
+          for (int c = 0; c < BN / 2 && n0 + c < a.N; c += 32) {
+            uint32_t gr[32];
+            uint4 packed[4];
+            tmem_ld32(taddr + c, gr);
+            tmem_wait_ld();
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              float f[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(gr[v * 8 + e]);
+              packed[v] = pack16(f, (const bf16*)nullptr);
+            }
+            store_chunk(packed, row0, nvalid, n0 + c);
           }
         } else {
-          tmem_wait_ld();
+          // gate columns in lanes 0-63, the matching up columns in lanes
+          // 64-127: warp q + 2 hands its up values to warp q through s_xch
+          const int n0 = nt * BNC;
+          float* xrow = s_xch + ((q & 1) * 32 + lane) * XCH_STRIDE;
+#pragma unroll 1
+          for (int c = 0; c < BNC && n0 + c < a.N; c += 32) {   // same trip count in all four warps
+            uint32_t r[32];
+            tmem_ld32(taddr + c, r);
+            tmem_wait_ld();
+            if (q >= 2) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float f[8];
+              for (int e = 0; e < 32; ++e) xrow[e] = __uint_as_float(r[e]);
+            }
+            epi_bar();
+            if (q < 2) {
+              uint4 packed[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(gr[v * 8 + e]);
-            packed[v] = pack16(f, (const bf16*)nullptr);
+              for (int v = 0; v < 4; ++v) {
+                float f[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                  f[e] = silu_fast(__uint_as_float(r[v * 8 + e])) * xrow[v * 8 + e];
+                packed[v] = pack16(f, (const bf16*)nullptr);
+              }
+              store_chunk(packed, row0, nvalid, n0 + c);
+            }
+            epi_bar();   // s_xch is written again only after every read of this chunk
           }
         }
-#pragma unroll
-        for (int v = 0; v < 4; ++v) reinterpret_cast<uint4*>(my_row)[v] = packed[v];
-        __syncwarp();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int p = lane + 32 * i;   // 128 pieces: 32 rows x 4 x 16 B
-          const int rr = p >> 2, pc = p & 3;
-          const int n = n0 + c + pc * 8;
-          if (rr < nvalid && n < a.N)
-            *reinterpret_cast<uint4*>(out + (row0 + rr) * a.ldo + n) =
-                *reinterpret_cast<const uint4*>(stage + rr * OUT_ROW_BYTES + pc * 16);
-        }
-        __syncwarp();
       }
       tc_fence_before();
       mbar_arrive_cluster(map_to_rank(tempty(acc), 0));
@@ -442,7 +396,9 @@ cudaError_t launch_gemm_tc2(const GemmArgs& a, cudaStream_t st) {
   const int64_t rows = a.offsets ? a.rows_bound : a.single_rows;
   if (rows <= 0) return cudaSuccess;
   CUtensorMap mA, mB0, mB1;
+  CUtensorMap mA64;
   if (!tc::make_map_2d(&mA, a.A, rows, a.K, BMC)) return cudaErrorInvalidValue;
+  if (!tc::make_map_2d(&mA64, a.A, rows, a.K, BMC / 2)) return cudaErrorInvalidValue;
   if (!tc::make_map_3d(&mB0, a.B0, a.N, a.K, a.G, a.bstride, BNC)) return cudaErrorInvalidValue;
   if (a.mode == kSwiGLU) {
     if (!tc::make_map_3d(&mB1, a.B1, a.N, a.K, a.G, a.bstride, BNC)) return cudaErrorInvalidValue;
@@ -496,7 +452,7 @@ cudaError_t launch_gemm_tc2(const GemmArgs& a, cudaStream_t st) {
   if (mc < 0) return cudaErrorNotSupported;
   const int64_t ncl = tiles_bound < mc ? tiles_bound : mc;
   cfg.gridDim = dim3((unsigned)(2 * ncl));
-  e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel, mA, mB0, mB1, t);
+  e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel, mA, mA64, mB0, mB1, t);
   if (e != cudaSuccess) return e;
   count_launch();
   return cudaGetLastError();

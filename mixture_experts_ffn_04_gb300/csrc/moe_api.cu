@@ -177,13 +177,13 @@ static int engine_for(const GemmArgs& a) {
   if (ov == 4) return pair_ok ? 4 : 2;
   if (ov >= 1 && ov <= 3) return ov;
   if (rows <= 4) return 3;
-  // SM pairs halve the weight bytes each SM buffers (more loads in flight)
-  // but round every group up to 256 rows instead of 128: they pay off for one
-  // big group (the shared MLP) and for large routed groups.  Measured on the
-  // layer: DeepSeek-V3-shaped routed GEMMs (256 rows a group) 4-7 % slower on
-  // pairs, its shared MLP about a third faster; all-to-one and Zipf routing
-  // 9-11 % faster end to end.
-  if (pair_ok && rows >= 512 && (a.G == 1 || (a.offsets && rows / a.G >= 1024))) return 4;
+  // SM pairs: a 64-wide k-block needs 32 KB of operands per SM instead of
+  // 48 KB (six stages instead of four) for the same MMA work, and a group's
+  // last tile with at most 128 rows left runs at M = 128 (half the MMA time),
+  // so the row padding is that of 128-row tiles.  Measured level with or
+  // slightly ahead of the one-SM engine on every prefill-sized workload, a
+  // third faster on one big group (the shared MLP).
+  if (pair_ok && rows >= 512) return 4;
   return 2;
 }
 

@@ -55,10 +55,14 @@ def main(argv=None):
     ap.add_argument("--workload", default="qwen3-30b-a3b-shape-T4096")
     ap.add_argument("--weights", default="act", choices=["act", "mxfp8"],
                     help="gate_up / down: expert weights packed as MXFP8 (moe_quantize_mxfp8)")
+    ap.add_argument("--engine", type=int, default=0,
+                    help="grouped-GEMM engine forced for the run (moe_testing_set_gemm_engine; "
+                         "0 = the library's choice)")
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=2)
     a = ap.parse_args(argv)
     torch.cuda.set_device(0)
+    m.moe_testing_set_gemm_engine(a.engine)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
@@ -72,7 +76,7 @@ def main(argv=None):
         us = _time(lambda: layer.forward(x, y, dev.get("routes_idx"), dev.get("routes_w")),
                    flush, a.steps, a.warmup)
         st = layer.device_status()[0]
-        print(json.dumps({"op": a.op, "workload": wl.name, "us": us,
+        print(json.dumps({"op": a.op, "workload": wl.name, "engine": a.engine, "us": us,
                           "launches": m.moe_last_launch_count(), "status": st}))
         return 0 if st == m.MOE_OK else 1
 
@@ -148,7 +152,8 @@ def main(argv=None):
         flops = 2.0 * R * H * I
     us = _time(fn, flush, a.steps, a.warmup)
     st = m.moe_get_device_status(ws)[0]
-    print(json.dumps({"op": a.op, "weights": a.weights, "groups": E, "rows": R, "hidden": H,
+    print(json.dumps({"op": a.op, "engine": a.engine, "weights": a.weights, "groups": E,
+                      "rows": R, "hidden": H,
                       "inter": I, "us": us,
                       "tflops": flops / us / 1e6, "status": st}))
     return 0 if st == m.MOE_OK else 1

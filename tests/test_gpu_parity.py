@@ -90,7 +90,7 @@ def test_full_size_parity(wl, sample):
           "launches=%d" % (wl.name, out["rel_l2"], out["worst_token_rel_l2"],
                            out["tokens_checked"], out["ties"], out["max_group"], out["launches"]))
     if sample == "tiles":
-        assert out["tokens_checked"] >= min(wl.T, 128)
+        assert out["tokens_checked"] >= min(wl.T, 64)
     del dev, res
     torch.cuda.empty_cache()
 
@@ -243,13 +243,16 @@ def test_rows_beyond_bound_set_device_flag(engine):
     assert bool((h.float() == 7.0).all())  # nothing was computed
 
 
-@pytest.mark.parametrize("groups", [[1000], [300, 0, 513, 7, 256, 257]],
-                         ids=["one-group", "ragged-groups"])
+@pytest.mark.parametrize("groups", [[1000], [300, 0, 513, 7, 256, 257],
+                                    [1, 16, 17, 33, 0, 255, 257, 384, 385, 512, 8, 9, 130]],
+                         ids=["one-group", "ragged-groups", "small-and-half-tile-edges"])
 def test_sm_pair_engine_matches_one_sm_engine(groups):
-    """The SM-pair engine (256-row tiles over two CTAs) gives the one-SM
-    engine's h and y_perm bit for bit: the same fp32 sums in the same k order,
-    one rounding.  Ragged N and K (N = 200, K = 328), empty groups, groups of
-    one tile and of one row past a tile."""
+    """The SM-pair engine (256-row tiles over two CTAs; a group's last tile of
+    at most 128 rows as an M = 128 half tile) gives the one-SM engine's h and
+    y_perm bit for bit: the same fp32 sums in the same k order, one rounding.
+    Ragged N and K (N = 200, K = 328), empty groups, groups of one tile and
+    of one row past a tile, and groups whose last tile has 1, 128 and 129
+    rows (half tile, half tile, full tile)."""
     G = len(groups)
     rows = sum(groups)
     H, I = 328, 200
@@ -274,7 +277,7 @@ def test_sm_pair_engine_matches_one_sm_engine(groups):
             m.moe_testing_set_gemm_engine(prev)
         torch.cuda.synchronize()
         assert m.moe_get_device_status(ws)[0] == m.MOE_OK
-        assert torch.isfinite(yp.float()).all()
+        assert torch.isfinite(h.float()).all() and torch.isfinite(yp.float()).all()
         out[e] = (h, yp)
     assert torch.equal(out[2][0].view(torch.int16), out[4][0].view(torch.int16))
     assert torch.equal(out[2][1].view(torch.int16), out[4][1].view(torch.int16))
