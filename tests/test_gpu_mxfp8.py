@@ -52,11 +52,43 @@ def test_quantizer_matches_oracle(dtype):
         assert np.array_equal(got[b], MX.pack(c, s)), b
 
 
-def _grouped_pair(engine, mode):
+# every finite e4m3 code: all bytes but the two NaN codes (S.1111.111)
+FINITE_CODES = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+
+
+def extreme_packed(packed: torch.Tensor, N: int, K: int, seed: int, high: int) -> torch.Tensor:
+    """Packed matrices [G, N*K*9/8] rewritten so that each holds every finite
+    e4m3 code (both zeros, the subnormals, +-448) at seeded positions, and
+    scale bytes at both ends of the range: 10-12 (the smallest codes still
+    bf16 normals) and high-4 .. high (values up to 448 * 2^(high-127)), with
+    at most one high-scale block per row so the outputs stay finite.  The
+    rest keep their drawn codes and scales."""
+    rng = np.random.default_rng(seed)
+    out = packed.cpu().numpy().copy()
+    nk = N * K
+    for b in range(out.shape[0]):
+        codes = out[b, :nk]
+        pos = rng.choice(nk, size=FINITE_CODES.size, replace=False)
+        codes[pos] = FINITE_CODES
+        scales = out[b, nk:].reshape(N, K // 8)
+        for n in range(N):
+            lo = rng.choice(K // 8, size=2, replace=False)
+            scales[n, lo] = rng.integers(10, 13, size=2)
+            if n % 3 == 0:
+                scales[n, rng.integers(0, K // 8)] = rng.integers(high - 4, high + 1)
+    return torch.from_numpy(out).to(packed.device)
+
+
+def _grouped_pair(engine, mode, extreme=False):
     E, H, I, T, k = 6, 256, 128, 7, 4
     wl = dataclasses.replace(W.small(W.QWEN2_MOE, T=T, H=H, I=I, I_sh=0, E=E, k=k), weights="mxfp8",
                              shared_gate=False)
     d = W.make_inputs(wl, seed=2, device="cuda")
+    if extreme:
+        # gate and up share a row's output (silu(g) * u): a lower top scale
+        d["w_gate"] = extreme_packed(d["w_gate"], I, H, 11, 175)
+        d["w_up"] = extreme_packed(d["w_up"], I, H, 12, 175)
+        d["w_down"] = extreme_packed(d["w_down"], H, I, 13, 240)
     idx = torch.randint(0, E, (T, k), generator=torch.Generator().manual_seed(0)).int()
     counts, offsets, sidx, row_token = O.permute(idx.numpy(), E)
     R = T * k
@@ -93,10 +125,29 @@ def _grouped_pair(engine, mode):
 @pytest.mark.parametrize("engine", [3, 1, 2], ids=["decode-engine", "cuda-core-engine",
                                                   "tensor-core-engine"])
 @pytest.mark.parametrize("mode", ["swiglu", "down"])
-def test_mxfp8_bitwise_equals_dequantised_bf16(engine, mode):
-    out = _grouped_pair(engine, mode)
+@pytest.mark.parametrize("extreme", [False, True], ids=["drawn-codes", "every-code-extreme-scales"])
+def test_mxfp8_bitwise_equals_dequantised_bf16(engine, mode, extreme):
+    out = _grouped_pair(engine, mode, extreme)
     assert torch.isfinite(out["mxfp8"].float()).all()
     assert torch.equal(out["mxfp8"].view(torch.int16), out["bf16"].view(torch.int16))
+
+
+def test_extreme_packed_holds_every_code_and_both_scale_ends():
+    """The rewritten matrices hold what the bitwise test claims (checked on
+    the host before any engine sees them)."""
+    E, N, K = 2, 16, 256
+    base = torch.zeros(E, N * K // 8 * 9, dtype=torch.uint8)
+    base[:, N * K:] = 120
+    p = extreme_packed(base, N, K, 0, 240).numpy()
+    for b in range(E):
+        assert set(FINITE_CODES.tolist()) <= set(np.unique(p[b, :N * K]).tolist())
+        sc = p[b, N * K:]
+        assert sc.min() <= 12
+        assert sc.max() >= 236
+        v = MX.dequantize(*MX.unpack(p[b], N, K))
+        assert np.isfinite(v).all()
+        nz = np.abs(v[v != 0])
+        assert nz.min() >= 2.0 ** -126 and nz.max() <= 448.0 * 2.0 ** 113
 
 
 @pytest.mark.parametrize("T", [1, 3, 8, 200])
