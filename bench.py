@@ -47,18 +47,25 @@ PER_CONFIG = ("tiny-f32-T64", "qwen3-30b-a3b-shape-T4096", "qwen2-moe-shape-T204
 METRIC = "MoE layer tokens/s and grouped-GEMM TFLOP/s (% bf16 peak) on 1 GB300"
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one gate/up grouped-GEMM
-# launch, from an ncu capture, keyed by workload; valid only while the kernel
-# source hashes to the recorded value.
+# launch, from an ncu capture, keyed by workload; valid only while the device
+# code of the engine that ran it hashes to the recorded value.
 NCU_TRAFFIC = {
-    # profiles/tc_gemm_qwen3-30b-a3b-shape-T4096.md
+    # profiles/launches_qwen3-30b-a3b-shape-T4096.md (one-SM engine, before the
+    # SM-pair engine became the default for prefill-sized calls)
     "qwen3-30b-a3b-shape-T4096": {"bytes": 987034880, "kernel_hash": "483aa0cf870cd816"},
 }
 
 
-def _kernel_hash() -> str:
-    """Hash of the one-SM GEMM's device code: its PTX wrappers and the part of
-    gemm_tc.cu above the host-side launcher."""
+def _kernel_hash(engine: str = "tc_gemm_kernel") -> str:
+    """Hash of a grouped GEMM engine's device code: its PTX wrappers and the
+    part of its source above the host-side launcher."""
     d = os.path.join(ROOT, "mixture_experts_ffn_04_gb300", "csrc")
+    if engine == "tc2_gemm_kernel":
+        src = open(os.path.join(d, "gemm_tc2.cu"), "rb").read()
+        h = hashlib.sha256(open(os.path.join(d, "tcgen05.cuh"), "rb").read())
+        h.update(open(os.path.join(d, "tc_pair.cuh"), "rb").read())
+        h.update(src[:src.index(b"cudaError_t launch_gemm_tc2(")])
+        return h.hexdigest()[:16]
     src = open(os.path.join(d, "gemm_tc.cu"), "rb").read()
     h = hashlib.sha256(open(os.path.join(d, "tcgen05.cuh"), "rb").read())
     h.update(src[:src.index(b"// host side")])
@@ -482,8 +489,10 @@ def gate_up_roofline(wl, alg, gu_ms, peaks):
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s",
                 "frac": ach / peaks["hbm"]}
     tr = NCU_TRAFFIC.get(wl.name)
-    roof["traffic"] = tr["bytes"] if tr and tr.get("kernel_hash") == _kernel_hash() else None
     roof["kernel"] = gate_up_kernel_name(wl)
+    engine = roof["kernel"].split(" ")[0]
+    roof["traffic"] = (tr["bytes"] if tr and tr.get("kernel_hash") == _kernel_hash(engine)
+                       else None)
     roof["kernel_ms"] = gu_ms
     roof["peak_source"] = peaks["source"] + (" burst" if roof["bound"] == "tensor" else " copy")
     roof["algorithmic_per_launch"] = (alg["gu_flops"] if roof["bound"] == "tensor"
@@ -499,6 +508,11 @@ def gate_up_kernel_name(wl):
         return "skinny_kernel (decode engine: gate/up + SwiGLU)"
     if wl.weights == "mxfp8" and wl.H % 128 == 0:
         return "tc_mx_kernel (gate/up grouped GEMM + SwiGLU, MXFP8 weights)"
+    if wl.dtype == "f32":
+        return "simt_gemm_kernel (gate/up grouped GEMM + SwiGLU, fp32 on the CUDA cores)"
+    rows = wl.T * wl.k
+    if rows >= 512 and (rows // wl.E >= 1024 or wl.H >= 3072):
+        return "tc2_gemm_kernel (gate/up grouped GEMM + SwiGLU on SM pairs)"
     return "tc_gemm_kernel (gate/up grouped GEMM + SwiGLU)"
 
 

@@ -49,7 +49,20 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int RING_BYTES = S * STAGE_BYTES;
 constexpr int THREADS = 224;            // warps 0-6
 constexpr uint32_t TMEM_COLS = 512;     // two 256-column accumulators
-constexpr int BAR_BYTES = 256;
+constexpr int BAR_BYTES = 512;
+// Dynamic tile order: the even CTA's A producer takes tiles from a counter in
+// global memory (atomicAdd) and hands each tile number to every role of both
+// CTAs through a ring of NSLOT shared-memory slots, so the tiles in progress
+// across the GPU always form one window of consecutive tile numbers (a static
+// round-robin drifts apart, and then the CTAs that share a weight tile no
+// longer read it while it is in L2).
+constexpr int NSLOT = 4;
+// A group of at least this many pair m-tiles is ordered m-tile major when
+// its weights fit in half the L2 (they stay there while every m-tile passes
+// over them); other groups n-tile major (the m-tiles sharing a weight tile
+// run side by side, and a weight tile is read from DRAM once).
+constexpr int MMAJOR_TILES = 8;
+constexpr int64_t MMAJOR_WEIGHT_BYTES = 64ll << 20;
 constexpr int MAX_SMEM_G = 1024;
 constexpr int SCHED_BYTES = (MAX_SMEM_G + 1) * 4;
 constexpr int OUT_ROW_BYTES = 80;
@@ -62,7 +75,7 @@ constexpr int XCH_STRIDE = 33;
 constexpr int XCH_BYTES = 2 * 32 * XCH_STRIDE * 4;
 constexpr int SMEM_BYTES = 1024 + RING_BYTES + BAR_BYTES + OUT_BYTES + XCH_BYTES + SCHED_BYTES;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA");
-static_assert((2 * S + 5) * 8 + 12 <= BAR_BYTES, "barrier area");
+static_assert((2 * S + 5 + 3 * NSLOT + 1) * 8 + 12 <= BAR_BYTES, "barrier area");
 // kind::f16 instruction descriptor: D fp32, A and B bf16, both K-major,
 // N >> 3 at bits 17-22, M >> 4 at bits 24-28 (M = 256 across the pair).
 constexpr uint32_t IDESC = (1u << 4) | (1u << 7) | (1u << 10) |
@@ -81,15 +94,25 @@ struct Args {
   int64_t single_rows;
   int64_t rows_bound;
   const int32_t* sched;   // global pair-tile prefix, or NULL: built in shared memory
+  int32_t* ctr;           // zeroed tile counter (dynamic order), or NULL: round-robin
+  int mmajor;             // 1: large groups may be ordered m-tile major
   void* out;
   int64_t ldo;
   uint32_t* flags;
 };
 
-// Pair tile -> (group, pair m-tile, n-tile), pair m-tiles of BMP rows.
+// Pair tile -> (group, pair m-tile, n-tile), pair m-tiles of BMP rows; within
+// a group n-tile major, or m-tile major for groups of MMAJOR_TILES m-tiles
+// or more.
 __device__ __forceinline__ void decode_tile(const Args& a, const int32_t* sched, int64_t tile,
                                             int& g, int& mp, int& nt) {
   pair_decode_tile(a, sched, tile, g, mp, nt);
+  const int mtg = sched[g + 1] - sched[g];
+  if (a.mmajor && mtg >= MMAJOR_TILES) {
+    const int64_t local = tile - (int64_t)sched[g] * a.NT;
+    mp = (int)(local / a.NT);
+    nt = (int)(local % a.NT);
+  }
 }
 __device__ void build_schedule(const Args& a, int32_t* sched, int lane) {
   pair_schedule<BMP>(a, sched, lane);
@@ -115,8 +138,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   unsigned char* smem =
       reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
-  // bars: full[S] empty[S] tfull[2] tempty[2] final
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  // bars: full[S] empty[S] tfull[2] tempty[2] final tfill[NSLOT] tdrain[NSLOT];
+  // then the tile slots, the epilogue's copy of its tile, and the scalars
+  volatile int64_t* s_tile = reinterpret_cast<volatile int64_t*>(bars + 2 * S + 5 + 2 * NSLOT);
+  volatile int64_t* s_etile = s_tile + NSLOT;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * S + 5 + 3 * NSLOT + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* s_ok = reinterpret_cast<volatile int*>(tmem_slot + 2);
   unsigned char* s_out = smem + RING_BYTES + BAR_BYTES;
@@ -132,6 +158,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   auto tfull = [&](int b) { return smem_u32(&bars[2 * S + b]); };
   auto tempty = [&](int b) { return smem_u32(&bars[2 * S + 2 + b]); };
   const uint32_t final_bar = smem_u32(&bars[2 * S + 4]);
+  auto tfill = [&](int i) { return smem_u32(&bars[2 * S + 5 + i]); };
+  auto tdrain = [&](int i) { return smem_u32(&bars[2 * S + 5 + NSLOT + i]); };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -143,6 +171,10 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(tempty(b), 2 * 128);   // both CTAs' epilogue threads
     }
     mbar_init(final_bar, 1);
+    for (int i = 0; i < NSLOT; ++i) {
+      mbar_init(tfill(i), 1);   // the even CTA's tile taker
+      mbar_init(tdrain(i), 6);  // three readers in each CTA (see next_tile)
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -161,6 +193,39 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int64_t total = (int64_t)sched[a.G] * a.NT;
   const int64_t cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
 
+  // Tile n of this pair (n = 0, 1, ...), or -1 when there is none left (or a
+  // wait ran out).  The even CTA's A producer takes it (take = true) and
+  // writes it to slot n % NSLOT of both CTAs; every other reader -- the A
+  // producer of the odd CTA, both B producers, the MMA issuer and one thread
+  // of each CTA's epilogue -- reads it from its own CTA's slot and tells the
+  // even CTA that it has (six readers a slot use).
+  // The taker claims its tiles one ahead: the counter's reply for the next
+  // tile arrives while the loads of this one go out.
+  int64_t reserve = a.ctr && threadIdx.x == 0 && leader ? (int64_t)atomicAdd(a.ctr, 1) : -1;
+  auto next_tile = [&](int64_t n, bool take) -> int64_t {
+    const int slot = (int)(n % NSLOT);
+    const uint32_t use = (uint32_t)(n / NSLOT);
+    if (take) {
+      if (!wait2(tdrain(slot), (use & 1u) ^ 1u, abort_flag)) return -1;
+      int64_t t = cl + n * ncl;
+      if (a.ctr) {
+        t = reserve;
+        reserve = (int64_t)atomicAdd(a.ctr, 1);
+      }
+      if (t >= total) t = -1;
+      s_tile[slot] = t;
+      const uint32_t remote = map_to_rank(smem_u32((const void*)&s_tile[slot]), 1);
+      asm volatile("st.shared::cluster.b64 [%0], %1;" ::"r"(remote), "l"(t) : "memory");
+      mbar_arrive(tfill(slot));
+      mbar_arrive_cluster(map_to_rank(tfill(slot), 1));
+      return t;
+    }
+    if (!wait2(tfill(slot), use & 1u, abort_flag)) return -1;
+    const int64_t t = s_tile[slot];
+    mbar_arrive_cluster(map_to_rank(tdrain(slot), 0));
+    return t;
+  };
+
   if ((warp == 0 || warp == 6) && lane == 0) {
     // ---------------- TMA producers ----------------
     const bool is_a = warp == 0;
@@ -169,7 +234,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     int s = 0;
     uint32_t ph = 0, issued = 0, par = 0;
     bool ok = true;
-    for (int64_t tile = cl; tile < total && ok; tile += ncl) {
+    for (int64_t n = 0; ok; ++n) {
+      const int64_t tile = next_tile(n, is_a && leader);
+      if (tile < 0) break;
       int g, mp, nt;
       decode_tile(a, sched, tile, g, mp, nt);
       const int64_t gbase = a.offsets ? a.offsets[g] : 0;
@@ -202,7 +269,9 @@ __global__ void __launch_bounds__(THREADS, 1)
     int s = 0, acc = 0;
     uint32_t ph = 0, aph = 0;
     bool ok = true;
-    for (int64_t tile = cl; tile < total && ok; tile += ncl) {
+    for (int64_t n = 0; ok; ++n) {
+      const int64_t tile = next_tile(n, false);
+      if (tile < 0) break;
       int g, mp, nt;
       decode_tile(a, sched, tile, g, mp, nt);
       const uint32_t idesc = tile_rows_left(a, g, mp) <= BMC ? IDESC_HALF : IDESC;
@@ -259,19 +328,25 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
       __syncwarp();
     };
-    for (int64_t tile = cl; tile < total; tile += ncl) {
+    for (int64_t n = 0;; ++n) {
+      // one thread takes the tile and waits for its accumulator; the four
+      // warps follow its result together (the half tiles' hand-over meets
+      // at named barriers)
+      if (et == 0) {
+        const int64_t t = next_tile(n, false);
+        *s_etile = t;
+        *s_ok = t >= 0 && wait2(tfull(acc), aph, abort_flag) ? 1 : 0;
+      }
+      epi_bar();
+      const int okv = *s_ok;
+      const int64_t tile = *s_etile;
+      epi_bar();
+      if (!okv) break;
       int g, mp, nt;
       decode_tile(a, sched, tile, g, mp, nt);
       const int64_t gbeg = a.offsets ? a.offsets[g] : 0;
       const int64_t gend = a.offsets ? a.offsets[g + 1] : a.single_rows;
       const bool half = tile_rows_left(a, g, mp) <= BMC;
-      // one thread waits for the accumulator; the four warps follow its
-      // result together (the half tiles' hand-over meets at named barriers)
-      if (et == 0) *s_ok = wait2(tfull(acc), aph, abort_flag) ? 1 : 0;
-      epi_bar();
-      const int okv = *s_ok;
-      epi_bar();
-      if (!okv) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * BN;
       if (!half) {
@@ -416,6 +491,9 @@ cudaError_t launch_gemm_tc2(const GemmArgs& a, cudaStream_t st) {
   t.single_rows = a.single_rows;
   t.rows_bound = a.rows_bound;
   t.sched = smem_sched ? nullptr : a.sched;
+  t.ctr = a.ctr;
+  t.mmajor = (int64_t)(a.mode == kSwiGLU ? 2 : 1) * a.N * a.K * 2 <= MMAJOR_WEIGHT_BYTES;
+  if (a.ctr && (e = cudaMemsetAsync(a.ctr, 0, sizeof(int32_t), st)) != cudaSuccess) return e;
   t.out = a.out;
   t.ldo = a.ldo;
   t.flags = a.flags;

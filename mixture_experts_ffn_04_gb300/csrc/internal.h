@@ -31,7 +31,8 @@ moe_status decode_shape(const moe_shape* s, Shape* out, const char** why);
 // Byte offsets of every region inside the workspace (all 256-byte aligned).
 struct Layout {
   // scratch
-  size_t flags, logits, hist, base, sched_routed, sched_shared, sched_router, tmaps, scratch_end;
+  size_t flags, logits, hist, base, sched_routed, sched_shared, sched_router, tile_ctr, tmaps,
+      scratch_end;
   int nchunks, tokens_per_chunk;
   // layer-forward intermediates
   size_t x_norm, topk_idx, topk_w, gate, counts, offsets, sidx, row_token, x_perm, h, y_perm,
@@ -70,6 +71,8 @@ struct GemmArgs {
   void* out;               // [rows, ldo]
   int64_t ldo;             // elements
   int32_t* sched;          // [G + 1] scratch for the m-tile prefix
+  int32_t* ctr = nullptr;  // scratch tile counter (zeroed by the launcher) of the
+                           // SM-pair engine's dynamic tile order, or NULL
   uint32_t* flags;
   int ksplit = 1;          // kStoreF32 only: partial sums over K ranges,
   int64_t split_stride = 0;  // written split_stride floats apart

@@ -124,6 +124,7 @@ Layout layout_for(const Shape& s) {
   L.sched_routed = off; off += align256((E + 1) * 4);
   L.sched_shared = off; off += 256;
   L.sched_router = off; off += 256;
+  L.tile_ctr = off; off += 256;   // routed calls at +0, one-group calls at +128
   L.tmaps = off; off += align256(256 * E);   // two tensor maps per group
   L.scratch_end = off;
   L.x_norm = off; off += align256(s.input_norm ? T * (size_t)s.H * s.esize : 0);
@@ -178,12 +179,15 @@ static int engine_for(const GemmArgs& a) {
   if (ov >= 1 && ov <= 3) return ov;
   if (rows <= 4) return 3;
   // SM pairs: a 64-wide k-block needs 32 KB of operands per SM instead of
-  // 48 KB (six stages instead of four) for the same MMA work, and a group's
-  // last tile with at most 128 rows left runs at M = 128 (half the MMA time),
-  // so the row padding is that of 128-row tiles.  Measured level with or
-  // slightly ahead of the one-SM engine on every prefill-sized workload, a
-  // third faster on one big group (the shared MLP).
-  if (pair_ok && rows >= 512) return 4;
+  // 48 KB (six stages instead of four) for the same MMA work, a group's last
+  // tile with at most 128 rows left runs at M = 128 (half the MMA time), and
+  // the tiles are handed out in one window of consecutive tile numbers (big
+  // groups m-tile major).  Measured against the one-SM engine on the layer:
+  // ahead for one big group (the shared MLP), for large routed groups
+  // (all-to-one and Zipf routing) and for long reductions (K = 3584, 7168),
+  // 5 % behind on short ones (the Qwen3- and Gemma-4-shaped layers, K <= 2816,
+  // whose tiles are too short for the pair's per-tile hand-offs).
+  if (pair_ok && rows >= 512 && (a.G == 1 || rows / a.G >= 1024 || a.K >= 3072)) return 4;
   return 2;
 }
 
@@ -435,6 +439,7 @@ static moe_status grouped(int mode, const moe_shape* shape, const void* A, const
   a.out = out;
   a.ldo = a.N;
   a.sched = reinterpret_cast<int32_t*>(w + (G > 1 ? L.sched_routed : L.sched_shared));
+  a.ctr = reinterpret_cast<int32_t*>(w + L.tile_ctr + (G > 1 ? 0 : 128));
   a.flags = reinterpret_cast<uint32_t*>(w + L.flags);
   a.gather = gather;
   a.a_rows = s.T;
@@ -606,6 +611,7 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
   a.single_rows = 0;
   a.rows_bound = s.T * s.k;
   a.sched = reinterpret_cast<int32_t*>(w + L.sched_routed);
+  a.ctr = reinterpret_cast<int32_t*>(w + L.tile_ctr);
   a.flags = flags;
   a.wfmt = s.wfmt;
   a.mode = kSwiGLU;
@@ -648,6 +654,7 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
     b.single_rows = s.T;
     b.rows_bound = s.T;
     b.sched = reinterpret_cast<int32_t*>(w + L.sched_shared);
+    b.ctr = reinterpret_cast<int32_t*>(w + L.tile_ctr + 128);
     b.flags = flags;
     b.wfmt = s.wfmt;
     b.mode = kSwiGLU;
