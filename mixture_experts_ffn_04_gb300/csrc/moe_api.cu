@@ -6,6 +6,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 
 #include "../../include/moe.h"
 #include "../../include/moe_testing.h"
@@ -25,6 +26,39 @@ int gemm_path_override() { return g_engine.load(); }
 void set_error_message(const char* why) { tl_error = why; }
 
 static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// The layer forward's second stream (the shared MLP at decode sizes) and its
+// fork/join events, one set per device, made on first use; the mutex is held
+// from the fork to the join's enqueue so that concurrent callers never see
+// each other's event records.
+constexpr int64_t kForkMaxT = 64;
+struct SideStream {
+  cudaStream_t stream = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex mu;
+};
+static cudaError_t side_stream(SideStream** out) {
+  static SideStream sides[64];
+  static std::mutex init_mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  SideStream& sd = sides[dev];
+  std::lock_guard<std::mutex> lock(init_mu);
+  if (sd.stream == nullptr) {
+    cudaStream_t st = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr;
+    if ((e = cudaStreamCreateWithFlags(&st, cudaStreamNonBlocking)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&f, cudaEventDisableTiming)) != cudaSuccess) return e;
+    if ((e = cudaEventCreateWithFlags(&j, cudaEventDisableTiming)) != cudaSuccess) return e;
+    sd.fork = f;
+    sd.join = j;
+    sd.stream = st;
+  }
+  *out = &sd;
+  return cudaSuccess;
+}
 
 moe_status decode_shape(const moe_shape* s, Shape* o, const char** why) {
   if (!s) { *why = "shape is NULL"; return MOE_ERR_INVALID_ARG; }
@@ -577,6 +611,63 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
     CHECK_CUDA(launch_rmsnorm(s, x, W->norm_weight, s.norm_eps, w + L.x_norm, st));
     xin = w + L.x_norm;
   }
+  // The shared MLP depends on xin alone.  At decode sizes its weight stream
+  // runs on a second stream, forked here and joined before the combine, so it
+  // overlaps the routing, permute and routed GEMMs, which at a few tokens are
+  // short latency-bound launches that leave HBM idle.  (The traced entry point
+  // keeps one stream, so its stage events time each stage alone.)
+  void* sh_out = nullptr;
+  int sh_split = 1;
+  auto launch_shared = [&](cudaStream_t ss) -> cudaError_t {
+    sh_out = w + L.sh_out;
+    GemmArgs b;
+    b.dtype = s.dtype;
+    b.offsets = nullptr;
+    b.G = 1;
+    b.single_rows = s.T;
+    b.rows_bound = s.T;
+    b.sched = reinterpret_cast<int32_t*>(w + L.sched_shared);
+    b.ctr = reinterpret_cast<int32_t*>(w + L.tile_ctr + 128);
+    b.flags = flags;
+    b.wfmt = s.wfmt;
+    b.mode = kSwiGLU;
+    b.A = xin;
+    b.B0 = W->shared_gate_proj;
+    b.B1 = W->shared_up;
+    b.bstride = 0;
+    b.N = s.I_sh;
+    b.K = s.H;
+    b.out = w + L.sh_h;
+    b.ldo = s.I_sh;
+    cudaError_t e = launch_grouped_gemm(b, ss);
+    if (e != cudaSuccess) return e;
+    b.mode = kStoreAct;
+    b.A = w + L.sh_h;
+    b.B0 = W->shared_down;
+    b.B1 = nullptr;
+    b.N = s.H;
+    b.K = s.I_sh;
+    b.out = sh_out;
+    b.ldo = s.H;
+    sh_split = shared_split(s, b);
+    if (sh_split > 1) {
+      b.mode = kStoreF32;
+      b.ksplit = sh_split;
+      b.split_stride = s.T * (int64_t)s.H;
+    }
+    return launch_grouped_gemm(b, ss);
+  };
+  const bool fork = s.I_sh && ev == nullptr && s.T <= kForkMaxT;
+  SideStream* side = nullptr;
+  std::unique_lock<std::mutex> side_lock;
+  if (fork) {
+    CHECK_CUDA(side_stream(&side));
+    side_lock = std::unique_lock<std::mutex>(side->mu);
+    CHECK_CUDA(cudaEventRecord(side->fork, st));
+    CHECK_CUDA(cudaStreamWaitEvent(side->stream, side->fork, 0));
+    CHECK_CUDA(launch_shared(side->stream));
+    CHECK_CUDA(cudaEventRecord(side->join, side->stream));
+  }
   STAGE_EVENT(MOE_STAGE_ROUTE);
   if (direct) {
     use_idx = routes_idx;
@@ -643,46 +734,8 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
   CHECK_CUDA(launch_grouped_gemm(a, st));
 
   STAGE_EVENT(MOE_STAGE_SHARED);
-  void* sh_out = nullptr;
-  int sh_split = 1;
-  if (s.I_sh) {
-    sh_out = w + L.sh_out;
-    GemmArgs b;
-    b.dtype = s.dtype;
-    b.offsets = nullptr;
-    b.G = 1;
-    b.single_rows = s.T;
-    b.rows_bound = s.T;
-    b.sched = reinterpret_cast<int32_t*>(w + L.sched_shared);
-    b.ctr = reinterpret_cast<int32_t*>(w + L.tile_ctr + 128);
-    b.flags = flags;
-    b.wfmt = s.wfmt;
-    b.mode = kSwiGLU;
-    b.A = xin;
-    b.B0 = W->shared_gate_proj;
-    b.B1 = W->shared_up;
-    b.bstride = 0;
-    b.N = s.I_sh;
-    b.K = s.H;
-    b.out = w + L.sh_h;
-    b.ldo = s.I_sh;
-    CHECK_CUDA(launch_grouped_gemm(b, st));
-    b.mode = kStoreAct;
-    b.A = w + L.sh_h;
-    b.B0 = W->shared_down;
-    b.B1 = nullptr;
-    b.N = s.H;
-    b.K = s.I_sh;
-    b.out = sh_out;
-    b.ldo = s.H;
-    sh_split = shared_split(s, b);
-    if (sh_split > 1) {
-      b.mode = kStoreF32;
-      b.ksplit = sh_split;
-      b.split_stride = s.T * (int64_t)s.H;
-    }
-    CHECK_CUDA(launch_grouped_gemm(b, st));
-  }
+  if (s.I_sh && !fork) CHECK_CUDA(launch_shared(st));
+  if (fork) CHECK_CUDA(cudaStreamWaitEvent(st, side->join, 0));
   STAGE_EVENT(MOE_STAGE_COMBINE);
   const void* resid = s.residual ? x : nullptr;
   if (sh_split > 1) {

@@ -412,3 +412,34 @@ def test_step_api_with_input_norm_and_residual():
     torch.cuda.synchronize()
     assert m.moe_get_device_status(ws)[0] == m.MOE_OK
     assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
+
+
+@pytest.mark.parametrize("T", [1, 8, 64])
+def test_forked_shared_mlp_in_a_graph_matches_eager(T):
+    """At decode sizes the shared MLP runs on a second stream forked from and
+    joined back into the caller's stream.  The same forward captured in a CUDA
+    graph (the fork becomes a graph branch) gives the eager result bit for bit,
+    and the eager result equals the traced entry point's, which keeps one
+    stream."""
+    wl = W.get("qwen2-moe-shape-T%d" % T) if T in (1, 8, 64) else None
+    dev = W.make_inputs(wl, seed=4, device="cuda")
+    layer = m.MoELayer(wl, dev)
+    x = dev["x"]
+    y_eager = torch.empty_like(x)
+    layer.forward(x, y_eager)
+    torch.cuda.synchronize()
+    y_graph = torch.full_like(x, float("nan"))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        m.moe_layer_forward(layer.shape, layer.weights, x, None, None, y_graph, layer.ws)
+    g.replay()
+    torch.cuda.synchronize()
+    assert layer.device_status()[0] == m.MOE_OK
+    assert torch.equal(y_eager.view(torch.int16), y_graph.view(torch.int16))
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(m.STAGES) + 1)]
+    for e in evs:
+        e.record()
+    y_traced = torch.empty_like(x)
+    m.moe_layer_forward_traced(layer.shape, layer.weights, x, None, None, y_traced, layer.ws, evs)
+    torch.cuda.synchronize()
+    assert torch.equal(y_eager.view(torch.int16), y_traced.view(torch.int16))
