@@ -54,7 +54,8 @@ def main(argv=None):
     ap.add_argument("--inter", type=int, default=2048)
     ap.add_argument("--workload", default="qwen3-30b-a3b-shape-T4096")
     ap.add_argument("--weights", default="act", choices=["act", "mxfp8"],
-                    help="gate_up / down: expert weights packed as MXFP8 (moe_quantize_mxfp8)")
+                    help="gate_up / down: expert weights packed as MXFP8 (moe_quantize_mxfp8); "
+                         "layer: the workload's expert weights drawn as packed MXFP8")
     ap.add_argument("--engine", type=int, default=0,
                     help="grouped-GEMM engine forced for the run (moe_testing_set_gemm_engine; "
                          "0 = the library's choice)")
@@ -69,6 +70,9 @@ def main(argv=None):
 
     if a.op == "layer":
         wl = W.get(a.workload)
+        if a.weights == "mxfp8":
+            import dataclasses
+            wl = dataclasses.replace(wl, weights="mxfp8")
         dev = W.make_inputs(wl, seed=0, device="cuda")
         layer = m.MoELayer(wl, dev)
         x = dev["x"]
@@ -76,7 +80,8 @@ def main(argv=None):
         us = _time(lambda: layer.forward(x, y, dev.get("routes_idx"), dev.get("routes_w")),
                    flush, a.steps, a.warmup)
         st = layer.device_status()[0]
-        print(json.dumps({"op": a.op, "workload": wl.name, "engine": a.engine, "us": us,
+        print(json.dumps({"op": a.op, "workload": wl.name, "weights": a.weights,
+                          "engine": a.engine, "us": us,
                           "launches": m.moe_last_launch_count(), "status": st}))
         return 0 if st == m.MOE_OK else 1
 
