@@ -96,6 +96,13 @@ struct Args {
   const int32_t* sched;   // global pair-tile prefix, or NULL: built in shared memory
   int32_t* ctr;           // zeroed tile counter (dynamic order), or NULL: round-robin
   int mmajor;             // 1: large groups may be ordered m-tile major
+  // K split (few-tile calls): up to ksmax splits, chosen in the kernel from
+  // the real tile count; partial sums to part [split][row][NT * 256] (fp32),
+  // the number of splits to *ks_out; part == NULL: no split
+  int ksmax;
+  float* part;
+  int64_t part_ld, part_stride;
+  int32_t* ks_out;
   void* out;
   int64_t ldo;
   uint32_t* flags;
@@ -190,8 +197,24 @@ __global__ void __launch_bounds__(THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int32_t* sched = a.sched ? a.sched : s_sched;
-  const int64_t total = (int64_t)sched[a.G] * a.NT;
   const int64_t cl = blockIdx.x >> 1, ncl = gridDim.x >> 1;
+  // K splits: as many as keep every cluster busy (at most ksmax, at least 4
+  // k-blocks a split); the same in every CTA, recorded for the reduction.
+  const int64_t tiles1 = (int64_t)sched[a.G] * a.NT;
+  int ks = 1;
+  if (a.part != nullptr) {
+    int64_t k = tiles1 > 0 ? ncl / tiles1 : 1;
+    if (k > a.ksmax) k = a.ksmax;
+    if (k > a.KB / 4) k = a.KB / 4;
+    ks = k < 1 ? 1 : (int)k;
+    if (blockIdx.x == 0 && threadIdx.x == 0) *a.ks_out = ks;
+  }
+  const int64_t total = tiles1 * ks;
+  // k-blocks of split sp of a tile
+  auto kb_range = [&](int sp, int& kb0, int& kb1) {
+    kb0 = (int)((int64_t)sp * a.KB / ks);
+    kb1 = (int)((int64_t)(sp + 1) * a.KB / ks);
+  };
 
   // Tile n of this pair (n = 0, 1, ...), or -1 when there is none left (or a
   // wait ran out).  The even CTA's A producer takes it (take = true) and
@@ -237,13 +260,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int64_t n = 0; ok; ++n) {
       const int64_t tile = next_tile(n, is_a && leader);
       if (tile < 0) break;
-      int g, mp, nt;
-      decode_tile(a, sched, tile, g, mp, nt);
+      int g, mp, nt, kb0, kb1;
+      decode_tile(a, sched, tile / ks, g, mp, nt);
+      kb_range((int)(tile % ks), kb0, kb1);
       const int64_t gbase = a.offsets ? a.offsets[g] : 0;
       const bool half = tile_rows_left(a, g, mp) <= BMC;
       const int arow = (int)(gbase + (int64_t)mp * BMP + (int64_t)rank * (half ? BMC / 2 : BMC));
       const int brow = b_row(nt);
-      for (int kb = 0; kb < a.KB; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!wait2(empty(s), ph ^ 1u, abort_flag)) { ok = false; break; }
         const uint32_t st = ring + s * STAGE_BYTES;
         // the even CTA's "full" barrier counts both CTAs' bytes; only the
@@ -272,13 +296,14 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int64_t n = 0; ok; ++n) {
       const int64_t tile = next_tile(n, false);
       if (tile < 0) break;
-      int g, mp, nt;
-      decode_tile(a, sched, tile, g, mp, nt);
+      int g, mp, nt, kb0, kb1;
+      decode_tile(a, sched, tile / ks, g, mp, nt);
+      kb_range((int)(tile % ks), kb0, kb1);
       const uint32_t idesc = tile_rows_left(a, g, mp) <= BMC ? IDESC_HALF : IDESC;
       if (!wait2(tempty(acc), aph ^ 1u, abort_flag)) break;
       tc_fence_after();
       const uint32_t d = tmem_base + (uint32_t)acc * BN;
-      for (int kb = 0; kb < a.KB; ++kb) {
+      for (int kb = kb0; kb < kb1; ++kb) {
         if (!wait2(full(s), ph, abort_flag)) {
           ok = false;
           break;
@@ -288,7 +313,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
           mma2(d, sw128_desc(st + kk * 32), sw128_desc(st + A_BYTES + kk * 32), idesc,
-               (kb | kk) != 0 ? 1u : 0u);
+               (kb != kb0 || kk != 0) ? 1u : 0u);
         commit2_both(empty(s));
         if (++s == S) { s = 0; ph ^= 1u; }
       }
@@ -343,13 +368,36 @@ __global__ void __launch_bounds__(THREADS, 1)
       epi_bar();
       if (!okv) break;
       int g, mp, nt;
-      decode_tile(a, sched, tile, g, mp, nt);
+      decode_tile(a, sched, tile / ks, g, mp, nt);
+      const int sp = (int)(tile % ks);
       const int64_t gbeg = a.offsets ? a.offsets[g] : 0;
       const int64_t gend = a.offsets ? a.offsets[g + 1] : a.single_rows;
       const bool half = tile_rows_left(a, g, mp) <= BMC;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)acc * BN;
-      if (!half) {
+      if (ks > 1) {
+        // K split: this lane's row of the fp32 accumulator (256 columns of a
+        // full tile; 128 of a half tile) to the split's partial sums,
+        // columns nt * 256 + c; the reduction applies the epilogue
+        const int64_t row = half
+            ? gbeg + (int64_t)mp * BMP + (int64_t)rank * (BMC / 2) + (q & 1) * 32 + lane
+            : gbeg + (int64_t)mp * BMP + (int64_t)rank * BMC + q * 32 + lane;
+        const int cbase = half ? (q >> 1) * (BN / 2) : 0;
+        const int ncol = half ? BN / 2 : BN;
+        float* prow = a.part + (int64_t)sp * a.part_stride + row * a.part_ld + (int64_t)nt * BN + cbase;
+#pragma unroll 1
+        for (int c = 0; c < ncol; c += 32) {
+          uint32_t r[32];
+          tmem_ld32(taddr + c, r);
+          tmem_wait_ld();
+          if (row < gend) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              reinterpret_cast<uint4*>(prow + c)[v] =
+                  make_uint4(r[4 * v], r[4 * v + 1], r[4 * v + 2], r[4 * v + 3]);
+          }
+        }
+      } else if (!half) {
         const int64_t row0 = gbeg + (int64_t)mp * BMP + (int64_t)rank * BMC + q * 32;
         const int64_t nvalid64 = gend - row0;
         const int nvalid = nvalid64 < 0 ? 0 : (nvalid64 > 32 ? 32 : (int)nvalid64);
@@ -455,6 +503,65 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0 && *abort_flag) set_flag(a.flags, kFlagTimeout);
 }
 
+// The K split's reduction: out[r, j] for the group rows r < offsets[G] (or
+// single_rows), the splits' partial sums added in split order in fp32, then
+// the epilogue (SwiGLU: silu(gate) * up, gate at column (j / 128) * 256 +
+// j % 128 of the partials, up 128 further; plain: column j), rounded once.
+// Nothing to do when the GEMM chose one split (it wrote out itself).
+template <bool SWIGLU>
+__global__ void __launch_bounds__(256) split_reduce_kernel(const float* __restrict__ part,
+                                                           int64_t part_ld, int64_t part_stride,
+                                                           const int32_t* ks_ptr,
+                                                           const int32_t* offsets, int G,
+                                                           int64_t single_rows, int64_t rows_bound,
+                                                           int N,
+                                                           bf16* __restrict__ out, int64_t ldo) {
+  const int ks = *ks_ptr;
+  if (ks <= 1) return;
+  int64_t rows = offsets ? offsets[G] : single_rows;
+  if (rows > rows_bound) rows = rows_bound;   // the GEMM flagged it and computed nothing
+  const int per_row = N / 8;
+  const int64_t items = rows * per_row;
+  for (int64_t it = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; it < items;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = it / per_row;
+    const int j0 = (int)(it % per_row) * 8;
+    float f[8];
+    if (SWIGLU) {
+      const int64_t cg = (int64_t)(j0 / (BN / 2)) * BN + j0 % (BN / 2);
+      float gsum[8], usum[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) gsum[e] = usum[e] = 0.0f;
+      for (int sp = 0; sp < ks; ++sp) {
+        const float* p = part + sp * part_stride + r * part_ld + cg;
+        const float4 g0 = reinterpret_cast<const float4*>(p)[0], g1 = reinterpret_cast<const float4*>(p)[1];
+        const float4 u0 = reinterpret_cast<const float4*>(p + BN / 2)[0],
+                     u1 = reinterpret_cast<const float4*>(p + BN / 2)[1];
+        const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          gsum[e] += gv[e];
+          usum[e] += uv[e];
+        }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = silu_fast(gsum[e]) * usum[e];
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = 0.0f;
+      for (int sp = 0; sp < ks; ++sp) {
+        const float* p = part + sp * part_stride + r * part_ld + j0;
+        const float4 v0 = reinterpret_cast<const float4*>(p)[0], v1 = reinterpret_cast<const float4*>(p)[1];
+        const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] += vv[e];
+      }
+    }
+    *reinterpret_cast<uint4*>(out + r * ldo + j0) = pack16(f, (const bf16*)nullptr);
+  }
+}
+
 }  // namespace tc2
 
 cudaError_t launch_gemm_tc2(const GemmArgs& a, cudaStream_t st) {
@@ -492,6 +599,12 @@ cudaError_t launch_gemm_tc2(const GemmArgs& a, cudaStream_t st) {
   t.rows_bound = a.rows_bound;
   t.sched = smem_sched ? nullptr : a.sched;
   t.ctr = a.ctr;
+  t.ksmax = kSplitPairMax;
+  t.part = a.split_part;
+  t.ks_out = a.split_ks;
+  t.part_ld = (int64_t)t.NT * BN;
+  t.part_stride = a.rows_bound * t.part_ld;
+  if (t.part && !t.ks_out) return cudaErrorInvalidValue;
   t.mmajor = (int64_t)(a.mode == kSwiGLU ? 2 : 1) * a.N * a.K * 2 <= MMAJOR_WEIGHT_BYTES;
   if (a.ctr && (e = cudaMemsetAsync(a.ctr, 0, sizeof(int32_t), st)) != cudaSuccess) return e;
   t.out = a.out;
@@ -528,12 +641,32 @@ cudaError_t launch_gemm_tc2(const GemmArgs& a, cudaStream_t st) {
   }
   const int mc = max_clusters[dev].load();
   if (mc < 0) return cudaErrorNotSupported;
-  const int64_t ncl = tiles_bound < mc ? tiles_bound : mc;
+  // a K split needs every cluster there is (it splits until they are busy)
+  const int64_t ncl = (t.part || tiles_bound >= mc) ? mc : tiles_bound;
   cfg.gridDim = dim3((unsigned)(2 * ncl));
   e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel, mA, mA64, mB0, mB1, t);
   if (e != cudaSuccess) return e;
   count_launch();
-  return cudaGetLastError();
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (t.part) {
+    const int64_t items = a.rows_bound * (a.N / 8);
+    int64_t blocks = (items + 255) / 256;
+    const int64_t cap = (int64_t)tc_sm_count() * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    bf16* out = reinterpret_cast<bf16*>(a.out);
+    if (a.mode == kSwiGLU)
+      split_reduce_kernel<true><<<(unsigned)blocks, 256, 0, st>>>(
+          t.part, t.part_ld, t.part_stride, t.ks_out, a.offsets, a.G, a.single_rows, a.rows_bound, a.N,
+          out, a.ldo);
+    else
+      split_reduce_kernel<false><<<(unsigned)blocks, 256, 0, st>>>(
+          t.part, t.part_ld, t.part_stride, t.ks_out, a.offsets, a.G, a.single_rows, a.rows_bound, a.N,
+          out, a.ldo);
+    count_launch();
+    e = cudaGetLastError();
+  }
+  return e;
 }
 
 }  // namespace moe

@@ -36,7 +36,7 @@ struct Layout {
   int nchunks, tokens_per_chunk;
   // layer-forward intermediates
   size_t x_norm, topk_idx, topk_w, gate, counts, offsets, sidx, row_token, x_perm, h, y_perm,
-      sh_h, sh_out,
+      sh_h, sh_out, gemm_split,
       // training (shape.train): the gate/up pre-activations the forward keeps,
       // and the backward's grouped intermediates
       fc1, g_fc2, d_fc1, dx_perm, total;
@@ -73,6 +73,9 @@ struct GemmArgs {
   int32_t* sched;          // [G + 1] scratch for the m-tile prefix
   int32_t* ctr = nullptr;  // scratch tile counter (zeroed by the launcher) of the
                            // SM-pair engine's dynamic tile order, or NULL
+  float* split_part = nullptr;  // SM-pair engine K split (few-tile calls): fp32
+                                // partials [kSplitPairMax][rows_bound][NT * 256]
+  int32_t* split_ks = nullptr;  // the number of splits the kernel chose
   uint32_t* flags;
   int ksplit = 1;          // kStoreF32 only: partial sums over K ranges,
   int64_t split_stride = 0;  // written split_stride floats apart
@@ -153,6 +156,10 @@ cudaError_t launch_hash_route(const Shape& s, const int32_t* token_ids, const in
 // Split-K factor for a tensor-core fp32-output GEMM of one group (router):
 // enough CTAs to cover the SMs, at most kMaxSplit, at least 4 k-blocks each.
 constexpr int kMaxSplit = 8;
+// K splits of the SM-pair engine's few-tile calls (the shared MLP's gate/up
+// of 65..kSplitMaxRows rows, see moe_api.cu), at most kSplitPairMax.
+constexpr int kSplitPairMax = 4;
+constexpr int64_t kSplitMaxRows = 2048;
 int router_split(int64_t rows, int ncols, int K);
 
 cudaError_t launch_permute(const Shape& s, const Layout& L, char* ws, const void* x,

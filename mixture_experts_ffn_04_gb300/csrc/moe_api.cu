@@ -139,6 +139,21 @@ moe_status decode_shape(const moe_shape* s, Shape* o, const char** why) {
   return MOE_OK;
 }
 
+// The shared MLP's gate/up takes the SM-pair engine's K split when its pair
+// tiles (256-row m-tiles x 128-column n-tiles) would leave most of the SMs
+// idle: bf16, no MXFP8 weights, prefill-sized (decode sizes run on their own
+// stream), at most kSplitMaxTiles tiles.  Routed calls do not split: their
+// group sizes are known on the device only, and where they are few-tile (all
+// routes on one expert at T = 128) the fp32 partials of a 2I-wide SwiGLU
+// accumulator cost more than the split saves (gate/up 37 -> 48 us, measured).
+constexpr int64_t kSplitMaxTiles = 48;
+static bool shared_split_ok(const Shape& s) {
+  if (s.dtype != MOE_BF16 || s.wfmt || s.I_sh == 0 || s.T <= kForkMaxT || s.T > kSplitMaxRows)
+    return false;
+  const int64_t tiles = ((s.T + 255) / 256) * ((s.I_sh + 127) / 128);
+  return tiles <= kSplitMaxTiles;
+}
+
 Layout layout_for(const Shape& s) {
   Layout L;
   size_t off = 0;
@@ -158,7 +173,9 @@ Layout layout_for(const Shape& s) {
   L.sched_routed = off; off += align256((E + 1) * 4);
   L.sched_shared = off; off += 256;
   L.sched_router = off; off += 256;
-  L.tile_ctr = off; off += 256;   // routed calls at +0, one-group calls at +128
+  // tile counters (routed calls at +0, one-group calls at +128) and the K
+  // split the pair engine chose for a one-group call (+192)
+  L.tile_ctr = off; off += 256;
   L.tmaps = off; off += align256(256 * E);   // two tensor maps per group
   L.scratch_end = off;
   L.x_norm = off; off += align256(s.input_norm ? T * (size_t)s.H * s.esize : 0);
@@ -179,6 +196,12 @@ Layout layout_for(const Shape& s) {
   if (s.I_sh && s.T <= kSharedSplitMaxT)
     sh_bytes = std::max(sh_bytes, (size_t)kMaxSplit * T * (size_t)s.H * 4);
   L.sh_out = off; off += align256(sh_bytes);
+  // the SM-pair engine's K-split partials (the shared MLP's gate/up when it
+  // has few tiles)
+  size_t split = 0;
+  if (shared_split_ok(s))
+    split = (size_t)kSplitPairMax * T * (size_t)(((s.I_sh + 127) / 128) * 256) * 4;
+  L.gemm_split = off; off += align256(split);
   const size_t rows = s.train ? T * k : 0;
   L.fc1 = off; off += align256(rows * 2 * (size_t)s.I * s.esize);
   L.g_fc2 = off; off += align256(rows * (size_t)s.H * s.esize);
@@ -222,6 +245,9 @@ static int engine_for(const GemmArgs& a) {
   // 5 % behind on short ones (the Qwen3- and Gemma-4-shaped layers, K <= 2816,
   // whose tiles are too short for the pair's per-tile hand-offs).
   if (pair_ok && rows >= 512 && (a.G == 1 || rows / a.G >= 1024 || a.K >= 3072)) return 4;
+  // a few-tile one-group gate/up the layer gives a K-split buffer: the pair
+  // engine splits K until its clusters are busy
+  if (pair_ok && a.split_part) return 4;
   return 2;
 }
 
@@ -639,8 +665,14 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
     b.K = s.H;
     b.out = w + L.sh_h;
     b.ldo = s.I_sh;
+    if (shared_split_ok(s)) {
+      b.split_part = reinterpret_cast<float*>(w + L.gemm_split);
+      b.split_ks = reinterpret_cast<int32_t*>(w + L.tile_ctr + 192);
+    }
     cudaError_t e = launch_grouped_gemm(b, ss);
     if (e != cudaSuccess) return e;
+    b.split_part = nullptr;
+    b.split_ks = nullptr;
     b.mode = kStoreAct;
     b.A = w + L.sh_h;
     b.B0 = W->shared_down;

@@ -97,8 +97,12 @@ def test_full_size_parity(wl, sample):
 
 def test_step_api_matches_layer_and_merged_fc1():
     """route -> permute -> grouped gate/up -> grouped down -> shared -> combine
-    through the individual entry points gives the layer's output bit for bit,
-    and merged fc1 ([E, 2I, H] with stride 2*I*H) gives the split result."""
+    through the individual entry points gives the layer's grouped rows h and
+    y_perm bit for bit (merged fc1, [E, 2I, H] with stride 2*I*H, gives the
+    split result), and the combine of those rows with the layer's shared
+    output gives the layer's output bit for bit.  The shared MLP itself agrees
+    to rounding: at this size the layer splits its gate/up over K (fp32
+    partial sums added in split order), the one-group step call does not."""
     wl = W.small(W.QWEN2_MOE, T=300, H=512, I=256, I_sh=512)
     dev = to_dev(W.make_inputs(wl, seed=3, device="cpu"))
     layer = m.MoELayer(wl, dev)
@@ -125,10 +129,17 @@ def test_step_api_matches_layer_and_merged_fc1():
     m.moe_grouped_swiglu(s, dev["x"], dev["sh_gate"], dev["sh_up"], 0, one, 1, T, Ish, hs, ws)
     sh = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
     m.moe_grouped_down(s, hs, dev["sh_down"], 0, one, 1, T, Ish, sh, ws)
-    y = torch.empty_like(dev["x"])
-    m.moe_combine(s, y_perm, sidx, tw, sh, gate, y)   # no residual: this workload has none
     torch.cuda.synchronize()
     assert m.moe_get_device_status(ws)[0] == m.MOE_OK
+    v = layer.views()
+    assert torch.equal(h.view(torch.int16), v["h"].view(torch.int16))
+    assert torch.equal(y_perm.view(torch.int16), v["y_perm"].view(torch.int16))
+    sh_layer = v["shared_out"].clone()
+    assert rel_l2(sh.double().cpu().numpy(), sh_layer.double().cpu().numpy()) < 2e-3
+    torch.testing.assert_close(sh.float(), sh_layer.float(), rtol=2.0 ** -6, atol=1e-3)
+    y = torch.empty_like(dev["x"])
+    m.moe_combine(s, y_perm, sidx, tw, sh_layer, gate, y)   # no residual: this workload has none
+    torch.cuda.synchronize()
     assert torch.equal(y, y_ref)
 
 
