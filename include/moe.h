@@ -166,7 +166,10 @@ typedef struct {
  * bytes (dst_stride >= rows*K*9/8).  K a multiple of 8.  A block's scale is
  * the smallest power of two X with max|V| / X <= 448 (so MXFP8-representable
  * weights come back unchanged, as the pages state), values are rounded to
- * nearest even and saturate at 448.  Asynchronous on `stream`; no workspace. */
+ * nearest even and saturate at 448.  A block holding a NaN or an infinity is
+ * stored as NaN (scale byte 0xFF, the e8m0 NaN, and eight e4m3 NaN codes
+ * 0x7F), so its values, and every output they reach, are NaN.  Asynchronous
+ * on `stream`; no workspace. */
 moe_status moe_quantize_mxfp8(const void *w, int32_t dtype, int64_t batch, int64_t rows,
                               int32_t K, int64_t src_stride, int64_t dst_stride, void *packed,
                               void *stream);

@@ -29,6 +29,14 @@ extern "C" {
  * ignored for them). */
 int32_t moe_testing_set_gemm_engine(int32_t engine);
 
+/* How many SMs' worth of CTAs the shared MLP's GEMMs may take when
+ * moe_layer_forward runs them on its second stream (decode sizes), leaving
+ * the other SMs free for the routed chain on the caller's stream: 0 = the
+ * library's choice (default), -1 = all SMs, n > 0 = n SMs.  Applies to later
+ * calls from any thread; returns the previous setting.  Results do not
+ * depend on it. */
+int32_t moe_testing_set_fork_sms(int32_t sms);
+
 /* The router logits moe_route decides on: the router GEMM exactly as
  * moe_route runs it (same engine and K split), with the partial sums added in
  * the same order, written to logits [T, E + shared_gate] (fp32, device).

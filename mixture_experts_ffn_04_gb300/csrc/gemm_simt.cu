@@ -347,8 +347,12 @@ __global__ void __launch_bounds__(256, R == 1 ? (MODE == kSwiGLU ? 2 : 3) : 1)
   const int64_t row0 = gbeg + (int64_t)(j - sched[g]) * R;
   const int nrows = (int)min((int64_t)R, gend - row0);
   // warp -> (column group cg, K slice sl); the block owns kSkW/ks column groups
+  // of each column block by it takes (blockIdx.y, then gridDim.y apart: a
+  // grid capped below the column blocks loops over them)
   const int cg = warp / ks, sl = warp % ks, ncg = kSkW / ks;
-  const int n0 = (blockIdx.y * ncg + cg) * kSkC;
+  const int nby = (a.N + ncg * kSkC - 1) / (ncg * kSkC);
+  for (int by = blockIdx.y; by < nby; by += gridDim.y) {
+  const int n0 = (by * ncg + cg) * kSkC;
   const int K = a.K;
   constexpr int V = 16 / sizeof(T);
   constexpr int CH = PAIR ? 2 : 1;   // chunks per lane step
@@ -520,7 +524,7 @@ __global__ void __launch_bounds__(256, R == 1 ? (MODE == kSwiGLU ? 2 : 3) : 1)
       }
     }
   }
-  if (ks == 1) return;
+  if (ks == 1) continue;
   __syncthreads();
   const int tid = threadIdx.x;
   if (tid < ncg * R * kSkC) {
@@ -532,7 +536,7 @@ __global__ void __launch_bounds__(256, R == 1 ? (MODE == kSwiGLU ? 2 : 3) : 1)
         sg += red[w][(r * kSkC + q) * NU];
         if (MODE == kSwiGLU) su += red[w][(r * kSkC + q) * NU + 1];
       }
-      const int n = (blockIdx.y * ncg + gi) * kSkC + q;
+      const int n = (by * ncg + gi) * kSkC + q;
       if (n < a.N) {
         const int64_t o = (row0 + r) * a.ldo + n;
         if (MODE == kStoreF32) reinterpret_cast<float*>(a.out)[o] = sg;
@@ -540,6 +544,8 @@ __global__ void __launch_bounds__(256, R == 1 ? (MODE == kSwiGLU ? 2 : 3) : 1)
         else reinterpret_cast<T*>(a.out)[o] = from_f<T>(silu_f(sg) * su);
       }
     }
+  }
+  __syncthreads();   // red is rewritten by the next column block
   }
 }
 
@@ -585,6 +591,11 @@ cudaError_t launch_skinny_t(const GemmArgs& a, int R, int smem_sched, cudaStream
   while (ks < kSkW && base_warps * ks < 2432) ks *= 2;
   const int cols_per_block = (kSkW / ks) * kSkC;
   dim3 grid((unsigned)mt_bound, (unsigned)((a.N + cols_per_block - 1) / cols_per_block));
+  if (a.max_sms > 0) {   // resident blocks an SM: the kernel's launch bounds
+    const int per_sm = R == 1 ? (a.mode == kSwiGLU ? 2 : 3) : 1;
+    const int64_t cap = (int64_t)a.max_sms * per_sm / (int64_t)grid.x;
+    if (cap < (int64_t)grid.y) grid.y = (unsigned)(cap > 0 ? cap : 1);
+  }
   const bool pair = a.K % (2 * (16 / (int)sizeof(T))) == 0;
   // tiles of 1 or 4 rows exist for paired bf16 chunks in the two store modes
   if (R != kSkR && (sizeof(T) != 2 || !pair || a.mode == kStoreF32)) return cudaErrorInvalidValue;

@@ -624,7 +624,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
       attr_done[dev] = true;
     }
   }
-  const int grid = (int)(tiles_bound < sm_count() ? tiles_bound : sm_count());
+  const int sms = a.max_sms > 0 && a.max_sms < sm_count() ? a.max_sms : sm_count();
+  const int grid = (int)(tiles_bound < sms ? tiles_bound : sms);
   tc_gemm_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(mA, mB0, mB1, t);
   count_launch();
   return cudaGetLastError();

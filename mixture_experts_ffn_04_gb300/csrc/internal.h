@@ -85,6 +85,10 @@ struct GemmArgs {
   int64_t ldp = 0;                  // gate at pre[r, n], up at pre[r, N + n]
   int wfmt = 0;                     // 1: B0/B1 are packed MXFP8 [N, K] matrices,
                                     // bstride in bytes
+  int max_sms = 0;                  // > 0: the call's CTAs stay within this many
+                                    // SMs' worth (decode and one-SM tensor-core
+                                    // engines), leaving the rest to a concurrent
+                                    // stream
 };
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t st);

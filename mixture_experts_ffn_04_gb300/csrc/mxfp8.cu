@@ -41,8 +41,18 @@ __global__ void quantize_mxfp8_kernel(const T* __restrict__ w, int64_t batch, in
     float v[8];
     load8(w + b * src_stride + r * K + 8 * c, v);
     float amax = 0.f;
+    bool finite = true;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
+    for (int e = 0; e < 8; ++e) {
+      amax = fmaxf(amax, fabsf(v[e]));
+      finite = finite && isfinite(v[e]);
+    }
+    uint8_t* dst = out + b * dst_stride;
+    if (!finite) {   // a NaN or an infinity: the whole block is stored as NaN
+      *reinterpret_cast<uint2*>(dst + r * K + 8 * c) = make_uint2(0x7F7F7F7Fu, 0x7F7F7F7Fu);
+      dst[rows * K + r * kb + c] = 0xFF;
+      continue;
+    }
     int shared = 0;
     if (amax > 0.f) {
       int ex;
@@ -62,7 +72,6 @@ __global__ void quantize_mxfp8_kernel(const T* __restrict__ w, int64_t batch, in
           make_float2(v[4 * h + 2] * inv, v[4 * h + 3] * inv), __NV_SATFINITE, __NV_E4M3);
       word[h] = (uint32_t)lo | ((uint32_t)hi << 16);
     }
-    uint8_t* dst = out + b * dst_stride;
     *reinterpret_cast<uint2*>(dst + r * K + 8 * c) = make_uint2(word[0], word[1]);
     dst[rows * K + r * kb + c] = (uint8_t)byte;
   }

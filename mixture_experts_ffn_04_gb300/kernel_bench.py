@@ -59,11 +59,18 @@ def main(argv=None):
     ap.add_argument("--engine", type=int, default=0,
                     help="grouped-GEMM engine forced for the run (moe_testing_set_gemm_engine; "
                          "0 = the library's choice)")
+    ap.add_argument("--fork-sms", type=int, default=0,
+                    help="layer: SMs the shared MLP may take on its forked stream at decode "
+                         "sizes (moe_testing_set_fork_sms; 0 = the library's choice, -1 = all)")
+    ap.add_argument("--graph", action="store_true",
+                    help="layer: time the replay of one forward captured in a CUDA graph "
+                         "(as the benchmark does) instead of the launches from the host")
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=2)
     a = ap.parse_args(argv)
     torch.cuda.set_device(0)
     m.moe_testing_set_gemm_engine(a.engine)
+    m.moe_testing_set_fork_sms(a.fork_sms)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
     g = torch.Generator(device="cuda")
     g.manual_seed(0)
@@ -77,11 +84,20 @@ def main(argv=None):
         layer = m.MoELayer(wl, dev)
         x = dev["x"]
         y = torch.empty_like(x)
-        us = _time(lambda: layer.forward(x, y, dev.get("routes_idx"), dev.get("routes_w")),
-                   flush, a.steps, a.warmup)
+        fwd = lambda: layer.forward(x, y, dev.get("routes_idx"), dev.get("routes_w"))
+        if a.graph:
+            fwd()                      # first call outside the capture (side stream, tables)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                fwd()
+            us = _time(graph.replay, flush, a.steps, a.warmup)
+        else:
+            us = _time(fwd, flush, a.steps, a.warmup)
         st = layer.device_status()[0]
         print(json.dumps({"op": a.op, "workload": wl.name, "weights": a.weights,
-                          "engine": a.engine, "us": us,
+                          "engine": a.engine, "fork_sms": a.fork_sms, "graph": a.graph,
+                          "us": us,
                           "launches": m.moe_last_launch_count(), "status": st}))
         return 0 if st == m.MOE_OK else 1
 

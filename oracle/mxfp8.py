@@ -16,7 +16,11 @@ smallest power of two X with max|V| / X <= 448 (the largest e4m3 value), so
     (0 when V == 0), e8m0 byte = shared + 127 clamped to [0, 254]
     q_i = e4m3(V_i / 2^shared), round to nearest even, saturating at +-448
 
-and the value of a stored weight is e4m3_value(q) * 2^(byte - 127).  (The OCP
+and the value of a stored weight is e4m3_value(q) * 2^(byte - 127).  The
+pages say nothing of non-finite weights; the reading taken is that a block
+holding a NaN or an infinity is stored as NaN -- scale byte 0xFF (the e8m0
+NaN) and eight e4m3 NaN codes 0x7F -- rather than its finite values being
+quantised against a scale that the infinity or NaN decides.  (The OCP
 Microscaling rule, shared = floor(log2(max|V|)) - 8, would send a
 representable block whose largest value has the mantissa 1.875 to 480 and
 saturate it at 448, breaking the identity the pages state.)
@@ -99,11 +103,15 @@ def quantize(w, K: int):
                    dtype=np.float64).reshape(-1, K)
     N = W.shape[0]
     blocks = W.reshape(N, K // 8, 8)
-    amax = np.max(np.abs(blocks), axis=2)
+    bad = ~np.all(np.isfinite(blocks), axis=2)          # blocks stored as NaN
+    amax = np.where(bad, 0.0, np.max(np.abs(np.where(np.isfinite(blocks), blocks, 0.0)), axis=2))
     shared = np.vectorize(block_shared_exponent, otypes=[np.int64])(amax)
     byte = np.clip(shared + 127, 0, 254)
     x = np.exp2(byte.astype(np.float64) - 127.0)
-    codes = round_e4m3_array((blocks / x[:, :, None]).reshape(-1)).reshape(N, K)
+    finite = np.where(bad[:, :, None], 0.0, blocks)
+    codes = round_e4m3_array((finite / x[:, :, None]).reshape(-1)).reshape(N, K)
+    codes = np.where(np.repeat(bad, 8, axis=1), 0x7F, codes).astype(np.uint8)
+    byte = np.where(bad, 255, byte)
     return codes, byte.astype(np.uint8)
 
 
@@ -112,7 +120,7 @@ def dequantize(codes, scales) -> np.ndarray:
     c = np.asarray(codes, np.uint8)
     s = np.asarray(scales, np.uint8)
     N, K = c.shape
-    x = np.exp2(s.astype(np.float64) - 127.0)
+    x = np.where(s == 255, np.nan, np.exp2(s.astype(np.float64) - 127.0))   # 0xFF: e8m0 NaN
     return _VALUES[c] * np.repeat(x, 8, axis=1)
 
 

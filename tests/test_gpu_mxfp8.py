@@ -4,7 +4,8 @@ shared experts, arbitrary V_TOPK expert shapes, and an enforced stage-marker
 contract").
 
 * moe_quantize_mxfp8 is bit-exact against the oracle's quantiser (bf16 and
-  fp32 inputs; zero blocks, tiny and large blocks);
+  fp32 inputs; zero blocks, tiny and large blocks, blocks holding an
+  infinity or a NaN);
 * the decode, CUDA-core and tensor-core engines on packed MXFP8 weights give
   bit-identical results to the same engines on the dequantised weights
   stored in bf16 (the dequantisation is exact; the tensor-core engine
@@ -45,6 +46,10 @@ def test_quantizer_matches_oracle(dtype):
     w[0, :, :8] = 0.0                      # zero blocks
     w[1, 5, 8:16] = 448.0 * 2.0 ** 3      # exactly at the boundary of a scale
     w[2, 7, :8] = 1.875 * 2.0 ** -4       # the mantissa the floor rule would saturate
+    w[0, 3, 16:24] = 1.0
+    w[0, 3, 19] = float("inf")             # non-finite blocks are stored as NaN
+    w[1, 9, 40] = float("nan")
+    w[2, 2, 63] = float("-inf")
     w = w.to(dtype)
     got = m.mxfp8_pack(w.cuda()).cpu().numpy()
     for b in range(3):

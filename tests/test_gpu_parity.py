@@ -454,3 +454,70 @@ def test_forked_shared_mlp_in_a_graph_matches_eager(T):
     m.moe_layer_forward_traced(layer.shape, layer.weights, x, None, None, y_traced, layer.ws, evs)
     torch.cuda.synchronize()
     assert torch.equal(y_eager.view(torch.int16), y_traced.view(torch.int16))
+
+
+@pytest.mark.parametrize("T", [1, 8, 64])
+def test_forked_shared_mlp_sm_cap_keeps_results(T):
+    """The shared MLP's GEMMs on the forked stream may be held to fewer SMs
+    (their CTAs then loop over the remaining column blocks or tiles); every
+    cap gives the uncapped result bit for bit."""
+    wl = W.get("qwen2-moe-shape-T%d" % T)
+    dev = W.make_inputs(wl, seed=6, device="cuda")
+    layer = m.MoELayer(wl, dev)
+    prev = m.moe_testing_set_fork_sms(-1)
+    try:
+        ref = layer.forward(dev["x"])
+        for sms in (1, 7, 60, 151):
+            m.moe_testing_set_fork_sms(sms)
+            y = torch.full_like(ref, float("nan"))
+            layer.forward(dev["x"], y)
+            torch.cuda.synchronize()
+            assert layer.device_status()[0] == m.MOE_OK
+            assert torch.equal(y.view(torch.int16), ref.view(torch.int16)), sms
+    finally:
+        m.moe_testing_set_fork_sms(prev)
+
+
+def test_forked_shared_mlp_from_two_host_threads():
+    """Two host threads, each with its own layer, workspace and stream, call
+    the decode-sized forward at once; they share the library's side stream
+    (one per device, its fork and join taken under a lock), and every output
+    equals that layer's single-threaded result bit for bit."""
+    import threading
+    layers, xs, refs, outs, streams = [], [], [], [], []
+    for i, T in enumerate((1, 8)):
+        wl = W.get("qwen2-moe-shape-T%d" % T)
+        dev = W.make_inputs(wl, seed=20 + i, device="cuda")
+        layer = m.MoELayer(wl, dev)
+        ref = torch.empty_like(dev["x"])
+        layer.forward(dev["x"], ref)
+        layers.append(layer)
+        xs.append(dev["x"])
+        refs.append(ref)
+        outs.append([torch.full_like(dev["x"], float("nan")) for _ in range(24)])
+        streams.append(torch.cuda.Stream())
+    torch.cuda.synchronize()
+    errors = []
+    start = threading.Barrier(2)
+
+    def run(i):
+        try:
+            start.wait()
+            with torch.cuda.stream(streams[i]):
+                for y in outs[i]:
+                    layers[i].forward(xs[i], y, stream=streams[i])
+            streams[i].synchronize()
+        except Exception as exc:   # reported by the main thread
+            errors.append(exc)
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for i in range(2):
+        assert layers[i].device_status()[0] == m.MOE_OK
+        for y in outs[i]:
+            assert torch.equal(y.view(torch.int16), refs[i].view(torch.int16))

@@ -10,7 +10,11 @@
   the mantissa 1.875;
 * the block scale by brute force: the smallest power of two X over all
   candidates with max|V| / X <= 448;
-* packing keeps codes then scales.
+* packing keeps codes then scales;
+* a block holding a NaN or an infinity is stored as NaN (the reading taken
+  for non-finite weights): scale 0xFF, which torch's e8m0 type also decodes
+  to NaN, and e4m3 codes that torch decodes to NaN; the finite blocks of the
+  same row quantise as they do alone.
 Each check takes the module, so the mutation test can rerun them."""
 import importlib.util
 
@@ -82,8 +86,31 @@ def check_pack_layout(X=MX):
     assert np.array_equal(c2, c) and np.array_equal(s2, s)
 
 
+def check_nonfinite_blocks_are_nan(X=MX):
+    rng = np.random.default_rng(3)
+    w = rng.standard_normal((4, 32))
+    w[0, 3], w[1, 9], w[2, 30] = np.inf, np.nan, -np.inf
+    c, s = X.quantize(w, 32)
+    bad = {(0, 0), (1, 1), (2, 3)}
+    for n in range(4):
+        for b in range(4):
+            if (n, b) in bad:
+                assert s[n, b] == 0xFF and np.all(c[n, 8 * b:8 * b + 8] == 0x7F)
+            else:
+                c1, s1 = X.quantize(w[n, 8 * b:8 * b + 8], 8)
+                assert s[n, b] == s1[0, 0] and np.array_equal(c[n, 8 * b:8 * b + 8], c1[0])
+    v = X.dequantize(c, s)
+    assert np.array_equal(np.isnan(v), np.repeat(s == 0xFF, 8, axis=1))
+    code = torch.tensor([0x7F], dtype=torch.uint8).view(torch.float8_e4m3fn).float()
+    assert torch.isnan(code).all()
+    if hasattr(torch, "float8_e8m0fnu"):
+        sc = torch.tensor([0xFF], dtype=torch.uint8).view(torch.float8_e8m0fnu).float()
+        assert torch.isnan(sc).all()
+
+
 CHECKS = [check_decode_matches_torch, check_rounding_matches_torch,
-          check_representable_is_identity, check_scale_bruteforce, check_pack_layout]
+          check_representable_is_identity, check_scale_bruteforce, check_pack_layout,
+          check_nonfinite_blocks_are_nan]
 
 
 @pytest.mark.parametrize("check", CHECKS, ids=[c.__name__ for c in CHECKS])
@@ -96,6 +123,8 @@ MUTANTS = [
      "return E - 8"),
     ("ties away from zero", "pick = np.where(dlo < dhi, lo, np.where(dhi < dlo, hi, np.where(lo % 2 == 0, lo, hi)))",
      "pick = np.where(dlo < dhi, lo, hi)"),
+    ("non-finite blocks quantised like finite ones", "byte = np.where(bad, 255, byte)",
+     "byte = byte"),
     ("subnormals scaled like normals", "return s * (m / 8.0) * 2.0 ** -6",
      "return s * (1.0 + m / 8.0) * 2.0 ** -7"),
 ]
