@@ -65,74 +65,46 @@ __global__ void __launch_bounds__(256) rank_kernel(const int32_t* __restrict__ i
   for (int e = lane; e < E; e += 32) hist[(int64_t)c * E + e] = cnt[e];
 }
 
-// 2. scan: one block of 1024 threads.  Work items (e, seg): expert e and
-//    segment seg of the chunks (S segments when E <= 1024, else one).
-//    Produces counts, offsets and base[chunk][e] = offsets[e] + rows of e in
-//    earlier chunks.
+// 2. scan: block b takes experts [32 b, 32 b + 32) (lane = expert, so every
+//    load of a chunk's row of hist is one 128-byte line) and its 32 warps
+//    split the chunks into 32 ranges.  The warps' column sums, their
+//    exclusive prefix over the warps in shared memory, and a second pass over
+//    the warp's chunks give base[chunk][e] = rows of e in earlier chunks;
+//    counts[e] is the column total.  The experts' group offsets are added by
+//    the scatter (each of its blocks scans the E counts), so no step here
+//    waits for all experts.  T = 0 (no chunks): counts and offsets are zero.
 __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ hist, int nchunks,
-                                                    int E, int S, int32_t* __restrict__ base,
+                                                    int E, int32_t* __restrict__ base,
                                                     int32_t* __restrict__ counts,
                                                     int32_t* __restrict__ offsets) {
-  extern __shared__ int32_t sm[];
-  int32_t* segsum = sm;               // [S * E]
-  __shared__ int32_t warp_tot[32];
-  __shared__ int32_t carry;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const int items = S * E;
-  for (int it = tid; it < items; it += blockDim.x) {
-    const int e = it % E, seg = it / E;
-    const int c0 = (int)((int64_t)nchunks * seg / S), c1 = (int)((int64_t)nchunks * (seg + 1) / S);
-    int32_t s = 0;
-#pragma unroll 16
-    for (int c = c0; c < c1; ++c) s += hist[(int64_t)c * E + e];
-    segsum[seg * E + e] = s;
+  __shared__ int32_t tot[32][33];
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int e = blockIdx.x * 32 + lane;
+  const int c0 = (int)((int64_t)nchunks * w / 32), c1 = (int)((int64_t)nchunks * (w + 1) / 32);
+  int32_t sum = 0;
+  if (e < E) {
+#pragma unroll 8
+    for (int c = c0; c < c1; ++c) sum += hist[(int64_t)c * E + e];
   }
+  tot[w][lane] = sum;
   __syncthreads();
-  for (int e = tid; e < E; e += blockDim.x) {
+  if (w == 0) {
     int32_t run = 0;
-    for (int seg = 0; seg < S; ++seg) {
-      const int32_t v = segsum[seg * E + e];
-      segsum[seg * E + e] = run;
+    for (int i = 0; i < 32; ++i) {
+      const int32_t v = tot[i][lane];
+      tot[i][lane] = run;
       run += v;
     }
-    counts[e] = run;
-  }
-  if (tid == 0) carry = 0;
-  __syncthreads();
-  for (int b = 0; b < E; b += blockDim.x) {
-    const int e = b + tid;
-    const int32_t v = e < E ? counts[e] : 0;
-    int32_t incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int32_t t = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += t;
+    if (e < E) {
+      counts[e] = run;
+      if (nchunks == 0) offsets[e] = 0;
     }
-    if (lane == 31) warp_tot[wid] = incl;
-    __syncthreads();
-    if (wid == 0) {
-      const int32_t w = warp_tot[lane];
-      int32_t wi = w;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int32_t t = __shfl_up_sync(0xffffffffu, wi, o);
-        if (lane >= o) wi += t;
-      }
-      warp_tot[lane] = wi - w;
-    }
-    __syncthreads();
-    if (e < E) offsets[e] = carry + warp_tot[wid] + incl - v;
-    __syncthreads();
-    if (tid == blockDim.x - 1) carry += warp_tot[wid] + incl;
-    __syncthreads();
+    if (nchunks == 0 && e == E - 1) offsets[E] = 0;
   }
-  if (tid == 0) offsets[E] = carry;
   __syncthreads();
-  for (int it = tid; it < items; it += blockDim.x) {
-    const int e = it % E, seg = it / E;
-    const int c0 = (int)((int64_t)nchunks * seg / S), c1 = (int)((int64_t)nchunks * (seg + 1) / S);
-    int32_t run = offsets[e] + segsum[seg * E + e];
-#pragma unroll 16
+  if (e < E) {
+    int32_t run = tot[w][lane];
+#pragma unroll 8
     for (int c = c0; c < c1; ++c) {
       const int64_t at = (int64_t)c * E + e;
       const int32_t v = hist[at];
@@ -142,6 +114,53 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
   }
 }
 
+// Group offsets of the E experts in shared memory (off[E + 1], exclusive
+// prefix of counts), by all threads of the block: each thread takes a run of
+// consecutive experts, then the runs' totals are scanned across the block.
+// Block 0 also writes them to `offsets`.
+__device__ void block_offsets(const int32_t* __restrict__ counts, int E, int32_t* off,
+                              int32_t* wsum, int32_t* __restrict__ offsets) {
+  const int t = threadIdx.x, lane = t & 31, wid = t >> 5, nw = blockDim.x >> 5;
+  const int per = (E + blockDim.x - 1) / blockDim.x;
+  int32_t loc = 0;
+  for (int i = 0; i < per; ++i) {
+    const int e = t * per + i;
+    if (e < E) {
+      const int32_t v = counts[e];
+      off[e] = loc;
+      loc += v;
+    }
+  }
+  int32_t incl = loc;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    const int32_t v = lane < nw ? wsum[lane] : 0;
+    int32_t wi = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t u = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += u;
+    }
+    if (lane < nw) wsum[lane] = wi - v;
+  }
+  __syncthreads();
+  const int32_t add = wsum[wid] + incl - loc;
+  for (int i = 0; i < per; ++i) {
+    const int e = t * per + i;
+    if (e < E) off[e] += add;
+  }
+  if (t == blockDim.x - 1) off[E] = add + loc;
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int e = t; e <= E; e += blockDim.x) offsets[e] = off[e];
+}
+
 // 3. scatter + copy: one warp per token (grid-stride).  The warp turns the k
 //    local ranks into grouped rows (scatter_index, row_token), then copies the
 //    token's row once from x to each of its rows with 16-byte vectors, four
@@ -149,11 +168,15 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
 template <typename T>
 __global__ void __launch_bounds__(256) scatter_copy_kernel(
     const T* __restrict__ x, const int32_t* __restrict__ idx, int64_t T_, int k, int E, int H,
-    int tpc, const int32_t* __restrict__ base, int32_t* __restrict__ scatter_index,
+    int tpc, const int32_t* __restrict__ base, const int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ scatter_index,
     int32_t* __restrict__ row_token, T* __restrict__ x_perm) {
   extern __shared__ int32_t sm[];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int32_t* dst = sm + (size_t)wid * k;
+  int32_t* off = sm;                        // [E + 1]
+  int32_t* wsum = sm + E + 1;               // [32]
+  int32_t* dst = wsum + 32 + (size_t)wid * k;
+  block_offsets(counts, E, off, wsum, offsets);
   constexpr int V = 16 / sizeof(T);
   const int nvec = H / V;
   for (int64_t t = (int64_t)blockIdx.x * nw + wid; t < T_; t += (int64_t)gridDim.x * nw) {
@@ -164,7 +187,7 @@ __global__ void __launch_bounds__(256) scatter_copy_kernel(
       const int r = scatter_index[p];
       int d = -1;
       if (r >= 0) {
-        d = base[c * E + e] + r;
+        d = off[e] + base[c * E + e] + r;
         row_token[d] = (int32_t)t;
       }
       scatter_index[p] = d;
@@ -200,15 +223,20 @@ __global__ void __launch_bounds__(256) scatter_copy_kernel(
 //     through row_token): one thread per (token, slot) pair.
 __global__ void __launch_bounds__(256) scatter_index_kernel(
     const int32_t* __restrict__ idx, int64_t npairs, int k, int E, int tpc,
-    const int32_t* __restrict__ base, int32_t* __restrict__ scatter_index,
+    const int32_t* __restrict__ base, const int32_t* __restrict__ counts,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ scatter_index,
     int32_t* __restrict__ row_token) {
+  extern __shared__ int32_t sm[];
+  int32_t* off = sm;                        // [E + 1]
+  block_offsets(counts, E, off, sm + E + 1, offsets);
   for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p < npairs;
        p += (int64_t)gridDim.x * blockDim.x) {
     const int64_t t = p / k;
     const int r = scatter_index[p];
     int d = -1;
     if (r >= 0) {
-      d = base[(t / tpc) * E + idx[p]] + r;
+      const int e = idx[p];
+      d = off[e] + base[(t / tpc) * E + e] + r;
       row_token[d] = (int32_t)t;
     }
     scatter_index[p] = d;
@@ -368,39 +396,52 @@ cudaError_t launch_permute_scratch(const Shape& s, int nchunks, int tpc, int32_t
     count_launch();
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
-  int S = 1;
-  if (s.E <= 1024 && nchunks > 0) S = 1024 / s.E < nchunks ? 1024 / s.E : nchunks;
-  const size_t ssm = (size_t)S * s.E * 4;
-  if (ssm > 48 * 1024) {
-    e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ssm);
-    if (e != cudaSuccess) return e;
-  }
-  scan_kernel<<<1, 1024, ssm, st>>>(hist, nchunks, s.E, S, base, counts, offsets);
+  scan_kernel<<<(unsigned)((s.E + 31) / 32), 1024, 0, st>>>(hist, nchunks, s.E, base, counts,
+                                                             offsets);
   count_launch();
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (nchunks == 0) return cudaSuccess;
+  // the scatter kernels hold the E + 1 group offsets and 32 warp sums in
+  // shared memory (the copy kernel also k rows a warp)
+  const size_t osm = ((size_t)s.E + 1 + 32) * 4;
   if (x_perm == nullptr) {
     const int64_t np = s.T * s.k;
     int64_t blocks = (np + 255) / 256;
     const int64_t cap = (int64_t)sm_count_cached() * 16;
     if (blocks > cap) blocks = cap;
-    scatter_index_kernel<<<(unsigned)blocks, 256, 0, st>>>(topk_idx, np, s.k, s.E, tpc, base,
-                                                            scatter_index, row_token);
+    if (osm > 48 * 1024) {
+      e = cudaFuncSetAttribute(scatter_index_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)osm);
+      if (e != cudaSuccess) return e;
+    }
+    scatter_index_kernel<<<(unsigned)blocks, 256, osm, st>>>(topk_idx, np, s.k, s.E, tpc, base,
+                                                              counts, offsets, scatter_index,
+                                                              row_token);
     count_launch();
     return cudaGetLastError();
   }
-  const size_t csm = (size_t)8 * s.k * 4;
+  const size_t csm = osm + (size_t)8 * s.k * 4;
   int64_t blocks = (s.T + 7) / 8;
   const int64_t cap = (int64_t)sm_count_cached() * 8;
   if (blocks > cap) blocks = cap;
   if (s.dtype == MOE_F32) {
+    if (csm > 48 * 1024) {
+      e = cudaFuncSetAttribute(scatter_copy_kernel<float>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm);
+      if (e != cudaSuccess) return e;
+    }
     scatter_copy_kernel<float><<<(unsigned)blocks, 256, csm, st>>>(
-        reinterpret_cast<const float*>(x), topk_idx, s.T, s.k, s.E, s.H, tpc, base, scatter_index,
-        row_token, reinterpret_cast<float*>(x_perm));
+        reinterpret_cast<const float*>(x), topk_idx, s.T, s.k, s.E, s.H, tpc, base, counts,
+        offsets, scatter_index, row_token, reinterpret_cast<float*>(x_perm));
   } else {
+    if (csm > 48 * 1024) {
+      e = cudaFuncSetAttribute(scatter_copy_kernel<bf16>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csm);
+      if (e != cudaSuccess) return e;
+    }
     scatter_copy_kernel<bf16><<<(unsigned)blocks, 256, csm, st>>>(
-        reinterpret_cast<const bf16*>(x), topk_idx, s.T, s.k, s.E, s.H, tpc, base, scatter_index,
-        row_token, reinterpret_cast<bf16*>(x_perm));
+        reinterpret_cast<const bf16*>(x), topk_idx, s.T, s.k, s.E, s.H, tpc, base, counts, offsets,
+        scatter_index, row_token, reinterpret_cast<bf16*>(x_perm));
   }
   count_launch();
   return cudaGetLastError();
