@@ -54,8 +54,8 @@ NCU_TRAFFIC = {
     # SM-pair engine became the default for prefill-sized calls)
     "qwen3-30b-a3b-shape-T4096": {"bytes": 987034880, "kernel_hash": "483aa0cf870cd816"},
     # profiles/launches_deepseek-v3-shape-T8192.md (SM-pair engine; the launch
-    # of the first forward: 16 203 627 008 B read + 265 459 712 B written)
-    "deepseek-v3-shape-T8192": {"bytes": 16469086720, "kernel_hash": "ffbe1805de36f0da"},
+    # of the first forward: 16 117 852 416 B read + 266 108 928 B written)
+    "deepseek-v3-shape-T8192": {"bytes": 16383961344, "kernel_hash": "ed96c43966348175"},
 }
 
 
