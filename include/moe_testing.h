@@ -37,6 +37,14 @@ int32_t moe_testing_set_gemm_engine(int32_t engine);
  * depend on it. */
 int32_t moe_testing_set_fork_sms(int32_t sms);
 
+/* Per-group A maps of the tensor-core engines' grouped calls (the rows past
+ * a group's end in its last tile load as zeros, which lowers the tensor
+ * cores' power; used where the call is long and its groups small): 0 = the
+ * library's choice (default), 1 = every grouped call of those engines, -1 =
+ * none.  Applies to later calls from any thread; returns the previous
+ * setting.  Results do not depend on it. */
+int32_t moe_testing_set_zero_pad(int32_t mode);
+
 /* The router logits moe_route decides on: the router GEMM exactly as
  * moe_route runs it (same engine and K split), with the partial sums added in
  * the same order, written to logits [T, E + shared_gate] (fp32, device).

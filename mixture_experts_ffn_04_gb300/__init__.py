@@ -111,6 +111,7 @@ def lib():
         "moe_last_launch_count": (i32, []),
         "moe_testing_set_gemm_engine": (i32, [i32]),
         "moe_testing_set_fork_sms": (i32, [i32]),
+        "moe_testing_set_zero_pad": (i32, [i32]),
         "moe_get_route_stats": (i32, [P, P, ctypes.POINTER(u32)]),
         "moe_testing_router_logits": (i32, [S, P, P, P, P, sz, P]),
         "moe_testing_wait_probe": (i32, [P, i64, i32, P]),
@@ -370,6 +371,10 @@ def moe_testing_set_gemm_engine(engine: int) -> int:
 
 def moe_testing_set_fork_sms(sms: int) -> int:
     return int(lib().moe_testing_set_fork_sms(sms))
+
+
+def moe_testing_set_zero_pad(mode: int) -> int:
+    return int(lib().moe_testing_set_zero_pad(mode))
 
 
 # ---------------------------------------------------------------------------

@@ -623,6 +623,22 @@ static bool map_weights_kn(CUtensorMap* m, const void* ptr, int N, int K, int G,
 
 }  // namespace tcb
 
+// Per-group operand maps for other engines (the SM-pair forward GEMM's A
+// maps): the same kernel, launched on `st`.
+cudaError_t launch_group_maps(const CUtensorMap& baseA, const CUtensorMap& baseB, void* maps,
+                              const int32_t* offsets, int G, int64_t rows_bound, const void* A,
+                              int64_t lda_bytes, const void* B, int64_t ldb_bytes,
+                              cudaStream_t st) {
+  if (G <= 0) return cudaSuccess;
+  const int mg = G < 1024 ? G : 1024;
+  tcb::wgrad_maps_kernel<<<mg, 32, 0, st>>>(baseA, baseB, reinterpret_cast<CUtensorMap*>(maps),
+                                            offsets, G, rows_bound,
+                                            reinterpret_cast<const char*>(A), lda_bytes,
+                                            reinterpret_cast<const char*>(B), ldb_bytes);
+  count_launch();
+  return cudaGetLastError();
+}
+
 bool bwd_gemm_tc_ok(const BwdGemmArgs& a) {
   if (a.dtype != MOE_BF16 || tc::encode_fn() == nullptr) return false;
   // 16-byte TMA strides and base addresses, 8-column output pieces

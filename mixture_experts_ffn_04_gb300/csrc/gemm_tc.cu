@@ -85,6 +85,10 @@ struct TcArgs {
   int64_t a_rows;         // rows of gA (bound on gather values)
   bf16* pre;              // SwiGLU: also the pre-activations [rows, ldp] = [gate | up]
   int64_t ldp;
+  // grouped calls: group g's A map at amaps[2 g], spanning only the group's
+  // rows, so the rows of its last tile past the group load as zeros (less
+  // power in the tensor cores; the results do not change); NULL: tmA
+  const CUtensorMap* amaps;
 };
 
 // Tile -> (K split, group, m-tile, n-tile).  Within a split, tiles of one
@@ -264,11 +268,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int S = is_a ? SA : SB;
     int s = 0;
     uint32_t ph = 0, issued = 0, par = 0;
+    const CUtensorMap* acquired = nullptr;   // per-group map last made visible
     for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
       int ks, g, mt, nt;
       decode_tile(a, sched, tile, ks, g, mt, nt);
       const int64_t gbase = a.offsets ? a.offsets[g] : 0;
-      const int arow = (int)(gbase + (int64_t)mt * BM);
+      int arow = (int)(gbase + (int64_t)mt * BM);
+      const CUtensorMap* amap = &tmA;
+      if (is_a && a.amaps) {
+        amap = a.amaps + 2 * g;
+        arow = mt * BM;
+        if (amap != acquired) {   // written by the preceding kernel
+          asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(
+                           reinterpret_cast<uint64_t>(amap))
+                       : "memory");
+          acquired = amap;
+        }
+      }
       const int kb0 = ks * a.KB / a.ksplit, kb1 = (ks + 1) * a.KB / a.ksplit;
       bool ok = true;
       for (int kb = kb0; kb < kb1; ++kb) {
@@ -276,7 +292,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (!mbar_wait(is_a ? emptyA(s) : emptyB(s), ph ^ 1u, abort_flag)) { ok = false; break; }
         if (is_a) {
           mbar_expect_tx(fb, A_BYTES);
-          tma_load_2d(ringA + s * A_BYTES, &tmA, kb * BK, arow, fb);
+          tma_load_2d(ringA + s * A_BYTES, amap, kb * BK, arow, fb);
         } else {
           const uint32_t sb = ringB + s * B_BYTES;
           mbar_expect_tx(fb, B_BYTES);
@@ -556,6 +572,11 @@ int router_split(int64_t rows, int ncols, int K) {
   return s < 1 ? 1 : (int)s;
 }
 
+cudaError_t launch_group_maps(const CUtensorMap& baseA, const CUtensorMap& baseB, void* maps,
+                              const int32_t* offsets, int G, int64_t rows_bound, const void* A,
+                              int64_t lda_bytes, const void* B, int64_t ldb_bytes,
+                              cudaStream_t st);   // gemm_bwd.cu
+
 cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   using namespace tc;
   if (a.dtype != MOE_BF16 || encode_fn() == nullptr) return cudaErrorNotSupported;
@@ -608,6 +629,14 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
   t.pre = reinterpret_cast<bf16*>(a.pre);
   t.ldp = a.ldp;
   if (t.pre && (a.mode != kSwiGLU || (a.ldp % 8) != 0)) return cudaErrorInvalidValue;
+  t.amaps = nullptr;
+  if (zero_pad_pays(a)) {
+    if ((reinterpret_cast<uintptr_t>(a.amaps) & 127) != 0) return cudaErrorInvalidValue;
+    e = launch_group_maps(mA, mA, a.amaps, a.offsets, a.G, a.rows_bound, a.A, (int64_t)a.K * 2,
+                          a.A, (int64_t)a.K * 2, st);
+    if (e != cudaSuccess) return e;
+    t.amaps = reinterpret_cast<const CUtensorMap*>(a.amaps);
+  }
   int64_t mt_bound = a.offsets ? (a.rows_bound + BM - 1) / BM + a.G : (a.single_rows + BM - 1) / BM;
   if (a.offsets && mt_bound > a.rows_bound) mt_bound = a.rows_bound;  // >= 1 row per tile
   const int64_t tiles_bound = mt_bound * t.NT * t.ksplit;

@@ -106,6 +106,12 @@ struct Args {
   void* out;
   int64_t ldo;
   uint32_t* flags;
+  // grouped calls: group g's A maps at amaps[2 g] (BMC-row box) and
+  // amaps[2 g + 1] (BMC / 2 rows), spanning only the group's rows, so the
+  // padding rows of its last tile load as zeros (less power in the tensor
+  // cores than the next group's rows; the results do not change); NULL: the
+  // global maps
+  const CUtensorMap* amaps;
 };
 
 // Pair tile -> (group, pair m-tile, n-tile), pair m-tiles of BMP rows; within
@@ -257,6 +263,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int s = 0;
     uint32_t ph = 0, issued = 0, par = 0;
     bool ok = true;
+    const CUtensorMap* acquired = nullptr;   // per-group map last made visible
     for (int64_t n = 0; ok; ++n) {
       const int64_t tile = next_tile(n, is_a && leader);
       if (tile < 0) break;
@@ -265,7 +272,19 @@ __global__ void __launch_bounds__(THREADS, 1)
       kb_range((int)(tile % ks), kb0, kb1);
       const int64_t gbase = a.offsets ? a.offsets[g] : 0;
       const bool half = tile_rows_left(a, g, mp) <= BMC;
-      const int arow = (int)(gbase + (int64_t)mp * BMP + (int64_t)rank * (half ? BMC / 2 : BMC));
+      const int64_t local = (int64_t)mp * BMP + (int64_t)rank * (half ? BMC / 2 : BMC);
+      const CUtensorMap* amap = half ? &tmA64 : &tmA;
+      int arow = (int)(gbase + local);
+      if (is_a && a.amaps) {
+        amap = a.amaps + 2 * g + (half ? 1 : 0);
+        arow = (int)local;
+        if (amap != acquired) {   // written by the preceding kernel
+          asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(
+                           reinterpret_cast<uint64_t>(amap))
+                       : "memory");
+          acquired = amap;
+        }
+      }
       const int brow = b_row(nt);
       for (int kb = kb0; kb < kb1; ++kb) {
         if (!wait2(empty(s), ph ^ 1u, abort_flag)) { ok = false; break; }
@@ -274,7 +293,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // even CTA's producers arrive on it (with the pair's byte count)
         const uint32_t fb = map_to_rank(full(s), 0);
         if (leader) mbar_expect_tx(full(s), 2 * (is_a ? (half ? A_BYTES / 2 : A_BYTES) : B_BYTES));
-        if (is_a) tma_load_2d_pair(st, half ? &tmA64 : &tmA, kb * BK, arow, fb);
+        if (is_a) tma_load_2d_pair(st, amap, kb * BK, arow, fb);
         else tma_load_3d_pair(st + A_BYTES, bmap, kb * BK, brow, g, fb);
         issued |= 1u << s;
         par = (par & ~(1u << s)) | (ph << s);
@@ -564,6 +583,11 @@ __global__ void __launch_bounds__(256) split_reduce_kernel(const float* __restri
 
 }  // namespace tc2
 
+cudaError_t launch_group_maps(const CUtensorMap& baseA, const CUtensorMap& baseB, void* maps,
+                              const int32_t* offsets, int G, int64_t rows_bound, const void* A,
+                              int64_t lda_bytes, const void* B, int64_t ldb_bytes,
+                              cudaStream_t st);   // gemm_bwd.cu
+
 cudaError_t launch_gemm_tc2(const GemmArgs& a, cudaStream_t st) {
   using namespace tc2;
   if (a.dtype != MOE_BF16 || a.mode == kStoreF32 || a.ksplit != 1 || a.gather || a.wfmt)
@@ -610,6 +634,14 @@ cudaError_t launch_gemm_tc2(const GemmArgs& a, cudaStream_t st) {
   t.out = a.out;
   t.ldo = a.ldo;
   t.flags = a.flags;
+  t.amaps = nullptr;
+  if (zero_pad_pays(a)) {
+    if ((reinterpret_cast<uintptr_t>(a.amaps) & 127) != 0) return cudaErrorInvalidValue;
+    e = launch_group_maps(mA, mA64, a.amaps, a.offsets, a.G, a.rows_bound, a.A, (int64_t)a.K * 2,
+                          a.A, (int64_t)a.K * 2, st);
+    if (e != cudaSuccess) return e;
+    t.amaps = reinterpret_cast<const CUtensorMap*>(a.amaps);
+  }
   int64_t mt_bound = a.offsets ? (a.rows_bound + BMP - 1) / BMP + a.G : (a.single_rows + BMP - 1) / BMP;
   if (a.offsets && mt_bound > a.rows_bound) mt_bound = a.rows_bound;
   const int64_t tiles_bound = mt_bound * t.NT;

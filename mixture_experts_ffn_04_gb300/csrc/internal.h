@@ -85,11 +85,29 @@ struct GemmArgs {
   int64_t ldp = 0;                  // gate at pre[r, n], up at pre[r, N + n]
   int wfmt = 0;                     // 1: B0/B1 are packed MXFP8 [N, K] matrices,
                                     // bstride in bytes
+  void* amaps = nullptr;            // SM-pair engine, grouped calls: scratch for
+                                    // 2 * G tensor maps (per-group A maps, so the
+                                    // rows past a group's end load as zeros)
   int max_sms = 0;                  // > 0: the call's CTAs stay within this many
                                     // SMs' worth (decode and one-SM tensor-core
                                     // engines), leaving the rest to a concurrent
                                     // stream
 };
+
+// Per-group A maps (a.amaps: the padding rows of a group's last tile load as
+// zeros instead of the next group's rows) lower the tensor cores' power; that
+// pays where a call runs long enough for the power cap to set the SM clock
+// and its groups are small enough for the padding to be a real share of the
+// MMA work.  Layer A/B on one box: DeepSeek-V3 shape (256-row groups, 1e12
+// MAC a call) -3 %; Qwen3 and Gemma-4 shapes (5e10) +2 % from the map
+// launches; Zipf routing (1536 rows a group) neutral.
+int zero_pad_override();   // moe_testing_set_zero_pad: 0 auto, 1 always, -1 never
+inline bool zero_pad_pays(const GemmArgs& a) {
+  if (a.amaps == nullptr || a.offsets == nullptr || a.gather != nullptr || a.G <= 1) return false;
+  const int ov = zero_pad_override();
+  if (ov != 0) return ov > 0;
+  return (double)a.rows_bound * a.K * a.N >= 2.75e11 && a.rows_bound / a.G < 1024;
+}
 
 cudaError_t launch_grouped_gemm(const GemmArgs& a, cudaStream_t st);
 cudaError_t launch_gemm_simt(const GemmArgs& a, int bm, cudaStream_t st);

@@ -19,10 +19,12 @@ static thread_local int tl_launches = 0;
 static thread_local const char* tl_error = "";
 static std::atomic<int> g_engine{0};
 static std::atomic<int> g_fork_sms{0};   // moe_testing_set_fork_sms
+static std::atomic<int> g_zero_pad{0};   // moe_testing_set_zero_pad
 
 void count_launch(int n) { tl_launches += n; }
 void reset_launch_count() { tl_launches = 0; }
 int gemm_path_override() { return g_engine.load(); }
+int zero_pad_override() { return g_zero_pad.load(); }
 
 void set_error_message(const char* why) { tl_error = why; }
 
@@ -511,6 +513,7 @@ static moe_status grouped(int mode, const moe_shape* shape, const void* A, const
   a.ldo = a.N;
   a.sched = reinterpret_cast<int32_t*>(w + (G > 1 ? L.sched_routed : L.sched_shared));
   a.ctr = reinterpret_cast<int32_t*>(w + L.tile_ctr + (G > 1 ? 0 : 128));
+  if (G > 1 && G <= s.E) a.amaps = w + L.tmaps;
   a.flags = reinterpret_cast<uint32_t*>(w + L.flags);
   a.gather = gather;
   a.a_rows = s.T;
@@ -747,6 +750,7 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
   a.rows_bound = s.T * s.k;
   a.sched = reinterpret_cast<int32_t*>(w + L.sched_routed);
   a.ctr = reinterpret_cast<int32_t*>(w + L.tile_ctr);
+  a.amaps = w + L.tmaps;
   a.flags = flags;
   a.wfmt = s.wfmt;
   a.mode = kSwiGLU;
@@ -864,6 +868,11 @@ int32_t moe_last_launch_count(void) { return tl_launches; }
 int32_t moe_testing_set_gemm_engine(int32_t engine) {
   if (engine < 0 || engine > 4) engine = 0;
   return g_engine.exchange(engine);
+}
+
+int32_t moe_testing_set_zero_pad(int32_t mode) {
+  if (mode < -1 || mode > 1) mode = 0;
+  return g_zero_pad.exchange(mode);
 }
 
 int32_t moe_testing_set_fork_sms(int32_t sms) {

@@ -263,7 +263,9 @@ def test_sm_pair_engine_matches_one_sm_engine(groups):
     y_perm bit for bit: the same fp32 sums in the same k order, one rounding.
     Ragged N and K (N = 200, K = 328), empty groups, groups of one tile and
     of one row past a tile, and groups whose last tile has 1, 128 and 129
-    rows (half tile, half tile, full tile)."""
+    rows (half tile, half tile, full tile).  Both engines also give the same
+    bits with per-group A maps (the rows past a group's end load as zeros)
+    as with the global map (they load the next group's rows)."""
     G = len(groups)
     rows = sum(groups)
     H, I = 328, 200
@@ -277,21 +279,26 @@ def test_sm_pair_engine_matches_one_sm_engine(groups):
     wu = (torch.randn(G, I, H, device="cuda", generator=g) * 0.05).bfloat16()
     wd = (torch.randn(G, H, I, device="cuda", generator=g) * 0.05).bfloat16()
     out = {}
-    for e in (2, 4):
-        h = torch.full((rows, I), float("nan"), device="cuda").bfloat16()
-        yp = torch.full((rows, H), float("nan"), device="cuda").bfloat16()
-        prev = m.moe_testing_set_gemm_engine(e)
-        try:
-            m.moe_grouped_swiglu(s, xp, wg, wu, I * H, offs, G, rows, I, h, ws)
-            m.moe_grouped_down(s, h, wd, H * I, offs, G, rows, I, yp, ws)
-        finally:
-            m.moe_testing_set_gemm_engine(prev)
-        torch.cuda.synchronize()
-        assert m.moe_get_device_status(ws)[0] == m.MOE_OK
-        assert torch.isfinite(h.float()).all() and torch.isfinite(yp.float()).all()
-        out[e] = (h, yp)
-    assert torch.equal(out[2][0].view(torch.int16), out[4][0].view(torch.int16))
-    assert torch.equal(out[2][1].view(torch.int16), out[4][1].view(torch.int16))
+    for zp in (-1, 1):
+        for e in (2, 4):
+            h = torch.full((rows, I), float("nan"), device="cuda").bfloat16()
+            yp = torch.full((rows, H), float("nan"), device="cuda").bfloat16()
+            prev = m.moe_testing_set_gemm_engine(e)
+            prev_zp = m.moe_testing_set_zero_pad(zp)
+            try:
+                m.moe_grouped_swiglu(s, xp, wg, wu, I * H, offs, G, rows, I, h, ws)
+                m.moe_grouped_down(s, h, wd, H * I, offs, G, rows, I, yp, ws)
+            finally:
+                m.moe_testing_set_gemm_engine(prev)
+                m.moe_testing_set_zero_pad(prev_zp)
+            torch.cuda.synchronize()
+            assert m.moe_get_device_status(ws)[0] == m.MOE_OK
+            assert torch.isfinite(h.float()).all() and torch.isfinite(yp.float()).all()
+            out[(zp, e)] = (h, yp)
+    ref = out[(-1, 2)]
+    for key, (h, yp) in out.items():
+        assert torch.equal(ref[0].view(torch.int16), h.view(torch.int16)), key
+        assert torch.equal(ref[1].view(torch.int16), yp.view(torch.int16)), key
 
 
 def test_zero_tokens_is_a_no_op():
