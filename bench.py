@@ -50,12 +50,12 @@ METRIC = "MoE layer tokens/s and grouped-GEMM TFLOP/s (% bf16 peak) on 1 GB300"
 # launch, from an ncu capture, keyed by workload; valid only while the device
 # code of the engine that ran it hashes to the recorded value.
 NCU_TRAFFIC = {
-    # profiles/launches_qwen3-30b-a3b-shape-T4096.md (one-SM engine, before the
-    # SM-pair engine became the default for prefill-sized calls)
-    "qwen3-30b-a3b-shape-T4096": {"bytes": 987034880, "kernel_hash": "483aa0cf870cd816"},
+    # profiles/launches_qwen3-30b-a3b-shape-T4096.md (one-SM engine: K = 2048
+    # and 128-row groups keep this layer off the SM-pair engine; first forward)
+    "qwen3-30b-a3b-shape-T4096": {"bytes": 984390656, "kernel_hash": "7d2ea5ed3b98bf80"},
     # profiles/launches_deepseek-v3-shape-T8192.md (SM-pair engine; the launch
-    # of the first forward: 16 117 852 416 B read + 266 108 928 B written)
-    "deepseek-v3-shape-T8192": {"bytes": 16383961344, "kernel_hash": "ed96c43966348175"},
+    # of the first forward: 16 105 838 336 B read + 265 489 152 B written)
+    "deepseek-v3-shape-T8192": {"bytes": 16371327488, "kernel_hash": "ca189116ee311b94"},
 }
 
 

@@ -504,13 +504,14 @@ __global__ void __launch_bounds__(THREADS, 1)
   if (threadIdx.x == 0 && *abort_flag) set_flag(a.flags, kFlagTimeout);
 }
 
-// Per-group copies of the weight gradient's two operand maps: group g's maps
-// start at its first row and span its rows (at least one, so the map stays
-// valid for a group without rows, whose tiles load nothing).  One warp per
+// Per-group copies of two operand maps (the weight gradient's A and B; the
+// forward GEMMs' A maps of two box heights): group g's maps start at its
+// first row and span its rows (at least one, so the map stays valid for a
+// group without rows, whose tiles load nothing).  One warp per
 // group: copy the base map to shared memory, replace the base address and the
 // row extent (dimension 1), and copy it out with the proxy fence that makes
 // it visible to the TMA unit.
-__global__ void __launch_bounds__(32) wgrad_maps_kernel(const __grid_constant__ CUtensorMap baseA,
+__global__ void __launch_bounds__(32) group_maps_kernel(const __grid_constant__ CUtensorMap baseA,
                                                         const __grid_constant__ CUtensorMap baseB,
                                                         CUtensorMap* maps, const int32_t* offsets,
                                                         int G, int64_t rows_bound,
@@ -631,7 +632,7 @@ cudaError_t launch_group_maps(const CUtensorMap& baseA, const CUtensorMap& baseB
                               cudaStream_t st) {
   if (G <= 0) return cudaSuccess;
   const int mg = G < 1024 ? G : 1024;
-  tcb::wgrad_maps_kernel<<<mg, 32, 0, st>>>(baseA, baseB, reinterpret_cast<CUtensorMap*>(maps),
+  tcb::group_maps_kernel<<<mg, 32, 0, st>>>(baseA, baseB, reinterpret_cast<CUtensorMap*>(maps),
                                             offsets, G, rows_bound,
                                             reinterpret_cast<const char*>(A), lda_bytes,
                                             reinterpret_cast<const char*>(B), ldb_bytes);
@@ -689,7 +690,7 @@ cudaError_t launch_bwd_gemm_tc(const BwdGemmArgs& a, cudaStream_t st) {
     if (a.tmaps == nullptr) return cudaErrorInvalidValue;
     t.tmaps = reinterpret_cast<const CUtensorMap*>(a.tmaps);
     const int mg = a.G < 1024 ? a.G : 1024;
-    wgrad_maps_kernel<<<mg, 32, 0, st>>>(mA, mB0, reinterpret_cast<CUtensorMap*>(a.tmaps),
+    group_maps_kernel<<<mg, 32, 0, st>>>(mA, mB0, reinterpret_cast<CUtensorMap*>(a.tmaps),
                                          a.offsets, a.G, a.rows_bound,
                                          reinterpret_cast<const char*>(a.A), a.lda * 2,
                                          reinterpret_cast<const char*>(a.B0), a.ldb * 2);
