@@ -52,10 +52,10 @@ METRIC = "MoE layer tokens/s and grouped-GEMM TFLOP/s (% bf16 peak) on 1 GB300"
 NCU_TRAFFIC = {
     # profiles/launches_qwen3-30b-a3b-shape-T4096.md (one-SM engine: K = 2048
     # and 128-row groups keep this layer off the SM-pair engine; first forward)
-    "qwen3-30b-a3b-shape-T4096": {"bytes": 984390656, "kernel_hash": "7d2ea5ed3b98bf80"},
+    "qwen3-30b-a3b-shape-T4096": {"bytes": 984256000, "kernel_hash": "7d2ea5ed3b98bf80"},
     # profiles/launches_deepseek-v3-shape-T8192.md (SM-pair engine; the launch
-    # of the first forward: 16 105 838 336 B read + 265 489 152 B written)
-    "deepseek-v3-shape-T8192": {"bytes": 16371327488, "kernel_hash": "ca189116ee311b94"},
+    # of the first forward: 16 141 321 728 B read + 265 451 264 B written)
+    "deepseek-v3-shape-T8192": {"bytes": 16406772992, "kernel_hash": "ca189116ee311b94"},
 }
 
 
