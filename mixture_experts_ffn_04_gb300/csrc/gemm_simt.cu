@@ -551,7 +551,11 @@ cudaError_t launch_skinny_t(const GemmArgs& a, int R, int smem_sched, cudaStream
   while (ks < kSkW && base_warps * ks < 2432) ks *= 2;
   const int cols_per_block = (kSkW / ks) * kSkC;
   dim3 grid((unsigned)mt_bound, (unsigned)((a.N + cols_per_block - 1) / cols_per_block));
-  if (a.max_sms > 0) {   // resident blocks an SM: the kernel's launch bounds
+  if (a.max_sms > 0) {
+    // held to max_sms SMs (resident blocks an SM: the launch bounds): the
+    // blocks loop over the column blocks.  (Fewer blocks taking the same
+    // number of rounds measured slower here: a block's weight stream is
+    // latency-bound, so fewer blocks pull less bandwidth.)
     const int per_sm = R == 1 ? (a.mode == kSwiGLU ? 2 : 3) : 1;
     const int64_t cap = (int64_t)a.max_sms * per_sm / (int64_t)grid.x;
     if (cap < (int64_t)grid.y) grid.y = (unsigned)(cap > 0 ? cap : 1);

@@ -654,7 +654,12 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, cudaStream_t st) {
     }
   }
   const int sms = a.max_sms > 0 && a.max_sms < sm_count() ? a.max_sms : sm_count();
-  const int grid = (int)(tiles_bound < sms ? tiles_bound : sms);
+  int grid = (int)(tiles_bound < sms ? tiles_bound : sms);
+  if (a.max_sms > 0 && tiles_bound > grid) {
+    // held to max_sms SMs: the fewest CTAs that take the same rounds of tiles
+    const int64_t rounds = (tiles_bound + grid - 1) / grid;
+    grid = (int)((tiles_bound + rounds - 1) / rounds);
+  }
   tc_gemm_kernel<<<grid, THREADS, SMEM_BYTES, st>>>(mA, mB0, mB1, t);
   count_launch();
   return cudaGetLastError();
