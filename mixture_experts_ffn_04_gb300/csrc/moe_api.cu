@@ -256,8 +256,11 @@ static int engine_for(const GemmArgs& a) {
   // ahead for one big group (the shared MLP), for large routed groups
   // (all-to-one and Zipf routing) and for long reductions (K = 3584, 7168),
   // 5 % behind on short ones (the Qwen3- and Gemma-4-shaped layers, K <= 2816,
-  // whose tiles are too short for the pair's per-tile hand-offs).
-  if (pair_ok && rows >= 512 && (a.G == 1 || rows / a.G >= 1024 || a.K >= 3072)) return 4;
+  // whose tiles are too short for the pair's per-tile hand-offs), and behind
+  // for small grouped calls whatever K (768 rows at K = 4096, all-to-one and
+  // Zipf routing at T = 128: 122 -> 120 and 414 -> 399 us a layer).
+  if (pair_ok && rows >= 512 && (a.G == 1 || rows / a.G >= 1024 || (a.K >= 3072 && rows > 2048)))
+    return 4;
   // a few-tile one-group gate/up the layer gives a K-split buffer: the pair
   // engine splits K until its clusters are busy
   if (pair_ok && a.split_part) return 4;
