@@ -49,6 +49,10 @@ METRIC = "MoE layer tokens/s and grouped-GEMM TFLOP/s (% bf16 peak) on 1 GB300"
 # dram__bytes_read.sum + dram__bytes_write.sum of one gate/up grouped-GEMM
 # launch, from an ncu capture, keyed by workload; valid only while the device
 # code of the engine that ran it hashes to the recorded value.
+# Nominal HBM3e bandwidth of a GB300 (the fractions against it sit beside the
+# ones against the measured copy bandwidth).
+NOMINAL_HBM_GBS = 7900.0
+
 NCU_TRAFFIC = {
     # profiles/launches_qwen3-30b-a3b-shape-T4096.md (one-SM engine: K = 2048
     # and 128-row groups keep this layer off the SM-pair engine; first forward)
@@ -470,6 +474,8 @@ def measure_layer(m, wl, inputs, steps, warmup, flush, peaks, dist, use_graph=Tr
         "rpc_frac_hbm": rpc_floor_ms / rpc_ms if rpc_ms > 0 else None,
         "rpc": {"ms": rpc_ms, "algorithmic_bytes": rpc_bytes, "floor_ms": rpc_floor_ms,
                 "achieved_gbs": rpc_bytes / (rpc_ms / 1000.0) / 1e9 if rpc_ms > 0 else None,
+                "frac_nominal_hbm": (rpc_bytes / (rpc_ms / 1000.0) / 1e9 / NOMINAL_HBM_GBS
+                                     if rpc_ms > 0 else None),
                 "route_bytes": alg["route_bytes"], "permute_bytes": alg["permute_bytes"],
                 "combine_bytes": alg["combine_bytes"],
                 "what": "route (router GEMM + top-k) + permute + combine stage times "
@@ -494,7 +500,7 @@ def gate_up_roofline(wl, alg, gu_ms, peaks):
     else:
         ach = alg["gu_bytes"] / (gu_ms / 1000.0) / 1e9
         roof = {"bound": "hbm", "achieved": ach, "peak": peaks["hbm"], "unit": "GB/s",
-                "frac": ach / peaks["hbm"]}
+                "frac": ach / peaks["hbm"], "frac_nominal": ach / NOMINAL_HBM_GBS}
     tr = NCU_TRAFFIC.get(wl.name)
     roof["kernel"] = gate_up_kernel_name(wl)
     engine = roof["kernel"].split(" ")[0]
