@@ -3,8 +3,9 @@
  *
  * The bf16 grouped GEMMs have four engines: tensor-core tiles (tcgen05,
  * 128 x 256 tiles), the same on SM pairs (256 x 256 tiles, cta_group::2, the
- * default for calls of at least 512 rows; a group's last tile of at most 128
- * rows runs at M = 128), a skinny
+ * default for calls of at least 512 rows that are one group, average 1024
+ * rows a group, or have more than 2048 rows and K >= 3072; a group's last
+ * tile of at most 128 rows runs at M = 128), a skinny
  * weight-streaming engine (decode-sized calls, up to 4 rows) and CUDA-core
  * tiles.  Parity tests pin each engine against the oracle by
  * forcing it for a run of calls.
