@@ -331,11 +331,12 @@ moe_status moe_combine(const moe_shape *shape, const void *y_perm,
  * routes_idx/routes_w [T, k] (device) replace the router when non-NULL
  * (duplicates allowed); weights->router may then be NULL, and shared_gate
  * must be 0.  ws_bytes >= moe_workspace_bytes(shape).
- * At decode sizes (T <= 64, with a shared MLP) the shared MLP runs on a
- * second stream of the library's, forked from `stream` after the input
- * preparation and joined back before the combine (inside a stream capture
- * this becomes a branch of the graph).  That stream and its two events are
- * made on the first such call on a device: make it before any capture.
+ * With a shared MLP, the shared MLP runs on a second stream of the
+ * library's, forked from `stream` after the input preparation and joined back
+ * before the combine (inside a stream capture this becomes a branch of the
+ * graph); at decode sizes (T <= 64) its GEMMs are held to part of the SMs.
+ * That stream and its two events are made on the first such call on a
+ * device: make it before any capture.
  * moe_layer_forward_traced keeps every stage on `stream`. */
 moe_status moe_layer_forward(const moe_shape *shape, const moe_weights *weights,
                              const void *x, const int32_t *routes_idx,

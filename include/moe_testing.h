@@ -31,9 +31,10 @@ extern "C" {
 int32_t moe_testing_set_gemm_engine(int32_t engine);
 
 /* How many SMs' worth of CTAs the shared MLP's GEMMs may take when
- * moe_layer_forward runs them on its second stream (decode sizes), leaving
- * the other SMs free for the routed chain on the caller's stream: 0 = the
- * library's choice (default), -1 = all SMs, n > 0 = n SMs.  Applies to later
+ * moe_layer_forward runs them on its second stream, leaving the other SMs
+ * free for the routed chain on the caller's stream: 0 = the library's choice
+ * (default: 96 at decode sizes, all at prefill sizes), -1 = all SMs, n > 0 =
+ * n SMs.  Applies to later
  * calls from any thread; returns the previous setting.  Results do not
  * depend on it. */
 int32_t moe_testing_set_fork_sms(int32_t sms);

@@ -100,6 +100,8 @@ struct Args {
   // the real tile count; partial sums to part [split][row][NT * 256] (fp32),
   // the number of splits to *ks_out; part == NULL: no split
   int ksmax;
+  int ks_clusters;   // clusters the split count is sized for: all the GPU
+                     // holds, so a call held to fewer SMs sums in the same order
   float* part;
   int64_t part_ld, part_stride;
   int32_t* ks_out;
@@ -209,7 +211,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int64_t tiles1 = (int64_t)sched[a.G] * a.NT;
   int ks = 1;
   if (a.part != nullptr) {
-    int64_t k = tiles1 > 0 ? ncl / tiles1 : 1;
+    int64_t k = tiles1 > 0 ? (int64_t)a.ks_clusters / tiles1 : 1;
     if (k > a.ksmax) k = a.ksmax;
     if (k > a.KB / 4) k = a.KB / 4;
     ks = k < 1 ? 1 : (int)k;
@@ -673,8 +675,11 @@ cudaError_t launch_gemm_tc2(const GemmArgs& a, cudaStream_t st) {
   }
   const int mc = max_clusters[dev].load();
   if (mc < 0) return cudaErrorNotSupported;
-  // a K split needs every cluster there is (it splits until they are busy)
-  const int64_t ncl = (t.part || tiles_bound >= mc) ? mc : tiles_bound;
+  // a K split needs every cluster there is (it splits until they are busy);
+  // a call held to max_sms SMs takes at most max_sms / 2 clusters
+  t.ks_clusters = mc;
+  int64_t ncl = (t.part || tiles_bound >= mc) ? mc : tiles_bound;
+  if (a.max_sms > 0 && ncl > a.max_sms / 2) ncl = a.max_sms / 2 > 0 ? a.max_sms / 2 : 1;
   cfg.gridDim = dim3((unsigned)(2 * ncl));
   e = cudaLaunchKernelEx(&cfg, tc2_gemm_kernel, mA, mA64, mB0, mB1, t);
   if (e != cudaSuccess) return e;

@@ -30,20 +30,23 @@ void set_error_message(const char* why) { tl_error = why; }
 
 static size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
-// The layer forward's second stream (the shared MLP at decode sizes) and its
-// fork/join events, one set per device, made on first use; the mutex is held
-// from the fork to the join's enqueue so that concurrent callers never see
-// each other's event records.
-constexpr int64_t kForkMaxT = 64;
-// SMs the forked shared MLP's GEMMs may fill.  Left to themselves they take
-// every SM and the routed chain's short launches queue behind their CTAs;
-// held to 96 of the 152 the two streams overlap (Qwen2-MoE shape, graph
-// replay: T = 1 145 -> 133 us, T = 16 447 -> 422, T = 64 617 -> 584, T = 8
-// unchanged within noise; 32-64 SMs starve the shared MLP instead).
+// The layer forward's second stream (the shared MLP) and its fork/join
+// events, one set per device, made on first use; the mutex is held from the
+// fork to the join's enqueue so that concurrent callers never see each
+// other's event records.
+constexpr int64_t kForkMaxT = 64;   // decode sizes: the shared MLP held to fewer SMs
+// SMs the forked shared MLP's GEMMs may fill at decode sizes.  Left to
+// themselves they take every SM and the routed chain's short launches queue
+// behind their CTAs; held to 96 of the 152 the two streams overlap (Qwen2-MoE
+// shape, graph replay: T = 1 145 -> 133 us, T = 16 447 -> 422, T = 64 617 ->
+// 584, T = 8 unchanged within noise; 32-64 SMs starve the shared MLP
+// instead).  At prefill sizes the shared MLP takes whatever SMs are free:
+// caps of 60-140 SMs measured slower there.
 constexpr int kForkSharedSms = 96;
-static int fork_shared_sms() {
+static int fork_shared_sms(int64_t T) {
   const int v = g_fork_sms.load();
-  return v < 0 ? 0 : (v > 0 ? v : kForkSharedSms);
+  if (v != 0) return v < 0 ? 0 : v;
+  return T <= kForkMaxT ? kForkSharedSms : 0;
 }
 struct SideStream {
   cudaStream_t stream = nullptr;
@@ -154,8 +157,9 @@ moe_status decode_shape(const moe_shape* s, Shape* o, const char** why) {
 
 // The shared MLP's gate/up takes the SM-pair engine's K split when its pair
 // tiles (256-row m-tiles x 128-column n-tiles) would leave most of the SMs
-// idle: bf16, no MXFP8 weights, prefill-sized (decode sizes run on their own
-// stream), at most kSplitMaxTiles tiles.  Routed calls do not split: their
+// idle: bf16, no MXFP8 weights, prefill-sized (at decode sizes the shared
+// MLP's weight stream is held to part of the SMs instead), at most
+// kSplitMaxTiles tiles.  Routed calls do not split: their
 // group sizes are known on the device only, and where they are few-tile (all
 // routes on one expert at T = 128) the fp32 partials of a 2I-wide SwiGLU
 // accumulator cost more than the split saves (gate/up 37 -> 48 us, measured).
@@ -654,11 +658,15 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
     CHECK_CUDA(launch_rmsnorm(s, x, W->norm_weight, s.norm_eps, w + L.x_norm, st));
     xin = w + L.x_norm;
   }
-  // The shared MLP depends on xin alone.  At decode sizes its weight stream
-  // runs on a second stream, forked here and joined before the combine, so it
-  // overlaps the routing, permute and routed GEMMs, which at a few tokens are
-  // short latency-bound launches that leave HBM idle.  (The traced entry point
-  // keeps one stream, so its stage events time each stage alone.)
+  // The shared MLP depends on xin alone, so it runs on a second stream,
+  // forked here and joined before the combine, beside the routing, permute
+  // and routed GEMMs.  At decode sizes those are short latency-bound launches
+  // that leave HBM idle; at prefill sizes the HBM-bound stages (route,
+  // permute) leave power and tensor cores for the shared MLP's GEMMs under
+  // the power cap (graph replay, one box: Qwen2-MoE T = 2048 1180 -> 1112
+  // us, DeepSeek-V3 shape 5910 -> 5877, adversarial T = 16384 -1 to -2 %).
+  // (The traced entry point keeps one stream, so its stage events time each
+  // stage alone.)
   void* sh_out = nullptr;
   int sh_split = 1;
   auto launch_shared = [&](cudaStream_t ss, int max_sms) -> cudaError_t {
@@ -707,7 +715,7 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
     }
     return launch_grouped_gemm(b, ss);
   };
-  const bool fork = s.I_sh && ev == nullptr && s.T <= kForkMaxT;
+  const bool fork = s.I_sh && ev == nullptr;
   SideStream* side = nullptr;
   std::unique_lock<std::mutex> side_lock;
   if (fork) {
@@ -715,7 +723,7 @@ moe_status moe_layer_forward_traced(const moe_shape* shape, const moe_weights* W
     side_lock = std::unique_lock<std::mutex>(side->mu);
     CHECK_CUDA(cudaEventRecord(side->fork, st));
     CHECK_CUDA(cudaStreamWaitEvent(side->stream, side->fork, 0));
-    CHECK_CUDA(launch_shared(side->stream, fork_shared_sms()));
+    CHECK_CUDA(launch_shared(side->stream, fork_shared_sms(s.T)));
     CHECK_CUDA(cudaEventRecord(side->join, side->stream));
   }
   STAGE_EVENT(MOE_STAGE_ROUTE);

@@ -436,14 +436,14 @@ def test_step_api_with_input_norm_and_residual():
     assert torch.equal(y.view(torch.int16), y_ref.view(torch.int16))
 
 
-@pytest.mark.parametrize("T", [1, 8, 64])
+@pytest.mark.parametrize("T", [1, 8, 64, 2048])
 def test_forked_shared_mlp_in_a_graph_matches_eager(T):
-    """At decode sizes the shared MLP runs on a second stream forked from and
-    joined back into the caller's stream.  The same forward captured in a CUDA
-    graph (the fork becomes a graph branch) gives the eager result bit for bit,
-    and the eager result equals the traced entry point's, which keeps one
-    stream."""
-    wl = W.get("qwen2-moe-shape-T%d" % T) if T in (1, 8, 64) else None
+    """The shared MLP runs on a second stream forked from and joined back into
+    the caller's stream (held to part of the SMs at decode sizes).  The same
+    forward captured in a CUDA graph (the fork becomes a graph branch) gives
+    the eager result bit for bit, and the eager result equals the traced entry
+    point's, which keeps one stream."""
+    wl = W.get("qwen2-moe-shape-T%d" % T)
     dev = W.make_inputs(wl, seed=4, device="cuda")
     layer = m.MoELayer(wl, dev)
     x = dev["x"]
@@ -467,12 +467,16 @@ def test_forked_shared_mlp_in_a_graph_matches_eager(T):
     assert torch.equal(y_eager.view(torch.int16), y_traced.view(torch.int16))
 
 
-@pytest.mark.parametrize("T", [1, 8, 64])
+@pytest.mark.parametrize("T", [1, 8, 64, 300, 2048])
 def test_forked_shared_mlp_sm_cap_keeps_results(T):
     """The shared MLP's GEMMs on the forked stream may be held to fewer SMs
-    (their CTAs then loop over the remaining column blocks or tiles); every
-    cap gives the uncapped result bit for bit."""
-    wl = W.get("qwen2-moe-shape-T%d" % T)
+    (their CTAs then loop over the remaining column blocks or tiles; the
+    SM-pair engine's K split, T = 300, keeps the split count of the whole
+    GPU); every cap gives the uncapped result bit for bit."""
+    if T == 300:
+        wl = W.small(W.QWEN2_MOE, T=300, H=512, I=256, I_sh=512)
+    else:
+        wl = W.get("qwen2-moe-shape-T%d" % T)
     dev = W.make_inputs(wl, seed=6, device="cuda")
     layer = m.MoELayer(wl, dev)
     prev = m.moe_testing_set_fork_sms(-1)
