@@ -58,8 +58,8 @@ NCU_TRAFFIC = {
     # and 128-row groups keep this layer off the SM-pair engine; first forward)
     "qwen3-30b-a3b-shape-T4096": {"bytes": 984256000, "kernel_hash": "7d2ea5ed3b98bf80"},
     # profiles/launches_deepseek-v3-shape-T8192.md (SM-pair engine; the launch
-    # of the first forward: 16 141 321 728 B read + 265 451 264 B written)
-    "deepseek-v3-shape-T8192": {"bytes": 16406772992, "kernel_hash": "ca189116ee311b94"},
+    # of the first forward: 16 206 901 504 B read + 265 844 224 B written)
+    "deepseek-v3-shape-T8192": {"bytes": 16472745728, "kernel_hash": "6468578d8bae2304"},
 }
 
 
